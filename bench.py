@@ -1,0 +1,499 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused DiT QK-RMSNorm + RoPE on the Wan-A14B shape.
+
+One step = one qknr_forward over the full Wan workload: a packed bf16 QKV
+activation [32760, 3*40*128] (a 21x30x52 latent grid), per-head RMSNorm of
+the 40 Q and 40 K heads (head_dim 128) with fp32 gains, then interleaved
+RoPE from a shared fp32 cos/sin row per token (3-axis 44/42/42 split),
+in place, V untouched.
+
+Prints one JSON line: microseconds per call (whole job), achieved HBM
+bandwidth against the measured copy peak, the CPU oracle's time on a
+bounded sample, an end-to-end number through the public Python API with
+host buffers, the SM clocks seen during the timed region and the launch
+count.  ``--impl reference`` times the fp64 CPU oracle instead.
+
+Multi-GPU: one process per GPU (torchrun); every rank runs its own full
+workload (replicas, weak scaling), timing is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from diffusion_transformer_qk_gb300 import inputs as I  # noqa: E402
+
+METRIC = "fused QK-RMSNorm+RoPE µs/call and achieved HBM GB/s (% of peak), Wan 40x128"
+UNIT = "us/call"
+DEFAULT_WORKLOAD = "wan_32760x40x128"
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ("qknr_kernel.cuh", "qknr_api.cu", "qknr_internal.h")
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas: barrier and max over ranks only)
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def dist_init(backend: str):
+    import torch.distributed as dist
+
+    rank, world, local = dist_env()
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        os.environ.setdefault("MASTER_PORT", "29511")
+        dist.init_process_group(backend, rank=rank, world_size=world)
+    return rank, world, local
+
+
+def barrier():
+    import torch.distributed as dist
+
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    """Largest value of x over all ranks (x itself when not distributed)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_us_per_call(max_elapsed_s: float, steps: int, world: int) -> float:
+    """Microseconds per call over the whole job: every rank made `steps`
+    calls inside the slowest rank's elapsed time."""
+    return max_elapsed_s * 1e6 / (steps * world)
+
+
+# ---------------------------------------------------------------------------
+# measured peaks, clocks, traffic record
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "diffusion_transformer_qk_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu record, if it was taken
+    on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f).get(workload)
+    except Exception:
+        return None
+    if not rec or rec.get("kernel_src_sha256") != kernel_source_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 100 ms."""
+
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown", "clocks_event_reasons.sw_thermal_slowdown",
+              "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, gpu_id: str):
+        self.samples = []
+        self.error = None
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", gpu_id, "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception as e:  # no nvidia-smi
+            self.error = str(e)
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == len(self.FIELDS):
+                self.samples.append((time.perf_counter(), parts))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float):
+        if self.error:
+            return {"error": self.error}
+        inside = [s for t, s in self.samples if t0 <= t <= t1]
+        note = "sampled during the timed region"
+        if not inside:
+            inside = [s for _, s in self.samples]
+            note = "timed region shorter than the 100 ms sampling period: samples span warm-up and timed steps"
+        mhz = []
+        reasons = set()
+        max_mhz = None
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for s in inside:
+            try:
+                mhz.append(float(s[0]))
+                max_mhz = float(s[1])
+            except ValueError:
+                pass
+            for n, v in zip(names, s[3:]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(mhz) if mhz else None, "sm_max_mhz": max_mhz,
+                "reasons": sorted(reasons), "samples": len(inside), "note": note}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing
+
+def oracle_rows(w, inp, rows):
+    """The oracle over the given token rows of one workload instance."""
+    from oracle import qknr_oracle as O
+
+    if w.packed:
+        return O.forward_packed(inp["qkv"], w.dtype, w.n_heads_q, w.n_heads_k, w.n_heads_v, w.head_dim,
+                                inp["gamma_q"], inp["gamma_k"], w.eps, inp["cos"], inp["sin"], w.cos_dtype,
+                                w.rope_style, "shared_row", rows=rows)
+    return [O.forward_separate(inp[n], w.dtype, h, w.head_dim, inp[g], w.eps, inp["cos"], inp["sin"],
+                               w.cos_dtype, w.rope_style, "shared_row", rows=rows)
+            for n, h, g in (("q", w.n_heads_q, "gamma_q"), ("k", w.n_heads_k, "gamma_k"))]
+
+
+def time_oracle_workload(w, inp, target_s: float):
+    """Time the oracle on the first token rows, as many as take about
+    target_s seconds; returns (us per full call, rows, seconds).  The
+    expanded-layout workloads hold equal values in every head's table row,
+    so the oracle runs them from the shared rows (the same numbers)."""
+    rows_avail = (inp["qkv"] if w.packed else inp["q"]).shape[0]
+    probe = np.arange(min(256, rows_avail))
+    t0 = time.perf_counter()
+    oracle_rows(w, inp, probe)
+    per_tok = (time.perf_counter() - t0) / len(probe)
+    n = int(min(rows_avail, max(len(probe), target_s / max(per_tok, 1e-9))))
+    t0 = time.perf_counter()
+    oracle_rows(w, inp, np.arange(n))
+    dt = time.perf_counter() - t0
+    return dt / n * w.tokens * 1e6, n, dt
+
+
+# ---------------------------------------------------------------------------
+# the reference arm: the CPU oracle as it stands
+
+def run_reference(args, w):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    max_rows = min(w.tokens, 4096)
+    inp = I.make_inputs(w, tokens=max_rows)
+    # size one step so the warm-up and timed steps end in about two minutes
+    probe = np.arange(min(64, max_rows))
+    t0 = time.perf_counter()
+    oracle_rows(w, inp, probe)
+    per_tok = (time.perf_counter() - t0) / len(probe)
+    per_step = 120.0 / (args.steps + args.warmup)
+    n = int(max(1, min(max_rows, per_step / max(per_tok, 1e-9))))
+    times = []
+    start = 0
+    for i in range(args.warmup + args.steps):
+        rows = (np.arange(n) + start) % max_rows
+        start = (start + n) % max_rows
+        t0 = time.perf_counter()
+        oracle_rows(w, inp, rows)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    total = sum(times)
+    us = total / (len(times) * n) * w.tokens * 1e6
+    sample = (f"{n} token rows per step of the {w.tokens}-token workload "
+              f"(scaled to a full call by tokens), fp64 numpy, 1 thread")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": us, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": us / 1e3, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(w, world),
+        "cpu_baseline": {"value": us, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": us, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(w, world):
+    return {
+        "workload": w.name, "tokens": w.tokens, "n_heads_q": w.n_heads_q, "n_heads_k": w.n_heads_k,
+        "n_heads_v": w.n_heads_v, "head_dim": w.head_dim, "layout": "packed_qkv" if w.packed else "separate",
+        "rope": w.rope_style, "cos_layout": w.cos_layout, "cos_dtype": w.cos_dtype,
+        "rope_axes": list(w.axes_dim), "in_place": True,
+        "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}",
+    }
+
+
+# ---------------------------------------------------------------------------
+# our arm
+
+class Runner:
+    """Device buffers and launch arguments of one workload.  A step is the
+    list of launches that processes the whole workload once: one launch for
+    a packed QKV activation, one per tensor (Q, then K) for FLUX.2's
+    separate tensors."""
+
+    def __init__(self, w, dev, tune, status):
+        import torch
+
+        from diffusion_transformer_qk_gb300 import qknr as Q
+
+        self.Q, self.w, self.dev = Q, w, dev
+        inp = I.make_inputs(w)
+        self.inp = inp
+        D = w.head_dim
+
+        def dev_bits(a):
+            return torch.from_numpy(a.view(np.int16)).view(
+                torch.bfloat16 if w.dtype == "bf16" else torch.float16)
+
+        def dev_tab(a):
+            t = torch.from_numpy(a) if w.cos_dtype == "fp32" else torch.from_numpy(a.view(np.int16)).view(
+                torch.bfloat16)
+            return t
+
+        self.host = {}
+        if w.packed:
+            self.host["qkv"] = dev_bits(inp["qkv"])
+        else:
+            for n in ("q", "k", "v"):
+                self.host[n] = dev_bits(inp[n])
+        self.host["gamma_q"] = torch.from_numpy(inp["gamma_q"])
+        self.host["gamma_k"] = torch.from_numpy(inp["gamma_k"])
+        cos, sin = dev_tab(inp["cos"]), dev_tab(inp["sin"])
+        if w.cos_layout == "per_head_expanded":
+            H = w.n_heads_q
+            cos = cos[:, None, :].expand(cos.shape[0], H, D).contiguous()
+            sin = sin[:, None, :].expand(sin.shape[0], H, D).contiguous()
+        self.host["cos"], self.host["sin"] = cos, sin
+        self.d = {k: v.to(dev) for k, v in self.host.items()}
+        kw = dict(rope_style=w.rope_style, cos_layout=w.cos_layout, eps=w.eps, dev_status=status, **tune)
+        d = self.d
+        if w.packed:
+            self.args = [Q.packed_args(d["qkv"], w.n_heads_q, w.n_heads_k, w.n_heads_v, D, d["gamma_q"],
+                                       d["gamma_k"], d["cos"], d["sin"], **kw)]
+            self.bytes_per_launch = I.algorithmic_bytes(w)
+            self.outputs = ["qkv"]
+        else:
+            self.args = [Q.make_args(q=d["q"], n_heads_q=w.n_heads_q, head_dim=D, gamma_q=d["gamma_q"],
+                                     cos=d["cos"], sin=d["sin"], **kw),
+                         Q.make_args(k=d["k"], n_heads_k=w.n_heads_k, head_dim=D, gamma_k=d["gamma_k"],
+                                     cos=d["cos"], sin=d["sin"], **kw)]
+            self.bytes_per_launch = I.algorithmic_bytes(w, launches="q")
+            self.outputs = ["q", "k"]
+        self.info = Q.query(self.args[0])
+
+    def step(self, stream):
+        for a in self.args:
+            self.Q.launch(a, stream)
+
+    def e2e_buffers(self):
+        self.pinned = {k: v.pin_memory() for k, v in self.host.items()}
+        self.pinned_out = {k: torch_empty_pinned_like(self.host[k]) for k in self.outputs}
+        h2d = sum(t.numel() * t.element_size() for t in self.pinned.values())
+        d2h = sum(t.numel() * t.element_size() for t in self.pinned_out.values())
+        return h2d, d2h
+
+    def e2e_step(self, stream):
+        for k, t in self.pinned.items():
+            self.d[k].copy_(t, non_blocking=True)
+        self.step(stream)
+        for k, t in self.pinned_out.items():
+            t.copy_(self.d[k], non_blocking=True)
+
+
+def torch_empty_pinned_like(t):
+    import torch
+
+    return torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+
+
+def run_ours(args, w):
+    import torch
+
+    from diffusion_transformer_qk_gb300 import build as B
+    from diffusion_transformer_qk_gb300 import qknr as Q
+
+    rank, world, local = dist_init("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    B.ensure_built()
+    Q.load()
+
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    tune = dict(ctas_per_sm=args.ctas_per_sm, stages=args.stages, consumer_warps=args.consumer_warps)
+    run = Runner(w, dev, tune, status)
+    stream = torch.cuda.current_stream(dev)
+    L = len(run.args)
+
+    for _ in range(args.warmup):
+        run.step(stream)
+    torch.cuda.synchronize(dev)
+
+    props = torch.cuda.get_device_properties(dev)
+    gpu_id = ("GPU-" + str(props.uuid)) if getattr(props, "uuid", None) else str(local)
+    sampler = ClockSampler(gpu_id)
+    time.sleep(0.3)                       # let the sampler start
+    for _ in range(args.warmup):
+        run.step(stream)
+    K = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K * L)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K * L)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    barrier()
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    e0.record(stream)
+    j = 0
+    for _ in range(K):
+        for a in run.args:
+            starts[j].record(stream)
+            Q.launch(a, stream)
+            ends[j].record(stream)
+            j += 1
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    t1 = time.perf_counter()
+    barrier()
+    sampler.stop()
+    clocks = sampler.summary(t0, t1)
+
+    elapsed = e0.elapsed_time(e1) / 1e3
+    kernel_ms = statistics.fmean(s.elapsed_time(e) for s, e in zip(starts, ends))
+    st = int(status.item())
+    if st != 0:
+        raise RuntimeError(f"kernel reported status {st} ({Q.STATUS.get(st)})")
+    max_elapsed = max_over_ranks(elapsed, dev)
+    max_kernel_ms = max_over_ranks(kernel_ms, dev)
+
+    # end to end through the public API: pinned host inputs -> device -> calls -> host
+    e2e = None
+    if not args.no_e2e:
+        n_e2e = min(K, args.e2e_steps)
+        h2d, d2h = run.e2e_buffers()
+        for _ in range(3):
+            run.e2e_step(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for _ in range(n_e2e):
+            run.e2e_step(stream)
+        s1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_s = max_over_ranks(s0.elapsed_time(s1) / 1e3, dev)
+        e2e = {"value": whole_job_us_per_call(e2e_s, n_e2e, world), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "steps": n_e2e,
+               "path": "pinned host -> device copies, qknr_forward via the Python binding, "
+                       "device -> pinned host, one stream"}
+        if w.packed:
+            # each e2e step starts from the host input, so V comes back unchanged
+            D3 = (w.n_heads_q + w.n_heads_k) * w.head_dim
+            back = run.pinned_out["qkv"].view(torch.int16).numpy().view(np.uint16)
+            if not np.array_equal(back[:, D3:], run.inp["qkv"][:, D3:]):
+                raise RuntimeError("e2e: V slice changed")
+        if int(status.item()) != 0:
+            raise RuntimeError("kernel reported a timeout during the e2e loop")
+
+    if rank != 0:
+        return 0
+
+    value = whole_job_us_per_call(max_elapsed, K, world)
+    achieved = run.bytes_per_launch / (max_kernel_ms / 1e3) / 1e9
+    peak, peak_kind = hbm_peak()
+    traffic = recorded_traffic(w.name)
+    info = run.info
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": max_elapsed * 1e3 / K, "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic", "config": workload_config(w, world),
+        "gbs": run.bytes_per_launch * L * K * world / max_elapsed / 1e9,
+        "pct_of_hbm_peak": 100.0 * achieved / peak,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": traffic, "peak_source": f"{peak_kind} copy bandwidth (hbm_gbs)",
+                     "algorithmic_bytes_per_launch": run.bytes_per_launch, "kernel_us": max_kernel_ms * 1e3,
+                     "launches_per_step": L, "kernel": info["kernel"]},
+        "gpu_launches": K * L,
+        "clocks": clocks,
+        "launch": {k: info[k] for k in ("grid", "block", "dyn_smem", "stages", "ctas_per_sm", "consumer_warps",
+                                        "stage_bytes", "registers", "num_sms")},
+    }
+    if e2e:
+        line["e2e"] = e2e
+    if world == 1 and not args.no_cpu_baseline:
+        us, n, dt = time_oracle_workload(w, run.inp, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": us, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                "sample": f"first {n} of {w.tokens} token rows, {dt:.1f} s, fp64 numpy, "
+                                          f"1 thread, scaled to a full call by tokens"}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=5000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(I.WORKLOADS))
+    p.add_argument("--ctas-per-sm", type=int, default=0)
+    p.add_argument("--stages", type=int, default=0)
+    p.add_argument("--consumer-warps", type=int, default=0)
+    p.add_argument("--e2e-steps", type=int, default=20)
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = p.parse_args(argv)
+    if args.warmup < 3:
+        p.error("--warmup must be >= 3")
+    w = I.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

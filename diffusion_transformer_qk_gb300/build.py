@@ -1,0 +1,128 @@
+"""Build libqknr.so in-tree with nvcc for sm_103a.
+
+The translation units compile in parallel; ptxas resource usage (registers,
+stack frame, spill bytes, shared memory) of every kernel instance is kept
+in ``_build/ptxas.log`` beside the objects.  A content stamp of the sources
+and flags decides whether a rebuild is needed.
+"""
+from __future__ import annotations
+
+import hashlib
+import os
+import shutil
+import subprocess
+import sys
+from concurrent.futures import ThreadPoolExecutor
+from typing import List
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(PKG)
+CSRC = os.path.join(PKG, "csrc")
+INCLUDE = os.path.join(ROOT, "include")
+BUILD_DIR = os.path.join(PKG, "_build")
+LIB_NAME = "libqknr.so"
+
+ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
+CXX_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas", "-v",
+             "-I" + INCLUDE, "-I" + CSRC]
+
+SOURCES = [
+    "qknr_api.cu",
+    "qknr_inst_bf16_f32.cu",
+    "qknr_inst_bf16_bf16.cu",
+    "qknr_inst_fp16_f32.cu",
+    "qknr_inst_fp16_bf16.cu",
+]
+
+
+def library_path() -> str:
+    return os.path.join(PKG, LIB_NAME)
+
+
+def nvcc() -> str:
+    cand = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    if not os.path.exists(cand):
+        raise RuntimeError("nvcc not found: the CUDA toolkit is required to build libqknr.so")
+    return cand
+
+
+def cuda_lib_dir() -> str:
+    return os.path.join(os.path.dirname(os.path.dirname(os.path.realpath(nvcc()))), "lib64")
+
+
+def _inputs() -> List[str]:
+    files = [os.path.join(CSRC, f) for f in sorted(os.listdir(CSRC))
+             if f.endswith((".cu", ".cuh", ".h"))]
+    files.append(os.path.join(INCLUDE, "qknr.h"))
+    files.append(os.path.abspath(__file__))
+    return files
+
+
+def _stamp() -> str:
+    h = hashlib.sha256()
+    for f in _inputs():
+        h.update(f.encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    h.update(" ".join(ARCH_FLAGS + CXX_FLAGS).encode())
+    return h.hexdigest()
+
+
+def _stamp_path() -> str:
+    return os.path.join(BUILD_DIR, "stamp")
+
+
+def is_stale() -> bool:
+    if not os.path.exists(library_path()) or not os.path.exists(_stamp_path()):
+        return True
+    with open(_stamp_path()) as f:
+        return f.read().strip() != _stamp()
+
+
+def build_library(verbose: bool = False, jobs: int = 0) -> str:
+    """Compile every translation unit and link libqknr.so; returns its path."""
+    os.makedirs(BUILD_DIR, exist_ok=True)
+    cc = nvcc()
+    objs, cmds = [], []
+    for src in SOURCES:
+        obj = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
+        objs.append(obj)
+        cmds.append([cc, *ARCH_FLAGS, *CXX_FLAGS, "-c", os.path.join(CSRC, src), "-o", obj])
+
+    def run(cmd):
+        return subprocess.run(cmd, capture_output=True, text=True)
+
+    with ThreadPoolExecutor(max_workers=jobs or len(cmds)) as ex:
+        results = list(ex.map(run, cmds))
+    log = []
+    for cmd, r in zip(cmds, results):
+        log.append("$ " + " ".join(cmd) + "\n" + r.stdout + r.stderr)
+        if r.returncode != 0:
+            sys.stderr.write(r.stdout + r.stderr)
+            raise RuntimeError(f"nvcc failed on {cmd[-3]}")
+    with open(os.path.join(BUILD_DIR, "ptxas.log"), "w") as f:
+        f.write("\n".join(log))
+    tmp = library_path() + ".tmp"
+    link = [cc, *ARCH_FLAGS, "-shared", "-cudart", "shared", "-o", tmp, *objs,
+            "-Xlinker", "-rpath," + cuda_lib_dir()]
+    r = subprocess.run(link, capture_output=True, text=True)
+    if r.returncode != 0:
+        sys.stderr.write(r.stdout + r.stderr)
+        raise RuntimeError("linking libqknr.so failed")
+    os.replace(tmp, library_path())
+    with open(_stamp_path(), "w") as f:
+        f.write(_stamp())
+    if verbose:
+        print("\n".join(log))
+    return library_path()
+
+
+def ensure_built() -> str:
+    if is_stale():
+        build_library()
+    return library_path()
+
+
+if __name__ == "__main__":
+    build_library(verbose="-v" in sys.argv)
+    print(library_path())

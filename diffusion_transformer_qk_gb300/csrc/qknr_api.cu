@@ -1,0 +1,393 @@
+// C-ABI launcher of the fused DiT QK-RMSNorm + RoPE kernels: argument
+// validation, launch planning (persistent grid, stage ring depth, shared
+// memory) and the launch itself.  No allocation, no synchronisation.
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <unordered_map>
+
+#include "../../include/qknr.h"
+#include "qknr_internal.h"
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+qknr_status fail(qknr_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+qknr_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(QKNR_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+struct DeviceInfo {
+  int num_sms = 0;
+  int smem_optin = 0;       // max dynamic shared memory per block (opt-in)
+  int smem_per_sm = 0;
+  int smem_reserved = 0;    // per-block reservation
+};
+
+std::mutex g_mu;
+std::unordered_map<int, DeviceInfo> g_dev;
+std::unordered_map<const void*, int> g_configured;   // kernel -> device mask with attribute set
+std::unordered_map<const void*, int> g_regs;
+
+qknr_status device_info(int dev, DeviceInfo* out) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  auto it = g_dev.find(dev);
+  if (it != g_dev.end()) {
+    *out = it->second;
+    return QKNR_OK;
+  }
+  DeviceInfo d;
+  cudaError_t e;
+  if ((e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return cuda_fail(e, "cudaDeviceGetAttribute(MultiProcessorCount)");
+  if ((e = cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) !=
+      cudaSuccess)
+    return cuda_fail(e, "cudaDeviceGetAttribute(MaxSharedMemoryPerBlockOptin)");
+  if ((e = cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) !=
+      cudaSuccess)
+    return cuda_fail(e, "cudaDeviceGetAttribute(MaxSharedMemoryPerMultiprocessor)");
+  if ((e = cudaDeviceGetAttribute(&d.smem_reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev)) !=
+      cudaSuccess)
+    return cuda_fail(e, "cudaDeviceGetAttribute(ReservedSharedMemoryPerBlock)");
+  g_dev[dev] = d;
+  *out = d;
+  return QKNR_OK;
+}
+
+// Set the kernel's dynamic shared memory ceiling to the device maximum
+// (once per kernel and device) and return its register count.
+qknr_status configure_kernel(const void* fn, int dev, const DeviceInfo& di, int* regs) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  int& mask = g_configured[fn];
+  if (!(mask & (1 << (dev & 31)))) {
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, di.smem_optin);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(MaxDynamicSharedMemorySize)");
+    cudaFuncAttributes fa;
+    e = cudaFuncGetAttributes(&fa, fn);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncGetAttributes");
+    g_regs[fn] = fa.numRegs;
+    mask |= 1 << (dev & 31);
+  }
+  *regs = g_regs[fn];
+  return QKNR_OK;
+}
+
+struct Span {
+  uintptr_t lo, hi;   // [lo, hi)
+};
+
+Span span_of(const void* base, long long rows, long long stride_bytes, long long row_bytes) {
+  uintptr_t lo = reinterpret_cast<uintptr_t>(base);
+  if (!base || rows <= 0 || row_bytes <= 0) return {lo, lo};
+  return {lo, lo + static_cast<uintptr_t>((rows - 1) * stride_bytes + row_bytes)};
+}
+
+bool overlaps(Span a, Span b) { return a.lo < a.hi && b.lo < b.hi && a.lo < b.hi && b.lo < a.hi; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Plan {
+  qknr::KernelParams kp;
+  const void* fn = nullptr;
+  int grid = 0, block = 0, smem = 0, stages = 0, ctas_per_sm = 0, warps = 0, regs = 0, num_sms = 0;
+  bool launch = false;   // false: nothing to do
+  char name[96];
+};
+
+qknr_status make_plan(const qknr_args* a, Plan* pl) {
+  if (!a) return fail(QKNR_ERR_NULL, "args is NULL");
+  if (a->abi_version != QKNR_ABI_VERSION)
+    return fail(QKNR_ERR_ABI, "abi_version %u, library expects %d", a->abi_version, QKNR_ABI_VERSION);
+  if (a->dtype != QKNR_BF16 && a->dtype != QKNR_FP16)
+    return fail(QKNR_ERR_UNSUPPORTED, "activation dtype must be BF16 or FP16");
+  if (a->cos_dtype != QKNR_FP32 && a->cos_dtype != QKNR_BF16)
+    return fail(QKNR_ERR_UNSUPPORTED, "cos/sin dtype must be FP32 or BF16");
+  if (a->cos_layout != QKNR_COS_SHARED_ROW && a->cos_layout != QKNR_COS_PER_HEAD_EXPANDED)
+    return fail(QKNR_ERR_UNSUPPORTED, "unknown cos_layout %d", a->cos_layout);
+  if (a->rope_style != QKNR_ROPE_INTERLEAVED && a->rope_style != QKNR_ROPE_ROTATE_HALF)
+    return fail(QKNR_ERR_UNSUPPORTED, "unknown rope_style %d", a->rope_style);
+  const int D = a->head_dim;
+  if (D != 64 && D != 128) return fail(QKNR_ERR_UNSUPPORTED, "head_dim %d (supported: 64, 128)", D);
+  if (a->tokens < 0) return fail(QKNR_ERR_SHAPE, "tokens < 0");
+  if (a->n_heads_q < 0 || a->n_heads_k < 0 || a->n_heads_v < 0)
+    return fail(QKNR_ERR_SHAPE, "negative head count");
+  if (!(a->eps >= 0.0f)) return fail(QKNR_ERR_SHAPE, "eps must be >= 0");
+  if (a->consumer_warps < 0 || a->consumer_warps > qknr::kMaxConsumerWarps)
+    return fail(QKNR_ERR_SHAPE, "consumer_warps out of range 0..%d", qknr::kMaxConsumerWarps);
+  if (a->stages < 0 || a->stages == 1 || a->stages > qknr::kMaxStages)
+    return fail(QKNR_ERR_SHAPE, "stages must be 0 (auto) or 2..%d", qknr::kMaxStages);
+  if (a->ctas_per_sm < 0 || a->ctas_per_sm > 4) return fail(QKNR_ERR_SHAPE, "ctas_per_sm out of range 0..4");
+
+  const int es = 2;
+  const int ces = a->cos_dtype == QKNR_FP32 ? 4 : 2;
+  const long long T = a->tokens;
+  const int hq = a->n_heads_q, hk = a->n_heads_k;
+  const bool expanded = a->cos_layout == QKNR_COS_PER_HEAD_EXPANDED;
+
+  const bool rh = a->rope_style == QKNR_ROPE_ROTATE_HALF;
+  const bool bf16_tab = a->cos_dtype == QKNR_BF16;
+  if (a->dtype == QKNR_BF16)
+    pl->fn = bf16_tab ? qknr::kernel_bf16_bf16(D, rh, expanded) : qknr::kernel_bf16_f32(D, rh, expanded);
+  else
+    pl->fn = bf16_tab ? qknr::kernel_fp16_bf16(D, rh, expanded) : qknr::kernel_fp16_f32(D, rh, expanded);
+  if (!pl->fn) return fail(QKNR_ERR_UNSUPPORTED, "no kernel instance for this combination");
+  snprintf(pl->name, sizeof(pl->name), "qknr_fused<%s,%s,D%d,%s,%s>", a->dtype == QKNR_BF16 ? "bf16" : "fp16",
+           bf16_tab ? "bf16" : "fp32", D, rh ? "rotate_half" : "interleaved", expanded ? "expanded" : "shared");
+  memset(&pl->kp, 0, sizeof(pl->kp));
+  pl->launch = false;
+  if (T == 0) return QKNR_OK;   // nothing to read or write: pointers may be NULL
+
+  // outputs default to in place
+  const void* q = a->q;
+  const void* k = a->k;
+  const void* v = a->v;
+  void* q_out = a->q_out ? a->q_out : const_cast<void*>(q);
+  void* k_out = a->k_out ? a->k_out : const_cast<void*>(k);
+  const long long qs = a->q_stride ? a->q_stride : (long long)hq * D;
+  const long long ks = a->k_stride ? a->k_stride : (long long)hk * D;
+  const long long vs = a->v_stride ? a->v_stride : (long long)a->n_heads_v * D;
+  const long long qos = a->q_out_stride ? a->q_out_stride : qs;
+  const long long kos = a->k_out_stride ? a->k_out_stride : ks;
+  const long long vos = a->v_out_stride ? a->v_out_stride : vs;
+  const bool copy_v = a->n_heads_v > 0 && a->v_out && !(a->v_out == v && vos == vs);
+  const int hv = copy_v ? a->n_heads_v : 0;
+
+  if (hq > 0 && (!q || !a->gamma_q)) return fail(QKNR_ERR_NULL, "q and gamma_q are required when n_heads_q > 0");
+  if (hk > 0 && (!k || !a->gamma_k)) return fail(QKNR_ERR_NULL, "k and gamma_k are required when n_heads_k > 0");
+  if (copy_v && !v) return fail(QKNR_ERR_NULL, "v is required to copy V into v_out");
+  if (hq + hk > 0 && (!a->cos || !a->sin)) return fail(QKNR_ERR_NULL, "cos and sin are required");
+  if (hq > 0 && qs < (long long)hq * D) return fail(QKNR_ERR_SHAPE, "q_stride < n_heads_q * head_dim");
+  if (hk > 0 && ks < (long long)hk * D) return fail(QKNR_ERR_SHAPE, "k_stride < n_heads_k * head_dim");
+  if (hq > 0 && qos < (long long)hq * D) return fail(QKNR_ERR_SHAPE, "q_out_stride too small");
+  if (hk > 0 && kos < (long long)hk * D) return fail(QKNR_ERR_SHAPE, "k_out_stride too small");
+  if (hv > 0 && (vs < (long long)hv * D || vos < (long long)hv * D))
+    return fail(QKNR_ERR_SHAPE, "v strides too small");
+  if (expanded && hq > 0 && hk > 0 && hq != hk)
+    return fail(QKNR_ERR_SHAPE, "per-head expanded tables need n_heads_q == n_heads_k");
+  const long long cos_rows = a->cos_rows ? a->cos_rows : T;
+  if (a->cos_rows < 0) return fail(QKNR_ERR_SHAPE, "cos_rows < 0");
+
+  // alignment: every bulk copy and 16-byte store starts on a 16-byte boundary
+  if (hq > 0 && (!aligned16(q) || !aligned16(q_out) || (qs * es) % 16 || (qos * es) % 16))
+    return fail(QKNR_ERR_ALIGN, "q / q_out base or row stride not 16-byte aligned");
+  if (hk > 0 && (!aligned16(k) || !aligned16(k_out) || (ks * es) % 16 || (kos * es) % 16))
+    return fail(QKNR_ERR_ALIGN, "k / k_out base or row stride not 16-byte aligned");
+  if (hv > 0 && (!aligned16(v) || !aligned16(a->v_out) || (vs * es) % 16 || (vos * es) % 16))
+    return fail(QKNR_ERR_ALIGN, "v / v_out base or row stride not 16-byte aligned");
+  if (hq + hk > 0 && (!aligned16(a->cos) || !aligned16(a->sin)))
+    return fail(QKNR_ERR_ALIGN, "cos / sin not 16-byte aligned");
+  if ((a->gamma_q && (reinterpret_cast<uintptr_t>(a->gamma_q) & 3u)) ||
+      (a->gamma_k && (reinterpret_cast<uintptr_t>(a->gamma_k) & 3u)))
+    return fail(QKNR_ERR_ALIGN, "gamma not 4-byte aligned");
+
+  pl->launch = T > 0 && (hq + hk + hv) > 0;
+  const int table_heads = expanded ? (hq > hk ? hq : hk) : 1;
+  const long long cos_row_bytes = hq + hk > 0 ? (long long)table_heads * D * ces : 0;
+
+  // overlap: an output that is not exactly its own input must not touch any input
+  if (pl->launch) {
+    const Span in[] = {
+        span_of(q, hq ? T : 0, qs * es, (long long)hq * D * es),
+        span_of(k, hk ? T : 0, ks * es, (long long)hk * D * es),
+        span_of(v, hv ? T : 0, vs * es, (long long)hv * D * es),
+        span_of(a->cos, hq + hk ? cos_rows : 0, cos_row_bytes, cos_row_bytes),
+        span_of(a->sin, hq + hk ? cos_rows : 0, cos_row_bytes, cos_row_bytes),
+        span_of(a->gamma_q, hq ? 1 : 0, 0, (long long)D * 4),
+        span_of(a->gamma_k, hk ? 1 : 0, 0, (long long)D * 4),
+    };
+    struct {
+      const void* out;
+      const void* own;
+      long long os, is, heads;
+      const char* name;
+    } outs[] = {{q_out, q, qos, qs, hq, "q_out"}, {k_out, k, kos, ks, hk, "k_out"},
+                {a->v_out, v, vos, vs, hv, "v_out"}};
+    for (auto& o : outs) {
+      if (o.heads == 0) continue;
+      if (o.out == o.own && o.os == o.is) continue;   // exactly in place
+      const Span so = span_of(o.out, T, o.os * es, o.heads * D * es);
+      for (const Span& si : in)
+        if (overlaps(so, si)) return fail(QKNR_ERR_OVERLAP, "%s overlaps an input without being in place", o.name);
+    }
+  }
+
+  // stage layout
+  const unsigned q_bytes = hq * D * es, k_bytes = hk * D * es, v_bytes = hv * D * es;
+  const long long tx = (long long)q_bytes + k_bytes + v_bytes + 2 * cos_row_bytes;
+  const long long stage_bytes = (tx + qknr::kStageAlign - 1) / qknr::kStageAlign * qknr::kStageAlign;
+
+  qknr::KernelParams& kp = pl->kp;
+  kp.q = static_cast<const char*>(q);
+  kp.k = static_cast<const char*>(k);
+  kp.v = static_cast<const char*>(v);
+  kp.q_out = static_cast<char*>(q_out);
+  kp.k_out = static_cast<char*>(k_out);
+  kp.v_out = static_cast<char*>(a->v_out);
+  kp.q_stride = qs * es;
+  kp.k_stride = ks * es;
+  kp.v_stride = vs * es;
+  kp.q_out_stride = qos * es;
+  kp.k_out_stride = kos * es;
+  kp.v_out_stride = vos * es;
+  kp.tokens = T;
+  kp.cos_rows = cos_rows > 0 ? cos_rows : 1;
+  kp.cos = static_cast<const char*>(a->cos);
+  kp.sin = static_cast<const char*>(a->sin);
+  kp.cos_row_bytes = cos_row_bytes;
+  kp.gamma_q = a->gamma_q;
+  kp.gamma_k = a->gamma_k;
+  kp.status = a->dev_status;
+  kp.wait_limit_ns = a->wait_limit_ns ? a->wait_limit_ns : 2000000000ull;
+  kp.eps = a->eps;
+  kp.inv_d = 1.0f / static_cast<float>(D);
+  kp.hq = hq;
+  kp.hk = hk;
+  kp.hv = hv;
+  kp.flags = a->flags;
+  kp.off_k = q_bytes;
+  kp.off_v = q_bytes + k_bytes;
+  kp.off_cos = q_bytes + k_bytes + v_bytes;
+  kp.off_sin = kp.off_cos + static_cast<unsigned>(cos_row_bytes);
+  kp.stage_bytes = static_cast<unsigned>(stage_bytes);
+  kp.tx_bytes = static_cast<unsigned>(tx);
+
+  return QKNR_OK;
+}
+
+// Device-dependent part of the plan: grid, ring depth and shared memory.
+qknr_status size_launch(const qknr_args* a, Plan* pl) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  DeviceInfo di;
+  qknr_status st = device_info(dev, &di);
+  if (st != QKNR_OK) return st;
+  st = configure_kernel(pl->fn, dev, di, &pl->regs);
+  if (st != QKNR_OK) return st;
+  pl->num_sms = di.num_sms;
+
+  const int warps = a->consumer_warps ? a->consumer_warps : 8;
+  const int cps = a->ctas_per_sm ? a->ctas_per_sm : 1;
+  const long long stage_bytes = pl->kp.stage_bytes;
+  // shared memory one CTA may use when `cps` CTAs share an SM
+  long long budget = di.smem_per_sm / cps - di.smem_reserved;
+  if (budget > di.smem_optin) budget = di.smem_optin;
+  const long long ring = budget - qknr::kOffStage0;
+  const long long fit = ring > 0 ? ring / stage_bytes : 0;
+  int stages = a->stages;
+  if (stages == 0) {
+    stages = static_cast<int>(fit < qknr::kMaxStages ? fit : qknr::kMaxStages);
+    // no deeper than the rows one CTA will see
+    const long long grid0 = (long long)di.num_sms * cps;
+    const long long rows_per_cta = (a->tokens + grid0 - 1) / grid0;
+    if (rows_per_cta >= 2 && stages > rows_per_cta) stages = static_cast<int>(rows_per_cta);
+    if (stages < 2) stages = 2;
+  }
+  const long long smem = qknr::kOffStage0 + stages * stage_bytes;
+  if (smem > di.smem_optin)
+    return fail(QKNR_ERR_UNSUPPORTED, "a %d-stage ring of %lld-byte rows needs %lld B of shared memory (max %d)",
+                stages, stage_bytes, smem, di.smem_optin);
+  const int block = 32 * (warps + 1);
+  int occ = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, pl->fn, block, static_cast<size_t>(smem));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+  if (occ < 1) return fail(QKNR_ERR_UNSUPPORTED, "kernel does not fit on an SM with %lld B shared memory", smem);
+  const int per_sm = cps < occ ? cps : occ;
+  long long grid = (long long)di.num_sms * per_sm;
+  if (grid > a->tokens) grid = a->tokens;
+  pl->kp.stages = stages;
+  pl->kp.consumer_warps = warps;
+  pl->grid = static_cast<int>(grid);
+  pl->block = block;
+  pl->smem = static_cast<int>(smem);
+  pl->stages = stages;
+  pl->ctas_per_sm = per_sm;
+  pl->warps = warps;
+  return QKNR_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+void qknr_args_init(qknr_args* a) {
+  if (!a) return;
+  memset(a, 0, sizeof(*a));
+  a->abi_version = QKNR_ABI_VERSION;
+  a->dtype = QKNR_BF16;
+  a->eps = 1e-6f;
+  a->cos_dtype = QKNR_FP32;
+  a->cos_layout = QKNR_COS_SHARED_ROW;
+  a->rope_style = QKNR_ROPE_INTERLEAVED;
+}
+
+qknr_status qknr_query(const qknr_args* args, qknr_launch_info* info) {
+  if (!info) return fail(QKNR_ERR_NULL, "info is NULL");
+  memset(info, 0, sizeof(*info));
+  Plan pl;
+  qknr_status st = make_plan(args, &pl);
+  if (st != QKNR_OK) return st;
+  snprintf(info->kernel, sizeof(info->kernel), "%s", pl.name);
+  info->stage_bytes = static_cast<int32_t>(pl.kp.stage_bytes);
+  if (!pl.launch) return QKNR_OK;
+  st = size_launch(args, &pl);
+  if (st != QKNR_OK) return st;
+  info->grid = pl.grid;
+  info->block = pl.block;
+  info->dyn_smem = pl.smem;
+  info->stages = pl.stages;
+  info->ctas_per_sm = pl.ctas_per_sm;
+  info->consumer_warps = pl.warps;
+  info->registers = pl.regs;
+  info->num_sms = pl.num_sms;
+  return QKNR_OK;
+}
+
+qknr_status qknr_forward(const qknr_args* args, qknr_stream_t stream) {
+  Plan pl;
+  qknr_status st = make_plan(args, &pl);
+  if (st != QKNR_OK || !pl.launch) return st;
+  st = size_launch(args, &pl);
+  if (st != QKNR_OK) return st;
+  void* kargs[] = {&pl.kp};
+  cudaError_t e = cudaLaunchKernel(pl.fn, dim3(pl.grid), dim3(pl.block), kargs, static_cast<size_t>(pl.smem),
+                                   reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchKernel");
+  return QKNR_OK;
+}
+
+const char* qknr_status_string(int32_t s) {
+  switch (s) {
+    case QKNR_OK: return "ok";
+    case QKNR_ERR_NULL: return "required pointer is NULL";
+    case QKNR_ERR_SHAPE: return "size, count or stride out of range";
+    case QKNR_ERR_ALIGN: return "address or row stride not 16-byte aligned";
+    case QKNR_ERR_UNSUPPORTED: return "unsupported combination";
+    case QKNR_ERR_CUDA: return "CUDA runtime error";
+    case QKNR_ERR_TIMEOUT: return "in-kernel wait timed out";
+    case QKNR_ERR_OVERLAP: return "output overlaps an input";
+    case QKNR_ERR_ABI: return "ABI version mismatch";
+    default: return "unknown status";
+  }
+}
+
+const char* qknr_last_error(void) { return g_err; }
+
+int32_t qknr_abi_version(void) { return QKNR_ABI_VERSION; }
+
+size_t qknr_sizeof_args(void) { return sizeof(qknr_args); }
+
+size_t qknr_sizeof_launch_info(void) { return sizeof(qknr_launch_info); }
+
+}  // extern "C"

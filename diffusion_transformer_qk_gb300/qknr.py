@@ -1,0 +1,346 @@
+"""Python binding of libqknr.so (ctypes).
+
+Argument marshalling only: tensors are turned into device pointers, row
+strides and the current CUDA stream, and every step of the operation runs
+in the library's kernels.  The binding has no fallback: if the library is
+missing or cannot be loaded, every call raises.
+
+The operation (per-head RMSNorm of Q and K followed by RoPE, V passed
+through) is described in ``include/qknr.h``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from ctypes import c_char, c_float, c_int32, c_int64, c_size_t, c_uint32, c_uint64, c_void_p
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+# enum values of include/qknr.h
+BF16, FP16, FP32 = 0, 1, 2
+ROPE = {"interleaved": 0, "rotate_half": 1}
+COS_LAYOUT = {"shared_row": 0, "per_head_expanded": 1}
+STATUS = {
+    0: "QKNR_OK", 1: "QKNR_ERR_NULL", 2: "QKNR_ERR_SHAPE", 3: "QKNR_ERR_ALIGN",
+    4: "QKNR_ERR_UNSUPPORTED", 5: "QKNR_ERR_CUDA", 6: "QKNR_ERR_TIMEOUT",
+    7: "QKNR_ERR_OVERLAP", 8: "QKNR_ERR_ABI",
+}
+OK, ERR_TIMEOUT = 0, 6
+FLAG_TEST_STALL = 0x1
+ABI_VERSION = 1
+
+EXPORTS = (
+    "qknr_args_init", "qknr_forward", "qknr_query", "qknr_status_string",
+    "qknr_last_error", "qknr_abi_version", "qknr_sizeof_args", "qknr_sizeof_launch_info",
+)
+
+
+class QknrArgs(ctypes.Structure):
+    """Mirror of ``qknr_args``."""
+
+    _fields_ = [
+        ("abi_version", c_uint32), ("dtype", c_int32),
+        ("q", c_void_p), ("k", c_void_p), ("v", c_void_p),
+        ("q_out", c_void_p), ("k_out", c_void_p), ("v_out", c_void_p),
+        ("q_stride", c_int64), ("k_stride", c_int64), ("v_stride", c_int64),
+        ("q_out_stride", c_int64), ("k_out_stride", c_int64), ("v_out_stride", c_int64),
+        ("tokens", c_int64),
+        ("n_heads_q", c_int32), ("n_heads_k", c_int32), ("n_heads_v", c_int32),
+        ("head_dim", c_int32),
+        ("gamma_q", c_void_p), ("gamma_k", c_void_p), ("eps", c_float),
+        ("cos", c_void_p), ("sin", c_void_p),
+        ("cos_dtype", c_int32), ("cos_layout", c_int32), ("cos_rows", c_int64),
+        ("rope_style", c_int32),
+        ("dev_status", c_void_p),
+        ("ctas_per_sm", c_int32), ("stages", c_int32), ("consumer_warps", c_int32),
+        ("flags", c_uint32), ("wait_limit_ns", c_uint64),
+    ]
+
+
+class QknrLaunchInfo(ctypes.Structure):
+    """Mirror of ``qknr_launch_info``."""
+
+    _fields_ = [
+        ("grid", c_int32), ("block", c_int32), ("dyn_smem", c_int32), ("stages", c_int32),
+        ("ctas_per_sm", c_int32), ("consumer_warps", c_int32), ("stage_bytes", c_int32),
+        ("registers", c_int32), ("num_sms", c_int32), ("kernel", c_char * 96),
+    ]
+
+    def as_dict(self):
+        d = {name: getattr(self, name) for name, _ in self._fields_}
+        d["kernel"] = self.kernel.decode()
+        return d
+
+
+class QknrError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def library_path() -> str:
+    return _build.library_path()
+
+
+def load(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load libqknr.so (once).  Raises if it is missing or malformed."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or library_path()
+        if not os.path.exists(p):
+            raise RuntimeError(
+                f"{p} is not built; build it with diffusion_transformer_qk_gb300.build.build_library()")
+        lib = ctypes.CDLL(p)
+        lib.qknr_args_init.argtypes = [ctypes.POINTER(QknrArgs)]
+        lib.qknr_args_init.restype = None
+        lib.qknr_forward.argtypes = [ctypes.POINTER(QknrArgs), c_void_p]
+        lib.qknr_forward.restype = c_int32
+        lib.qknr_query.argtypes = [ctypes.POINTER(QknrArgs), ctypes.POINTER(QknrLaunchInfo)]
+        lib.qknr_query.restype = c_int32
+        lib.qknr_status_string.argtypes = [c_int32]
+        lib.qknr_status_string.restype = ctypes.c_char_p
+        lib.qknr_last_error.argtypes = []
+        lib.qknr_last_error.restype = ctypes.c_char_p
+        lib.qknr_abi_version.argtypes = []
+        lib.qknr_abi_version.restype = c_int32
+        lib.qknr_sizeof_args.restype = c_size_t
+        lib.qknr_sizeof_launch_info.restype = c_size_t
+        if lib.qknr_abi_version() != ABI_VERSION:
+            raise RuntimeError("libqknr.so ABI version mismatch")
+        if lib.qknr_sizeof_args() != ctypes.sizeof(QknrArgs) or \
+                lib.qknr_sizeof_launch_info() != ctypes.sizeof(QknrLaunchInfo):
+            raise RuntimeError("libqknr.so struct layout differs from the binding")
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def last_error() -> str:
+    return load().qknr_last_error().decode()
+
+
+# ---------------------------------------------------------------------------
+# marshalling helpers
+
+_ACT = {torch.bfloat16: BF16, torch.float16: FP16}
+_TAB = {torch.float32: FP32, torch.bfloat16: BF16}
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _rows(t: Optional[torch.Tensor], name: str) -> int:
+    """Row stride (elements) of a 2-D activation view with unit inner stride."""
+    if t is None:
+        return 0
+    if t.dim() != 2:
+        raise ValueError(f"{name} must be 2-D [tokens, heads*head_dim]")
+    if t.stride(1) != 1:
+        raise ValueError(f"{name} rows must be contiguous")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    return t.stride(0)
+
+
+_status_bufs = {}
+
+
+def status_buffer(device=None) -> torch.Tensor:
+    """The per-device int32 status word the binding passes by default."""
+    dev = torch.device("cuda", torch.cuda.current_device() if device is None else torch.device(device).index)
+    buf = _status_bufs.get(dev.index)
+    if buf is None:
+        buf = torch.zeros(1, dtype=torch.int32, device=dev)
+        _status_bufs[dev.index] = buf
+    return buf
+
+
+def read_status(device=None, reset: bool = True) -> int:
+    """Synchronise and return the kernel-side status word (0 = no timeout)."""
+    buf = status_buffer(device)
+    v = int(buf.item())
+    if reset and v:
+        buf.zero_()
+    return v
+
+
+def make_args(
+    *,
+    q: Optional[torch.Tensor] = None,
+    k: Optional[torch.Tensor] = None,
+    v: Optional[torch.Tensor] = None,
+    q_out: Optional[torch.Tensor] = None,
+    k_out: Optional[torch.Tensor] = None,
+    v_out: Optional[torch.Tensor] = None,
+    n_heads_q: int = 0,
+    n_heads_k: int = 0,
+    n_heads_v: int = 0,
+    head_dim: int,
+    gamma_q: Optional[torch.Tensor] = None,
+    gamma_k: Optional[torch.Tensor] = None,
+    cos: Optional[torch.Tensor] = None,
+    sin: Optional[torch.Tensor] = None,
+    rope_style: str = "interleaved",
+    cos_layout: str = "shared_row",
+    cos_rows: Optional[int] = None,
+    eps: float = 1e-6,
+    tokens: Optional[int] = None,
+    dev_status: Optional[torch.Tensor] = None,
+    ctas_per_sm: int = 0,
+    stages: int = 0,
+    consumer_warps: int = 0,
+    flags: int = 0,
+    wait_limit_ns: int = 0,
+) -> QknrArgs:
+    """Build a ``QknrArgs`` from tensors (no checks beyond marshalling; the
+    library validates)."""
+    a = QknrArgs()
+    load().qknr_args_init(ctypes.byref(a))
+    acts = [t for t in (q, k, v) if t is not None]
+    if acts:
+        dt = acts[0].dtype
+        if dt not in _ACT or any(t.dtype != dt for t in acts):
+            raise ValueError("q, k, v must share one dtype: bfloat16 or float16")
+        a.dtype = _ACT[dt]
+    for out, inp, name in ((q_out, q, "q_out"), (k_out, k, "k_out"), (v_out, v, "v_out")):
+        if out is not None and inp is not None and out.dtype != inp.dtype:
+            raise ValueError(f"{name} dtype differs from its input")
+    a.q, a.k, a.v = _ptr(q), _ptr(k), _ptr(v)
+    a.q_out, a.k_out, a.v_out = _ptr(q_out), _ptr(k_out), _ptr(v_out)
+    a.q_stride, a.k_stride, a.v_stride = _rows(q, "q"), _rows(k, "k"), _rows(v, "v")
+    a.q_out_stride = _rows(q_out, "q_out")
+    a.k_out_stride = _rows(k_out, "k_out")
+    a.v_out_stride = _rows(v_out, "v_out")
+    if tokens is None:
+        tokens = acts[0].shape[0] if acts else 0
+    a.tokens = tokens
+    a.n_heads_q, a.n_heads_k, a.n_heads_v, a.head_dim = n_heads_q, n_heads_k, n_heads_v, head_dim
+    for g, name in ((gamma_q, "gamma_q"), (gamma_k, "gamma_k")):
+        if g is not None and (g.dtype != torch.float32 or not g.is_cuda or not g.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous float32 CUDA tensor")
+    a.gamma_q, a.gamma_k = _ptr(gamma_q), _ptr(gamma_k)
+    a.eps = eps
+    if cos is not None:
+        if cos.dtype not in _TAB or sin is None or sin.dtype != cos.dtype:
+            raise ValueError("cos and sin must both be float32 or both bfloat16")
+        if not (cos.is_contiguous() and sin.is_contiguous() and cos.is_cuda and sin.is_cuda):
+            raise ValueError("cos and sin must be contiguous CUDA tensors")
+        if cos.shape != sin.shape:
+            raise ValueError("cos and sin shapes differ")
+        a.cos_dtype = _TAB[cos.dtype]
+        if cos_rows is None:
+            cos_rows = cos.shape[0]
+    a.cos, a.sin = _ptr(cos), _ptr(sin)
+    a.cos_layout = COS_LAYOUT[cos_layout]
+    a.cos_rows = cos_rows or 0
+    a.rope_style = ROPE[rope_style]
+    a.dev_status = _ptr(dev_status)
+    a.ctas_per_sm, a.stages, a.consumer_warps = ctas_per_sm, stages, consumer_warps
+    a.flags, a.wait_limit_ns = flags, wait_limit_ns
+    return a
+
+
+def launch(a: QknrArgs, stream: Optional[torch.cuda.Stream] = None) -> None:
+    """qknr_forward on ``stream`` (default: the current stream)."""
+    lib = load()
+    s = torch.cuda.current_stream() if stream is None else stream
+    st = lib.qknr_forward(ctypes.byref(a), c_void_p(s.cuda_stream))
+    if st != OK:
+        raise QknrError(st, lib.qknr_last_error().decode())
+
+
+def query(a: QknrArgs) -> dict:
+    """qknr_query: the launch qknr_forward would make, as a dict."""
+    lib = load()
+    info = QknrLaunchInfo()
+    st = lib.qknr_query(ctypes.byref(a), ctypes.byref(info))
+    if st != OK:
+        raise QknrError(st, lib.qknr_last_error().decode())
+    return info.as_dict()
+
+
+# ---------------------------------------------------------------------------
+# convenience forms
+
+def _check_table(cos, head_dim, cos_layout, heads):
+    if cos_layout == "shared_row":
+        if cos.dim() != 2 or cos.shape[1] != head_dim:
+            raise ValueError("shared cos/sin must be [rows, head_dim]")
+    else:
+        if cos.dim() != 3 or cos.shape[1] != heads or cos.shape[2] != head_dim:
+            raise ValueError("expanded cos/sin must be [rows, heads, head_dim]")
+
+
+def packed_args(qkv, n_heads_q, n_heads_k, n_heads_v, head_dim, gamma_q, gamma_k, cos, sin, *,
+                out=None, **kw) -> QknrArgs:
+    """Arguments for a packed [T, (Hq+Hk+Hv)*D] activation.  ``out=None``
+    normalises Q and K in place and leaves V alone; otherwise ``out`` (same
+    shape) receives Q, K and a copy of V."""
+    D = head_dim
+    width = (n_heads_q + n_heads_k + n_heads_v) * D
+    if qkv.dim() != 2 or qkv.shape[1] != width:
+        raise ValueError(f"qkv must be [tokens, {width}]")
+    _check_table(cos, D, kw.get("cos_layout", "shared_row"), n_heads_q)
+    q0, k0, v0, v1 = 0, n_heads_q * D, (n_heads_q + n_heads_k) * D, width
+    views = dict(q=qkv[:, q0:k0] if n_heads_q else None,
+                 k=qkv[:, k0:v0] if n_heads_k else None,
+                 v=qkv[:, v0:v1] if n_heads_v else None)
+    if out is not None:
+        if out.shape != qkv.shape or out.dtype != qkv.dtype:
+            raise ValueError("out must match qkv's shape and dtype")
+        views.update(q_out=out[:, q0:k0] if n_heads_q else None,
+                     k_out=out[:, k0:v0] if n_heads_k else None,
+                     v_out=out[:, v0:v1] if n_heads_v else None)
+    return make_args(**views, n_heads_q=n_heads_q, n_heads_k=n_heads_k, n_heads_v=n_heads_v,
+                     head_dim=D, gamma_q=gamma_q if n_heads_q else None,
+                     gamma_k=gamma_k if n_heads_k else None, cos=cos, sin=sin,
+                     tokens=qkv.shape[0], **kw)
+
+
+def qk_norm_rope_packed(qkv, n_heads_q, n_heads_k, n_heads_v, head_dim, gamma_q, gamma_k, cos, sin, *,
+                        out=None, stream=None, status=True, **kw):
+    """Fused QK-RMSNorm + RoPE on a packed QKV activation; returns the
+    tensor holding the result (``qkv`` itself when in place)."""
+    if status and "dev_status" not in kw:
+        kw["dev_status"] = status_buffer(qkv.device)
+    launch(packed_args(qkv, n_heads_q, n_heads_k, n_heads_v, head_dim, gamma_q, gamma_k, cos, sin,
+                       out=out, **kw), stream)
+    return qkv if out is None else out
+
+
+def qk_norm_rope_tensor(x, n_heads, head_dim, gamma, cos, sin, *, out=None, stream=None, status=True,
+                        **kw):
+    """Per-tensor launch (one separate Q or K tensor [T, H*D]), the form
+    of page 2's FLUX.2 integration.  In place unless ``out`` is given."""
+    if x.dim() != 2 or x.shape[1] != n_heads * head_dim:
+        raise ValueError("x must be [tokens, n_heads*head_dim]")
+    _check_table(cos, head_dim, kw.get("cos_layout", "shared_row"), n_heads)
+    if status and "dev_status" not in kw:
+        kw["dev_status"] = status_buffer(x.device)
+    launch(make_args(q=x, q_out=out, n_heads_q=n_heads, head_dim=head_dim, gamma_q=gamma, cos=cos, sin=sin,
+                     **kw), stream)
+    return x if out is None else out
+
+
+def qk_norm_rope_separate(q, k, n_heads, head_dim, gamma_q, gamma_k, cos, sin, *, v=None, q_out=None,
+                          k_out=None, v_out=None, n_heads_v=None, stream=None, status=True, **kw):
+    """Q and K as separate [T, H*D] tensors in one launch (and V copied into
+    ``v_out`` when both are given)."""
+    _check_table(cos, head_dim, kw.get("cos_layout", "shared_row"), n_heads)
+    if status and "dev_status" not in kw:
+        kw["dev_status"] = status_buffer(q.device)
+    hv = (n_heads if n_heads_v is None else n_heads_v) if (v is not None and v_out is not None) else 0
+    launch(make_args(q=q, k=k, v=v if hv else None, q_out=q_out, k_out=k_out, v_out=v_out if hv else None,
+                     n_heads_q=n_heads, n_heads_k=n_heads, n_heads_v=hv, head_dim=head_dim,
+                     gamma_q=gamma_q, gamma_k=gamma_k, cos=cos, sin=sin, **kw), stream)

@@ -1,0 +1,187 @@
+/*
+ * qknr.h — C ABI of the fused DiT QK-RMSNorm + RoPE library (libqknr.so).
+ *
+ * The operation, per token row t of a Q/K/V activation, follows two pages:
+ *
+ *  - "fused qknorm rope Flux 2.0" (TensorRT-Model-Connect PR #239, title
+ *    section): one fused call replaces each block's per-head RMSNorms and
+ *    the RoPEs that follow them; the kernel is templated on the activation
+ *    dtype (fp16 and bf16) and can be launched once per tensor.
+ *  - "VisualGen Wan: deduplicate shared RoPE SMEM staging" (TensorRT-LLM
+ *    PR #18036, Description and Test Coverage): one cos/sin row per token
+ *    is staged once and indexed by dimension for every head; the per-head
+ *    expanded table must give the same bits; the V slice is unchanged.
+ *
+ * For each head h of Q (gain gamma_q) and of K (gain gamma_k), with
+ * x = the head's D input values widened to fp32:
+ *
+ *     r    = rsqrt(sum_d x[d]^2 / D + eps)               (fp32)
+ *     y[d] = x[d] * r * gamma[d]
+ *     o[d] = y[d] * cos[d] + s(d) * y[p(d)] * sin[d]
+ *
+ * p(d) is d's rotation partner: d xor 1 for interleaved pairing, d +/- D/2
+ * for rotate-half.  s(d) is -1 for the first member of a pair (even d;
+ * d < D/2) and +1 for the second.  The result is rounded once, to nearest
+ * even, into the activation dtype.  V is either left alone or copied
+ * bit for bit.  The kernel evaluates o[d] as r * (x[d]*a[d] + x[p]*b[d])
+ * with a[d] = gamma[d]*cos[d] and b[d] = s(d)*gamma[p]*sin[d], each
+ * product rounded in fp32, so shared and expanded tables of equal values
+ * give bitwise-equal outputs.
+ *
+ * Ownership: the caller owns every buffer.  The library allocates no
+ * memory, never synchronises the stream, and keeps no state between calls
+ * beyond a per-kernel "max dynamic shared memory" attribute it sets once.
+ */
+#ifndef QKNR_H_
+#define QKNR_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+struct CUstream_st;
+typedef struct CUstream_st *qknr_stream_t;
+
+#define QKNR_ABI_VERSION 1
+
+typedef enum {
+  QKNR_BF16 = 0, /* activations or cos/sin */
+  QKNR_FP16 = 1, /* activations only */
+  QKNR_FP32 = 2  /* cos/sin only */
+} qknr_dtype;
+
+typedef enum {
+  QKNR_ROPE_INTERLEAVED = 0, /* pairs (2i, 2i+1) */
+  QKNR_ROPE_ROTATE_HALF = 1  /* pairs (i, i + D/2) */
+} qknr_rope_style;
+
+typedef enum {
+  /* cos, sin: [cos_rows, D]; token t reads row t % cos_rows for all heads */
+  QKNR_COS_SHARED_ROW = 0,
+  /* cos, sin: [cos_rows, H, D]; head h of Q and head h of K read [t % cos_rows, h] */
+  QKNR_COS_PER_HEAD_EXPANDED = 1
+} qknr_cos_layout;
+
+typedef enum {
+  QKNR_OK = 0,
+  QKNR_ERR_NULL = 1,        /* a required pointer is NULL */
+  QKNR_ERR_SHAPE = 2,       /* a size, count or stride is out of range */
+  QKNR_ERR_ALIGN = 3,       /* a base address or row stride is not 16-byte aligned */
+  QKNR_ERR_UNSUPPORTED = 4, /* valid request the library does not implement */
+  QKNR_ERR_CUDA = 5,        /* a CUDA runtime call failed; see qknr_last_error() */
+  QKNR_ERR_TIMEOUT = 6,     /* written to *dev_status by a kernel whose wait ran out */
+  QKNR_ERR_OVERLAP = 7,     /* an output partially overlaps an input */
+  QKNR_ERR_ABI = 8          /* args->abi_version != QKNR_ABI_VERSION */
+} qknr_status;
+
+/* Launch-time flags (qknr_args.flags). */
+#define QKNR_FLAG_TEST_STALL 0x1u /* test only: issue no loads, so every wait runs out
+                                     and the kernel reports QKNR_ERR_TIMEOUT */
+
+/*
+ * Arguments of one call.  Fill with qknr_args_init() and then set fields.
+ *
+ * Activations are row-major with one row per token; a row holds the heads
+ * of that tensor back to back (head h at elements [h*D, (h+1)*D)).
+ *  - Packed QKV [T, (Hq+Hk+Hv)*D]: q = base, k = base + Hq*D elements,
+ *    v = base + (Hq+Hk)*D elements, all three strides (Hq+Hk+Hv)*D.
+ *  - Separate tensors [T, H*D]: stride H*D (or 0, meaning H*D).
+ *  - Per-tensor launch (page 2's form): set only one of q / k and give the
+ *    other zero heads.
+ *
+ * Strides are in elements.  Every base address and every stride in bytes
+ * must be a multiple of 16 (QKNR_ERR_ALIGN otherwise).
+ *
+ * q_out / k_out NULL, or equal to q / k with the same stride, means in
+ * place.  V is copied only when v_out is non-NULL, differs from v and
+ * n_heads_v > 0; otherwise it is not touched.  An output that is not its
+ * own input must not overlap any input (QKNR_ERR_OVERLAP).
+ */
+typedef struct qknr_args {
+  uint32_t abi_version;       /* QKNR_ABI_VERSION */
+  int32_t dtype;              /* qknr_dtype of q, k, v and outputs: BF16 or FP16 */
+
+  const void *q, *k, *v;      /* device pointers; unused ones may be NULL */
+  void *q_out, *k_out, *v_out;
+  int64_t q_stride, k_stride, v_stride;             /* elements per row; 0 = H*D */
+  int64_t q_out_stride, k_out_stride, v_out_stride; /* elements per row; 0 = input's */
+
+  int64_t tokens;             /* rows T (batch * sequence); 0 is a no-op */
+  int32_t n_heads_q, n_heads_k, n_heads_v;          /* >= 0 */
+  int32_t head_dim;           /* D: 64 or 128 */
+
+  const float *gamma_q;       /* device fp32 [D]; required when n_heads_q > 0 */
+  const float *gamma_k;       /* device fp32 [D]; required when n_heads_k > 0 */
+  float eps;                  /* added to mean(x^2); default 1e-6 */
+
+  const void *cos, *sin;      /* device tables, see qknr_cos_layout */
+  int32_t cos_dtype;          /* FP32 or BF16 */
+  int32_t cos_layout;         /* qknr_cos_layout */
+  int64_t cos_rows;           /* table rows; 0 = tokens.  Row of token t: t % cos_rows */
+  int32_t rope_style;         /* qknr_rope_style */
+
+  /* Optional device int32.  A kernel whose bounded wait runs out writes a
+     nonzero qknr_status here (it never clears it; zero it before the call). */
+  int32_t *dev_status;
+
+  /* Launch tuning; 0 = automatic.  See qknr_query(). */
+  int32_t ctas_per_sm;        /* persistent CTAs per SM (1..4) */
+  int32_t stages;             /* shared-memory ring depth (2..16) */
+  int32_t consumer_warps;     /* compute warps per CTA (1..16) */
+  uint32_t flags;             /* QKNR_FLAG_* */
+  uint64_t wait_limit_ns;     /* bound on every in-kernel wait; 0 = 2 s */
+} qknr_args;
+
+/* What qknr_forward would launch for these arguments. */
+typedef struct qknr_launch_info {
+  int32_t grid;               /* CTAs (persistent) */
+  int32_t block;              /* threads per CTA: consumer warps + 1 producer warp */
+  int32_t dyn_smem;           /* dynamic shared memory per CTA, bytes */
+  int32_t stages;
+  int32_t ctas_per_sm;
+  int32_t consumer_warps;
+  int32_t stage_bytes;        /* bytes staged per token row */
+  int32_t registers;          /* registers per thread of the chosen kernel */
+  int32_t num_sms;
+  char kernel[96];            /* kernel variant name */
+} qknr_launch_info;
+
+/* Fill *a with defaults: zero pointers and sizes, eps 1e-6, bf16, fp32
+   shared-row cos/sin, interleaved, automatic tuning. */
+void qknr_args_init(qknr_args *a);
+
+/*
+ * Launch the fused QK-RMSNorm + RoPE on `stream` (asynchronous).
+ * Returns QKNR_OK after enqueueing, an argument error (nothing launched),
+ * or QKNR_ERR_CUDA if the launch failed.  Kernel-side wait timeouts are
+ * reported through args->dev_status only.
+ * Thread-safe.
+ */
+qknr_status qknr_forward(const qknr_args *args, qknr_stream_t stream);
+
+/* Validate *args and describe the launch without launching anything. */
+qknr_status qknr_query(const qknr_args *args, qknr_launch_info *info);
+
+/* Short English text of a status code (static storage). */
+const char *qknr_status_string(int32_t status);
+
+/* Message of the last error returned on this thread (static per thread). */
+const char *qknr_last_error(void);
+
+/* QKNR_ABI_VERSION of the built library. */
+int32_t qknr_abi_version(void);
+
+/* sizeof(qknr_args) and sizeof(qknr_launch_info) as compiled into the
+   library, so a binding can check its own copy of the layouts. */
+size_t qknr_sizeof_args(void);
+size_t qknr_sizeof_launch_info(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QKNR_H_ */

@@ -1,0 +1,161 @@
+"""The C-ABI library builds, loads and exports every declared symbol, and its
+host-side validation rejects bad arguments before any CUDA call.  Runs
+without a GPU: the pointers here are plain integers that are never touched
+because every call returns during validation."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from diffusion_transformer_qk_gb300 import qknr as Q
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "qknr.h")
+
+
+@pytest.fixture(scope="module")
+def lib(built_lib):
+    return Q.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(qknr_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_binding_exports():
+    assert sorted(Q.EXPORTS) == declared_functions()
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_struct_layouts_match(lib):
+    assert lib.qknr_sizeof_args() == ctypes.sizeof(Q.QknrArgs)
+    assert lib.qknr_sizeof_launch_info() == ctypes.sizeof(Q.QknrLaunchInfo)
+    assert lib.qknr_abi_version() == Q.ABI_VERSION
+
+
+def test_args_init_defaults(lib):
+    a = Q.QknrArgs()
+    ctypes.memset(ctypes.byref(a), 0xFF, ctypes.sizeof(a))
+    lib.qknr_args_init(ctypes.byref(a))
+    assert a.abi_version == Q.ABI_VERSION
+    assert a.dtype == Q.BF16 and a.cos_dtype == Q.FP32
+    assert abs(a.eps - 1e-6) < 1e-12
+    assert a.q is None and a.tokens == 0 and a.stages == 0 and a.wait_limit_ns == 0
+
+
+def test_status_strings(lib):
+    for code, name in Q.STATUS.items():
+        s = lib.qknr_status_string(code).decode()
+        assert s and s != "unknown status", name
+    assert lib.qknr_status_string(99).decode() == "unknown status"
+
+
+FAKE = 1 << 40        # 16-byte aligned addresses that are never dereferenced
+
+
+def valid_packed(T=64, H=4, D=128):
+    """Args for an in-place packed call with fake device pointers."""
+    a = Q.QknrArgs()
+    Q.load().qknr_args_init(ctypes.byref(a))
+    row = 3 * H * D
+    a.q, a.k, a.v = FAKE, FAKE + H * D * 2, FAKE + 2 * H * D * 2
+    a.q_stride = a.k_stride = a.v_stride = row
+    a.tokens = T
+    a.n_heads_q = a.n_heads_k = a.n_heads_v = H
+    a.head_dim = D
+    a.gamma_q, a.gamma_k = FAKE + (1 << 30), FAKE + (1 << 30) + 4096
+    a.cos, a.sin = FAKE + (2 << 30), FAKE + (3 << 30)
+    return a
+
+
+def call(lib, a):
+    st = lib.qknr_forward(ctypes.byref(a), None)
+    return st, lib.qknr_last_error().decode()
+
+
+def test_null_args(lib):
+    assert lib.qknr_forward(None, None) == 1
+
+
+@pytest.mark.parametrize("mutate,expect", [
+    (lambda a: setattr(a, "abi_version", 7), 8),
+    (lambda a: setattr(a, "head_dim", 96), 4),
+    (lambda a: setattr(a, "dtype", 2), 4),
+    (lambda a: setattr(a, "cos_dtype", 1), 4),
+    (lambda a: setattr(a, "rope_style", 5), 4),
+    (lambda a: setattr(a, "cos_layout", 3), 4),
+    (lambda a: setattr(a, "tokens", -1), 2),
+    (lambda a: setattr(a, "n_heads_k", -2), 2),
+    (lambda a: setattr(a, "stages", 1), 2),
+    (lambda a: setattr(a, "stages", 17), 2),
+    (lambda a: setattr(a, "consumer_warps", 17), 2),
+    (lambda a: setattr(a, "ctas_per_sm", 5), 2),
+    (lambda a: setattr(a, "eps", -1.0), 2),
+    (lambda a: setattr(a, "gamma_q", None), 1),
+    (lambda a: setattr(a, "k", None), 1),
+    (lambda a: setattr(a, "cos", None), 1),
+    (lambda a: setattr(a, "q_stride", 100), 2),            # < heads * D
+    (lambda a: setattr(a, "q", FAKE + 8), 3),              # not 16-byte aligned
+    (lambda a: setattr(a, "q_stride", 3 * 4 * 128 + 4), 3),  # 8-byte row stride
+    (lambda a: setattr(a, "sin", FAKE + (3 << 30) + 4), 3),
+    (lambda a: setattr(a, "gamma_k", FAKE + (1 << 30) + 2), 3),
+    (lambda a: setattr(a, "cos_rows", -3), 2),
+])
+def test_validation_rejects(lib, mutate, expect):
+    a = valid_packed()
+    mutate(a)
+    st, msg = call(lib, a)
+    assert st == expect, (st, msg)
+    assert msg
+
+
+def test_expanded_layout_needs_equal_head_counts(lib):
+    a = valid_packed()
+    a.cos_layout = 1
+    a.n_heads_k = 2
+    assert call(lib, a)[0] == 2
+
+
+def test_out_of_place_output_overlapping_an_input_is_rejected(lib):
+    a = valid_packed()
+    a.q_out = FAKE + 4 * 128 * 2          # lands on K
+    assert call(lib, a)[0] == 7
+    b = valid_packed()
+    b.q_out = FAKE
+    b.q_out_stride = 4 * 128              # same base, different stride
+    assert call(lib, b)[0] == 7
+    c = valid_packed()
+    c.v_out = c.cos                        # V copied onto the cos table
+    assert call(lib, c)[0] == 7
+
+
+def test_nothing_to_do_returns_ok_without_cuda(lib):
+    # zero tokens, or no heads and no V copy: OK before any device query
+    a = valid_packed(T=0)
+    assert call(lib, a)[0] == 0
+    b = valid_packed()
+    b.n_heads_q = b.n_heads_k = 0
+    b.gamma_q = b.gamma_k = None
+    assert call(lib, b)[0] == 0          # V untouched (v_out NULL): no work
+
+
+def test_query_validates_too(lib):
+    info = Q.QknrLaunchInfo()
+    a = valid_packed()
+    a.head_dim = 32
+    assert lib.qknr_query(ctypes.byref(a), ctypes.byref(info)) == 4
+    b = valid_packed(T=0)
+    assert lib.qknr_query(ctypes.byref(b), ctypes.byref(info)) == 0
+    assert info.grid == 0 and "qknr_fused<bf16,fp32,D128,interleaved,shared>" == info.kernel.decode()
+
+
+def test_product_path_fails_loudly_without_library(tmp_path):
+    with pytest.raises(RuntimeError):
+        Q.load(str(tmp_path / "libqknr.so"))

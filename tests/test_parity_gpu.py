@@ -1,0 +1,192 @@
+"""CUDA path vs the fp64 oracle on the seeded workloads, through the C ABI.
+
+Small workloads are compared element by element; the full-size Wan and
+FLUX.2 workloads (in the launch configuration the benchmark times) are
+compared on sampled token rows, and every output is checked for the
+properties that hold at any size: V bit-exact, shared vs expanded tables
+bitwise equal, in place vs out of place bitwise equal.
+"""
+import numpy as np
+import pytest
+import torch
+
+from diffusion_transformer_qk_gb300 import inputs as I
+from diffusion_transformer_qk_gb300 import qknr as Q
+from oracle import qknr_oracle as O
+from tests.gpu_util import TOL, compare, table_to_dev, to_bits, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(built_lib, cuda_device):
+    Q.load()
+    Q.status_buffer().zero_()
+    yield
+    assert Q.read_status() == 0, "a kernel reported a wait timeout"
+
+
+def sample_rows(T, n, seed=0):
+    g = np.random.Generator(np.random.PCG64(seed))
+    fixed = [0, 1, T // 2, T - 2, T - 1]
+    rows = np.unique(np.concatenate([[r for r in fixed if 0 <= r < T], g.choice(T, size=min(n, T), replace=False)]))
+    return rows
+
+
+def run_packed(w, inp, *, out=False, cos_layout=None, dev_tabs=None, **kw):
+    """Launch on a device copy of inp['qkv']; returns (result tensor, input tensor)."""
+    qkv = to_dev(inp["qkv"], w.dtype)
+    gq = torch.from_numpy(inp["gamma_q"]).cuda()
+    gk = torch.from_numpy(inp["gamma_k"]).cuda()
+    if dev_tabs is None:
+        cos = table_to_dev(inp["cos"], w.cos_dtype)
+        sin = table_to_dev(inp["sin"], w.cos_dtype)
+    else:
+        cos, sin = dev_tabs
+    layout = cos_layout or w.cos_layout
+    o = torch.empty_like(qkv) if out else None
+    res = Q.qk_norm_rope_packed(qkv, w.n_heads_q, w.n_heads_k, w.n_heads_v, w.head_dim, gq, gk, cos, sin,
+                                out=o, rope_style=w.rope_style, cos_layout=layout, eps=w.eps, **kw)
+    torch.cuda.synchronize()
+    return res, qkv
+
+
+def oracle_packed(w, inp, rows=None, cos_layout="shared_row", tables=None):
+    cos, sin = (inp["cos"], inp["sin"]) if tables is None else tables
+    return O.forward_packed(inp["qkv"], w.dtype, w.n_heads_q, w.n_heads_k, w.n_heads_v, w.head_dim,
+                            inp["gamma_q"], inp["gamma_k"], w.eps, cos, sin, w.cos_dtype, w.rope_style,
+                            cos_layout, rows=rows)
+
+
+def check_packed(w, got_bits, inp, rows=None):
+    """Compare Q/K of a packed result with the oracle; V bitwise."""
+    ref = oracle_packed(w, inp, rows)
+    D, hq, hk = w.head_dim, w.n_heads_q, w.n_heads_k
+    g = got_bits if rows is None else got_bits[rows]
+    mq, fq = compare(g[:, : hq * D], ref["q"], w.dtype, "Q")
+    mk, fk = compare(g[:, hq * D:(hq + hk) * D], ref["k"], w.dtype, "K")
+    np.testing.assert_array_equal(g[:, (hq + hk) * D:], ref["v"])
+    return max(mq, mk), max(fq, fk)
+
+
+# ---------------------------------------------------------------------------
+# the tiny and 4096-token workloads, element by element
+
+def test_tiny_workload_full():
+    w = I.WORKLOADS["tiny_256x24x64"]
+    inp = I.make_inputs(w)
+    res, _ = run_packed(w, inp)
+    m, f = check_packed(w, to_bits(res), inp)
+    assert m <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_dense_4096_full(dtype):
+    w = I.WORKLOADS["dense_4096x24x128"].with_(dtype=dtype)
+    inp = I.make_inputs(w)
+    res, _ = run_packed(w, inp)
+    m, f = check_packed(w, to_bits(res), inp)
+    assert m <= TOL[dtype] and f < 0.02
+
+
+# ---------------------------------------------------------------------------
+# full-size Wan: sampled rows vs oracle, plus bitwise properties
+
+@pytest.fixture(scope="module")
+def wan():
+    w = I.WORKLOADS["wan_32760x40x128"]
+    return w, I.make_inputs(w)
+
+
+def test_wan_shared_fp32_sampled(wan):
+    w, inp = wan
+    res, _ = run_packed(w, inp)
+    bits = to_bits(res)
+    rows = sample_rows(w.tokens, 160)
+    m, f = check_packed(w, bits, inp, rows)
+    # V is untouched everywhere
+    D3 = 2 * w.n_heads_q * w.head_dim
+    np.testing.assert_array_equal(bits[:, D3:], inp["qkv"][:, D3:])
+
+
+@pytest.mark.parametrize("style", ["interleaved", "rotate_half"])
+@pytest.mark.parametrize("cos_dtype", ["fp32", "bf16"])
+def test_wan_expanded_bitwise_equals_shared(wan, style, cos_dtype):
+    w0, inp0 = wan
+    w = w0.with_(rope_style=style, cos_dtype=cos_dtype)
+    inp = dict(inp0)
+    inp["cos"], inp["sin"] = I.rope_table(w)
+    shared, _ = run_packed(w, inp)
+    cos = table_to_dev(inp["cos"], cos_dtype)
+    sin = table_to_dev(inp["sin"], cos_dtype)
+    H = w.n_heads_q
+    ce = cos[:, None, :].expand(cos.shape[0], H, w.head_dim).contiguous()
+    se = sin[:, None, :].expand(sin.shape[0], H, w.head_dim).contiguous()
+    expanded, _ = run_packed(w, inp, cos_layout="per_head_expanded", dev_tabs=(ce, se))
+    assert torch.equal(shared.view(torch.int16), expanded.view(torch.int16))
+    del ce, se, expanded
+    rows = sample_rows(w.tokens, 48, seed=1)
+    check_packed(w, to_bits(shared), inp, rows)
+
+
+def test_wan_out_of_place_equals_in_place_and_copies_v(wan):
+    w, inp = wan
+    inplace, _ = run_packed(w, inp)
+    outp, src = run_packed(w, inp, out=True)
+    assert torch.equal(inplace.view(torch.int16), outp.view(torch.int16))
+    # the input buffer is untouched when writing elsewhere
+    np.testing.assert_array_equal(to_bits(src), inp["qkv"])
+
+
+# ---------------------------------------------------------------------------
+# FLUX.2: separate Q, K, V, per-tensor launches, batch-broadcast table
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_flux_per_tensor_sampled(dtype):
+    w = I.WORKLOADS["flux2_2x4608x48x128"].with_(dtype=dtype)
+    inp = I.make_inputs(w)
+    D, H = w.head_dim, w.n_heads_q
+    q, k, v = (to_dev(inp[n], dtype) for n in ("q", "k", "v"))
+    gq = torch.from_numpy(inp["gamma_q"]).cuda()
+    gk = torch.from_numpy(inp["gamma_k"]).cuda()
+    cos = table_to_dev(inp["cos"], "fp32")
+    sin = table_to_dev(inp["sin"], "fp32")
+    Q.qk_norm_rope_tensor(q, H, D, gq, cos, sin, rope_style=w.rope_style)
+    Q.qk_norm_rope_tensor(k, H, D, gk, cos, sin, rope_style=w.rope_style)
+    torch.cuda.synchronize()
+    rows = sample_rows(w.tokens, 128, seed=2)
+    rows = np.unique(np.concatenate([rows, [511, 512, 4607, 4608, 4608 + 511, 4608 + 512]]))
+    for name, t, g in (("q", q, inp["gamma_q"]), ("k", k, inp["gamma_k"])):
+        ref = O.forward_separate(inp[name], dtype, H, D, g, w.eps, inp["cos"], inp["sin"], "fp32",
+                                 w.rope_style, rows=rows)
+        compare(to_bits(t)[rows], ref, dtype, name)
+    np.testing.assert_array_equal(to_bits(v), inp["v"])
+    # the single-launch Q+K form gives the same bits as two per-tensor launches
+    q2, k2 = to_dev(inp["q"], dtype), to_dev(inp["k"], dtype)
+    v_out = torch.empty_like(v)
+    Q.qk_norm_rope_separate(q2, k2, H, D, gq, gk, cos, sin, v=v, v_out=v_out, rope_style=w.rope_style)
+    torch.cuda.synchronize()
+    assert torch.equal(q2.view(torch.int16), q.view(torch.int16))
+    assert torch.equal(k2.view(torch.int16), k.view(torch.int16))
+    assert torch.equal(v_out.view(torch.int16), v.view(torch.int16))
+
+
+# ---------------------------------------------------------------------------
+# page 1's layout-parity matrix: 2 styles x (24,64), (24,128), (40,128),
+# rtol = atol = 0, with an unchanged V slice
+
+@pytest.mark.parametrize("style", ["interleaved", "rotate_half"])
+@pytest.mark.parametrize("H,D", [(24, 64), (24, 128), (40, 128)])
+def test_shared_fp32_matches_expanded_matrix(style, H, D):
+    w = I.Workload("parity", 1, 301, H, H, H, D, "bf16", True, style, "fp32", "shared_row", "1d", (), (D,),
+                   seed=7)
+    inp = I.make_inputs(w)
+    shared, _ = run_packed(w, inp)
+    ce = I.expand_per_head(inp["cos"], H)
+    se = I.expand_per_head(inp["sin"], H)
+    expanded, _ = run_packed(w, inp, cos_layout="per_head_expanded",
+                             dev_tabs=(torch.from_numpy(ce).cuda(), torch.from_numpy(se).cuda()))
+    sb, eb = to_bits(shared), to_bits(expanded)
+    np.testing.assert_array_equal(sb, eb)
+    np.testing.assert_array_equal(sb[:, 2 * H * D:], inp["qkv"][:, 2 * H * D:])
+    check_packed(w, sb, inp)
