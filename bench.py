@@ -198,7 +198,7 @@ def oracle_rows(w, inp, rows):
             for n, h, g in (("q", w.n_heads_q, "gamma_q"), ("k", w.n_heads_k, "gamma_k"))]
 
 
-def time_oracle_workload(w, inp, target_s: float):
+def time_oracle_workload(w, inp, target_s: float, tokens: int):
     """Time the oracle on the first token rows, as many as take about
     target_s seconds; returns (us per full call, rows, seconds).  The
     expanded-layout workloads hold equal values in every head's table row,
@@ -212,7 +212,7 @@ def time_oracle_workload(w, inp, target_s: float):
     t0 = time.perf_counter()
     oracle_rows(w, inp, np.arange(n))
     dt = time.perf_counter() - t0
-    return dt / n * w.tokens * 1e6, n, dt
+    return dt / n * tokens * 1e6, n, dt
 
 
 # ---------------------------------------------------------------------------
@@ -256,9 +256,9 @@ def run_reference(args, w):
     return 0
 
 
-def workload_config(w, world):
+def workload_config(w, world, tokens=None):
     return {
-        "workload": w.name, "tokens": w.tokens, "n_heads_q": w.n_heads_q, "n_heads_k": w.n_heads_k,
+        "workload": w.name, "tokens": w.tokens if tokens is None else tokens, "n_heads_q": w.n_heads_q, "n_heads_k": w.n_heads_k,
         "n_heads_v": w.n_heads_v, "head_dim": w.head_dim, "layout": "packed_qkv" if w.packed else "separate",
         "rope": w.rope_style, "cos_layout": w.cos_layout, "cos_dtype": w.cos_dtype,
         "rope_axes": list(w.axes_dim), "in_place": True,
@@ -275,13 +275,14 @@ class Runner:
     a packed QKV activation, one per tensor (Q, then K) for FLUX.2's
     separate tensors."""
 
-    def __init__(self, w, dev, tune, status):
+    def __init__(self, w, dev, tune, status, tokens=None):
         import torch
 
         from diffusion_transformer_qk_gb300 import qknr as Q
 
         self.Q, self.w, self.dev = Q, w, dev
-        inp = I.make_inputs(w)
+        self.tokens = w.tokens if tokens is None else tokens
+        inp = I.make_inputs(w, tokens=self.tokens)
         self.inp = inp
         D = w.head_dim
 
@@ -314,14 +315,14 @@ class Runner:
         if w.packed:
             self.args = [Q.packed_args(d["qkv"], w.n_heads_q, w.n_heads_k, w.n_heads_v, D, d["gamma_q"],
                                        d["gamma_k"], d["cos"], d["sin"], **kw)]
-            self.bytes_per_launch = I.algorithmic_bytes(w)
+            self.bytes_per_launch = I.algorithmic_bytes(w, tokens=self.tokens)
             self.outputs = ["qkv"]
         else:
             self.args = [Q.make_args(q=d["q"], n_heads_q=w.n_heads_q, head_dim=D, gamma_q=d["gamma_q"],
                                      cos=d["cos"], sin=d["sin"], **kw),
                          Q.make_args(k=d["k"], n_heads_k=w.n_heads_k, head_dim=D, gamma_k=d["gamma_k"],
                                      cos=d["cos"], sin=d["sin"], **kw)]
-            self.bytes_per_launch = I.algorithmic_bytes(w, launches="q")
+            self.bytes_per_launch = I.algorithmic_bytes(w, launches="q", tokens=self.tokens)
             self.outputs = ["q", "k"]
         self.info = Q.query(self.args[0])
 
@@ -364,7 +365,7 @@ def run_ours(args, w):
 
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     tune = dict(ctas_per_sm=args.ctas_per_sm, stages=args.stages, consumer_warps=args.consumer_warps)
-    run = Runner(w, dev, tune, status)
+    run = Runner(w, dev, tune, status, args.tokens)
     stream = torch.cuda.current_stream(dev)
     L = len(run.args)
 
@@ -449,7 +450,7 @@ def run_ours(args, w):
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": max_elapsed * 1e3 / K, "higher_is_better": False, "scaling": "weak",
-        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic", "config": workload_config(w, world),
+        "vs_baseline": None, "dtype": w.dtype, "data": "synthetic", "config": workload_config(w, world, run.tokens),
         "gbs": run.bytes_per_launch * L * K * world / max_elapsed / 1e9,
         "pct_of_hbm_peak": 100.0 * achieved / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
@@ -464,10 +465,10 @@ def run_ours(args, w):
     if e2e:
         line["e2e"] = e2e
     if world == 1 and not args.no_cpu_baseline:
-        us, n, dt = time_oracle_workload(w, run.inp, args.cpu_seconds)
+        us, n, dt = time_oracle_workload(w, run.inp, args.cpu_seconds, run.tokens)
         line["cpu_baseline"] = {"value": us, "unit": UNIT, "cores": 1, "kind": "oracle",
                                 "sample": f"first {n} of {w.tokens} token rows, {dt:.1f} s, fp64 numpy, "
-                                          f"1 thread, scaled to a full call by tokens"}
+                                          f"1 thread, scaled to a full call of {run.tokens} rows by tokens"}
     print(json.dumps(line), flush=True)
     return 0
 
@@ -479,6 +480,8 @@ def main(argv=None):
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(I.WORKLOADS))
+    p.add_argument("--tokens", type=int, default=None,
+                   help="run the first N token rows of the workload (small profiling cases)")
     p.add_argument("--ctas-per-sm", type=int, default=0)
     p.add_argument("--stages", type=int, default=0)
     p.add_argument("--consumer-warps", type=int, default=0)

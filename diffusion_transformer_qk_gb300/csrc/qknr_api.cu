@@ -255,6 +255,8 @@ qknr_status make_plan(const qknr_args* a, Plan* pl) {
   kp.hk = hk;
   kp.hv = hv;
   kp.flags = a->flags;
+  kp.qk_merged = hq > 0 && hk > 0 && static_cast<const char*>(k) == static_cast<const char*>(q) + q_bytes &&
+                 ks == qs;
   kp.off_k = q_bytes;
   kp.off_v = q_bytes + k_bytes;
   kp.off_cos = q_bytes + k_bytes + v_bytes;
@@ -277,7 +279,10 @@ qknr_status size_launch(const qknr_args* a, Plan* pl) {
   if (st != QKNR_OK) return st;
   pl->num_sms = di.num_sms;
 
-  const int warps = a->consumer_warps ? a->consumer_warps : 8;
+  // Defaults from sweeps on GB300: 12 consumer warps keep enough passes in
+  // flight to cover shuffle and rsqrt latencies; one CTA per SM (more do
+  // not fit beside 12 warps' registers) with about 128 KB of ring.
+  const int warps = a->consumer_warps ? a->consumer_warps : 12;
   const int cps = a->ctas_per_sm ? a->ctas_per_sm : 1;
   const long long stage_bytes = pl->kp.stage_bytes;
   // shared memory one CTA may use when `cps` CTAs share an SM
@@ -287,7 +292,10 @@ qknr_status size_launch(const qknr_args* a, Plan* pl) {
   const long long fit = ring > 0 ? ring / stage_bytes : 0;
   int stages = a->stages;
   if (stages == 0) {
-    stages = static_cast<int>(fit < qknr::kMaxStages ? fit : qknr::kMaxStages);
+    long long want = (128 * 1024) / stage_bytes;
+    if (want < 4) want = 4;
+    if (want > qknr::kMaxStages) want = qknr::kMaxStages;
+    stages = static_cast<int>(fit < want ? fit : want);
     // no deeper than the rows one CTA will see
     const long long grid0 = (long long)di.num_sms * cps;
     const long long rows_per_cta = (a->tokens + grid0 - 1) / grid0;
@@ -308,6 +316,20 @@ qknr_status size_launch(const qknr_args* a, Plan* pl) {
   if (grid > a->tokens) grid = a->tokens;
   pl->kp.stages = stages;
   pl->kp.consumer_warps = warps;
+  // split the consumer warps between Q and K in proportion to their passes
+  const int hpw = 32 / (a->head_dim / 8);
+  const int nq = (pl->kp.hq + hpw - 1) / hpw, nk = (pl->kp.hk + hpw - 1) / hpw;
+  if (nq == 0 || nk == 0) {
+    pl->kp.warps_q = nq ? warps : 0;
+    pl->kp.warps_k = nk ? warps : 0;
+  } else if (warps == 1) {
+    pl->kp.warps_q = pl->kp.warps_k = 1;
+  } else {
+    int wq = static_cast<int>((static_cast<long long>(warps) * nq + (nq + nk) / 2) / (nq + nk));
+    wq = wq < 1 ? 1 : (wq > warps - 1 ? warps - 1 : wq);
+    pl->kp.warps_q = wq;
+    pl->kp.warps_k = warps - wq;
+  }
   pl->grid = static_cast<int>(grid);
   pl->block = block;
   pl->smem = static_cast<int>(smem);

@@ -12,7 +12,9 @@
 // so a head of D dims spans LPH = D/8 lanes and a warp covers HPW = 32/LPH
 // heads at once.  The per-head sum of squares is a shuffle-xor reduction
 // inside those LPH lanes; a rotate-half partner lives in lane ^ (LPH/2),
-// an interleaved partner in the same lane.
+// an interleaved partner in the same lane.  Consumer warps are split
+// between Q and K heads, so each folds only its own tensor's gain, and a
+// warp works on two passes of heads at a time to overlap their latencies.
 //
 // cos/sin (page 1, "VisualGen Wan: deduplicate shared RoPE SMEM staging",
 // Description): the shared layout stages one row per token and every head
@@ -72,7 +74,9 @@ struct KernelParams {
   float inv_d;
   int hq, hk, hv;                                    // hv: V heads copied (0: V untouched)
   int consumer_warps;
+  int warps_q, warps_k;                              // consumer warps on Q heads / on K heads
   int stages;
+  int qk_merged;                                     // K directly follows Q: one copy for both
   unsigned flags;
   // stage layout: [Q heads | K heads | V heads | cos row | sin row]
   unsigned off_k, off_v, off_cos, off_sin;
@@ -134,21 +138,6 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       : "memory");
 }
 
-__device__ __forceinline__ uint4 lds128(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "r"(addr)
-               : "memory");
-  return v;
-}
-
-__device__ __forceinline__ void stg128(void* ptr, uint4 v) {
-  asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(ptr), "r"(v.x), "r"(v.y),
-               "r"(v.z), "r"(v.w)
-               : "memory");
-}
-
 // Wait for phase `parity` of `bar` to complete, giving up at the deadline
 // or when another warp of the CTA has aborted.  Returns false on give-up.
 static __device__ __noinline__ bool bounded_wait(uint32_t bar, uint32_t parity,
@@ -170,26 +159,32 @@ static __device__ __noinline__ bool bounded_wait(uint32_t bar, uint32_t parity,
 }
 
 // ---------------------------------------------------------------------------
-// element conversions (16 bytes of storage <-> 8 fp32 values)
+// element conversions: 16 bytes of storage <-> 4 fp32 pairs (elements 2i, 2i+1)
+// Arithmetic runs on Blackwell's paired fp32 instructions (__ffma2_rn and
+// friends), each half rounded exactly as the scalar instruction would.
 
 template <typename T>
 struct Elem;
 
 template <>
 struct Elem<__nv_bfloat16> {
-  static __device__ __forceinline__ void unpack(const uint4& r, float (&x)[8]) {
+  // X[i] = (x[2i], x[2i+1])
+  static __device__ __forceinline__ void unpack(const uint4& r, float2 (&X)[4]) {
     const uint32_t w[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      x[2 * i] = __uint_as_float(w[i] << 16);
-      x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-    }
+    for (int i = 0; i < 4; ++i) X[i] = make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
   }
-  static __device__ __forceinline__ uint4 pack(const float (&o)[8]) {
+  // X[i] = (x[2i+1], x[2i])
+  static __device__ __forceinline__ void unpack_swapped(const uint4& r, float2 (&X)[4]) {
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) X[i] = make_float2(__uint_as_float(w[i] & 0xffff0000u), __uint_as_float(w[i] << 16));
+  }
+  static __device__ __forceinline__ uint4 pack(const float2 (&O)[4]) {
     uint32_t w[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      __nv_bfloat162 h = __floats2bfloat162_rn(o[2 * i], o[2 * i + 1]);
+      __nv_bfloat162 h = __floats2bfloat162_rn(O[i].x, O[i].y);
       w[i] = *reinterpret_cast<uint32_t*>(&h);
     }
     return make_uint4(w[0], w[1], w[2], w[3]);
@@ -198,43 +193,45 @@ struct Elem<__nv_bfloat16> {
 
 template <>
 struct Elem<__half> {
-  static __device__ __forceinline__ void unpack(const uint4& r, float (&x)[8]) {
+  static __device__ __forceinline__ void unpack(const uint4& r, float2 (&X)[4]) {
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) X[i] = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+  }
+  static __device__ __forceinline__ void unpack_swapped(const uint4& r, float2 (&X)[4]) {
     const uint32_t w[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      __half2 h = *reinterpret_cast<const __half2*>(&w[i]);
-      float2 f = __half22float2(h);
-      x[2 * i] = f.x;
-      x[2 * i + 1] = f.y;
+      const __half2 h = *reinterpret_cast<const __half2*>(&w[i]);
+      X[i] = make_float2(__high2float(h), __low2float(h));
     }
   }
-  static __device__ __forceinline__ uint4 pack(const float (&o)[8]) {
+  static __device__ __forceinline__ uint4 pack(const float2 (&O)[4]) {
     uint32_t w[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      __half2 h = __floats2half2_rn(o[2 * i], o[2 * i + 1]);
+      __half2 h = __floats2half2_rn(O[i].x, O[i].y);
       w[i] = *reinterpret_cast<uint32_t*>(&h);
     }
     return make_uint4(w[0], w[1], w[2], w[3]);
   }
 };
 
-// 8 consecutive cos (or sin) values from shared memory, widened to fp32.
+// 8 consecutive cos (or sin) values from shared memory, widened to fp32 pairs.
 template <typename CT>
-__device__ __forceinline__ void load_table8(uint32_t addr, float (&c)[8]);
+__device__ __forceinline__ void load_table8(const unsigned char* p, float2 (&c)[4]);
 
 template <>
-__device__ __forceinline__ void load_table8<float>(uint32_t addr, float (&c)[8]) {
-  const uint4 a = lds128(addr), b = lds128(addr + 16);
-  c[0] = __uint_as_float(a.x); c[1] = __uint_as_float(a.y);
-  c[2] = __uint_as_float(a.z); c[3] = __uint_as_float(a.w);
-  c[4] = __uint_as_float(b.x); c[5] = __uint_as_float(b.y);
-  c[6] = __uint_as_float(b.z); c[7] = __uint_as_float(b.w);
+__device__ __forceinline__ void load_table8<float>(const unsigned char* p, float2 (&c)[4]) {
+  const float4 a = *reinterpret_cast<const float4*>(p);
+  const float4 b = *reinterpret_cast<const float4*>(p + 16);
+  c[0] = make_float2(a.x, a.y); c[1] = make_float2(a.z, a.w);
+  c[2] = make_float2(b.x, b.y); c[3] = make_float2(b.z, b.w);
 }
 
 template <>
-__device__ __forceinline__ void load_table8<__nv_bfloat16>(uint32_t addr, float (&c)[8]) {
-  Elem<__nv_bfloat16>::unpack(lds128(addr), c);
+__device__ __forceinline__ void load_table8<__nv_bfloat16>(const unsigned char* p, float2 (&c)[4]) {
+  Elem<__nv_bfloat16>::unpack(*reinterpret_cast<const uint4*>(p), c);
 }
 
 // ---------------------------------------------------------------------------
@@ -244,61 +241,152 @@ template <int D, bool RH>
 struct Geometry {
   static constexpr int LPH = D / 8;       // lanes per head
   static constexpr int HPW = 32 / LPH;    // heads per warp pass
-  // dimension of the partner of element j of a lane starting at d0
-  static __device__ __forceinline__ int partner_dim(int d0, int j) {
-    return RH ? ((d0 + D / 2) % D) + j : d0 + (j ^ 1);
-  }
   // true when element j of the lane is the first member of its pair
   static __device__ __forceinline__ bool first_member(int d0, int j) {
     return RH ? (d0 < D / 2) : ((j & 1) == 0);
   }
 };
 
-// a[j] = g[d]*c[j]; b[j] = s(d) * g[p(d)] * s[j]  (each product rounded in fp32)
+// a[j] = g[d]*c[j]; b[j] = s(d) * g[p(d)] * s[j]  (each product rounded in fp32),
+// held as pairs A[i] = (a[2i], a[2i+1]).  gamma points at the tensor's gains
+// in shared memory.
 template <int D, bool RH>
-__device__ __forceinline__ void fold_coefficients(const float* gamma, int d0, const float (&c)[8],
-                                                  const float (&s)[8], float (&a)[8],
-                                                  float (&b)[8]) {
+__device__ __forceinline__ void fold_coefficients(const float* gamma, int d0, const float2 (&C)[4],
+                                                  const float2 (&Sn)[4], float2 (&A)[4], float2 (&B)[4]) {
+  const float4 g0 = *reinterpret_cast<const float4*>(gamma + d0);
+  const float4 g1 = *reinterpret_cast<const float4*>(gamma + d0 + 4);
+  const float2 G[4] = {make_float2(g0.x, g0.y), make_float2(g0.z, g0.w), make_float2(g1.x, g1.y),
+                       make_float2(g1.z, g1.w)};
+  float2 GP[4];
+  if (RH) {
+    const int pd = (d0 + D / 2) % D;
+    const float4 p0 = *reinterpret_cast<const float4*>(gamma + pd);
+    const float4 p1 = *reinterpret_cast<const float4*>(gamma + pd + 4);
+    GP[0] = make_float2(p0.x, p0.y); GP[1] = make_float2(p0.z, p0.w);
+    GP[2] = make_float2(p1.x, p1.y); GP[3] = make_float2(p1.z, p1.w);
+  } else {
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const float g = gamma[d0 + j];
-    const float gp = gamma[Geometry<D, RH>::partner_dim(d0, j)];
-    a[j] = __fmul_rn(g, c[j]);
-    const float t = __fmul_rn(gp, s[j]);
-    b[j] = Geometry<D, RH>::first_member(d0, j) ? -t : t;
+    for (int i = 0; i < 4; ++i) GP[i] = make_float2(G[i].y, G[i].x);
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    A[i] = __fmul2_rn(G[i], C[i]);
+    const float2 t = __fmul2_rn(GP[i], Sn[i]);
+    // first pair members take -partner*sin: even dims (interleaved), the
+    // lower half (rotate-half)
+    if (RH)
+      B[i] = d0 < D / 2 ? make_float2(-t.x, -t.y) : t;
+    else
+      B[i] = make_float2(-t.x, t.y);
   }
 }
 
 // Normalise and rotate the 8 elements this lane holds of one head (raw
-// storage in `raw`), giving fp32 outputs in `o`.  Every lane of the warp
-// must call it: the reductions and the partner exchange shuffle the warp.
+// storage in `raw`), giving fp32 outputs O[i] = (o[2i], o[2i+1]).  Every
+// lane of the warp must call it: the reduction and the partner exchange
+// shuffle the warp.
 template <typename T, int D, bool RH>
-__device__ __forceinline__ void head_math(const uint4& raw, const float (&a)[8], const float (&b)[8],
-                                          float eps, float inv_d, float (&o)[8]) {
+__device__ __forceinline__ void head_math(const uint4& raw, const float2 (&A)[4], const float2 (&B)[4],
+                                          float eps, float inv_d, float2 (&O)[4]) {
   constexpr int LPH = Geometry<D, RH>::LPH;
-  float x[8];
-  Elem<T>::unpack(raw, x);
-  // sum of squares: fixed order inside the lane, then a butterfly over the head's lanes
-  float ss = __fmul_rn(x[0], x[0]);
-#pragma unroll
-  for (int j = 1; j < 8; ++j) ss = __fmaf_rn(x[j], x[j], ss);
+  float2 X[4];
+  Elem<T>::unpack(raw, X);
+  // sum of squares: even and odd elements in two fixed-order chains, then a
+  // butterfly over the head's lanes
+  float2 S2 = __fmul2_rn(X[0], X[0]);
+  S2 = __ffma2_rn(X[1], X[1], S2);
+  S2 = __ffma2_rn(X[2], X[2], S2);
+  S2 = __ffma2_rn(X[3], X[3], S2);
+  float ss = __fadd_rn(S2.x, S2.y);
 #pragma unroll
   for (int off = LPH / 2; off >= 1; off >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, off));
   const float r = rsqrtf(__fmaf_rn(ss, inv_d, eps));
-  float xp[8];
+  const float2 R = make_float2(r, r);
+  // XP[i] holds the rotation partners of X[i]
+  float2 XP[4];
   if (RH) {
     uint4 pr;
     pr.x = __shfl_xor_sync(0xffffffffu, raw.x, LPH / 2);
     pr.y = __shfl_xor_sync(0xffffffffu, raw.y, LPH / 2);
     pr.z = __shfl_xor_sync(0xffffffffu, raw.z, LPH / 2);
     pr.w = __shfl_xor_sync(0xffffffffu, raw.w, LPH / 2);
-    Elem<T>::unpack(pr, xp);
+    Elem<T>::unpack(pr, XP);
   } else {
-#pragma unroll
-    for (int j = 0; j < 8; ++j) xp[j] = x[j ^ 1];
+    Elem<T>::unpack_swapped(raw, XP);
   }
 #pragma unroll
-  for (int j = 0; j < 8; ++j) o[j] = __fmul_rn(__fmaf_rn(x[j], a[j], __fmul_rn(xp[j], b[j])), r);
+  for (int i = 0; i < 4; ++i) O[i] = __fmul2_rn(__ffma2_rn(X[i], A[i], __fmul2_rn(XP[i], B[i])), R);
+}
+
+// 16-byte streaming store to global memory (written once, not re-read).
+__device__ __forceinline__ void store16(char* dst, const uint4& v) {
+  __stcs(reinterpret_cast<uint4*>(dst), v);
+}
+
+// One tensor's heads of one staged row: this warp takes passes
+// lw, lw + G, lw + 2G, ... (a pass = HPW heads), two at a time so the
+// latencies of one pass hide behind the other's.
+template <typename T, typename CT, int D, bool RH, bool EXPANDED>
+__device__ __forceinline__ void process_tensor(const unsigned char* seg, const unsigned char* cos_s,
+                                               const unsigned char* sin_s, const float* gamma, char* out_row,
+                                               int n_heads, int n_pass, int lw, int G, int lane, float eps,
+                                               float inv_d) {
+  using Geo = Geometry<D, RH>;
+  constexpr int LPH = Geo::LPH;
+  constexpr int HPW = Geo::HPW;
+  constexpr int ES = 2;
+  constexpr int CES = sizeof(CT);
+  const int d0 = (lane % LPH) * 8;
+  const int hslot = lane / LPH;
+  float2 a[4], b[4];
+  if (!EXPANDED) {
+    // the row's one cos/sin row, folded once for every head this lane visits
+    float2 c[4], s[4];
+    load_table8<CT>(cos_s + d0 * CES, c);
+    load_table8<CT>(sin_s + d0 * CES, s);
+    fold_coefficients<D, RH>(gamma, d0, c, s, a, b);
+  }
+  int t = lw;
+  for (; t + G < n_pass; t += 2 * G) {
+    const int h0 = t * HPW + hslot;
+    const int h1 = (t + G) * HPW + hslot;
+    const bool act0 = h0 < n_heads, act1 = h1 < n_heads;
+    const int hc0 = act0 ? h0 : 0, hc1 = act1 ? h1 : 0;
+    const uint4 r0 = *reinterpret_cast<const uint4*>(seg + (hc0 * D + d0) * ES);
+    const uint4 r1 = *reinterpret_cast<const uint4*>(seg + (hc1 * D + d0) * ES);
+    float2 o0[4], o1[4];
+    if (EXPANDED) {
+      float2 c[4], s[4], a1[4], b1[4];
+      load_table8<CT>(cos_s + (hc0 * D + d0) * CES, c);
+      load_table8<CT>(sin_s + (hc0 * D + d0) * CES, s);
+      fold_coefficients<D, RH>(gamma, d0, c, s, a, b);
+      load_table8<CT>(cos_s + (hc1 * D + d0) * CES, c);
+      load_table8<CT>(sin_s + (hc1 * D + d0) * CES, s);
+      fold_coefficients<D, RH>(gamma, d0, c, s, a1, b1);
+      head_math<T, D, RH>(r0, a, b, eps, inv_d, o0);
+      head_math<T, D, RH>(r1, a1, b1, eps, inv_d, o1);
+    } else {
+      head_math<T, D, RH>(r0, a, b, eps, inv_d, o0);
+      head_math<T, D, RH>(r1, a, b, eps, inv_d, o1);
+    }
+    if (act0) store16(out_row + (h0 * D + d0) * ES, Elem<T>::pack(o0));
+    if (act1) store16(out_row + (h1 * D + d0) * ES, Elem<T>::pack(o1));
+  }
+  if (t < n_pass) {
+    const int h0 = t * HPW + hslot;
+    const bool act0 = h0 < n_heads;
+    const int hc0 = act0 ? h0 : 0;
+    const uint4 r0 = *reinterpret_cast<const uint4*>(seg + (hc0 * D + d0) * ES);
+    if (EXPANDED) {
+      float2 c[4], s[4];
+      load_table8<CT>(cos_s + (hc0 * D + d0) * CES, c);
+      load_table8<CT>(sin_s + (hc0 * D + d0) * CES, s);
+      fold_coefficients<D, RH>(gamma, d0, c, s, a, b);
+    }
+    float2 o0[4];
+    head_math<T, D, RH>(r0, a, b, eps, inv_d, o0);
+    if (act0) store16(out_row + (h0 * D + d0) * ES, Elem<T>::pack(o0));
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -307,26 +395,24 @@ __device__ __forceinline__ void head_math(const uint4& raw, const float (&a)[8],
 template <typename T, typename CT, int D, bool RH, bool EXPANDED>
 __global__ void __launch_bounds__(kMaxThreads, 1) qknr_fused_kernel(const __grid_constant__ KernelParams p) {
   extern __shared__ __align__(128) unsigned char smem[];
-  using G = Geometry<D, RH>;
-  constexpr int LPH = G::LPH;
-  constexpr int HPW = G::HPW;
+  using Geo = Geometry<D, RH>;
+  constexpr int HPW = Geo::HPW;
   constexpr int ES = 2;                      // activation bytes
-  constexpr int CES = sizeof(CT);            // table bytes
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int S = p.stages;
+  const int NW = p.consumer_warps;
   const uint32_t base = smem_addr(smem);
   const uint32_t full0 = base + kOffBarriers;
   const uint32_t empty0 = base + kOffBarriers + 8 * kMaxStages;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffAbort);
   float* gam = reinterpret_cast<float*>(smem + kOffGamma);   // [0,D): gamma_q, [D,2D): gamma_k
-  const uint32_t stage0 = base + kOffStage0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, p.consumer_warps);
+      mbar_init(empty0 + 8 * s, NW);
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -339,11 +425,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qknr_fused_kernel(const __grid
 
   const unsigned long long limit = p.wait_limit_ns;
 
-  if (warp == p.consumer_warps) {
+  if (warp == NW) {
     // ---------------- producer warp: one lane issues every bulk copy
     if (lane != 0) return;
     const uint32_t q_bytes = p.hq * D * ES, k_bytes = p.hk * D * ES, v_bytes = p.hv * D * ES;
     const uint32_t c_bytes = static_cast<uint32_t>(p.cos_row_bytes);
+    const uint32_t stage0 = base + kOffStage0;
     long long issued = 0;
     int s = 0;
     uint32_t ph = 0;
@@ -354,8 +441,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qknr_fused_kernel(const __grid
       const uint32_t full = full0 + 8 * s;
       const uint32_t dst = stage0 + s * p.stage_bytes;
       mbar_arrive_expect_tx(full, p.tx_bytes);
-      if (q_bytes) bulk_load(dst, p.q + row * p.q_stride, q_bytes, full);
-      if (k_bytes) bulk_load(dst + p.off_k, p.k + row * p.k_stride, k_bytes, full);
+      if (p.qk_merged) {
+        bulk_load(dst, p.q + row * p.q_stride, q_bytes + k_bytes, full);
+      } else {
+        if (q_bytes) bulk_load(dst, p.q + row * p.q_stride, q_bytes, full);
+        if (k_bytes) bulk_load(dst + p.off_k, p.k + row * p.k_stride, k_bytes, full);
+      }
       if (v_bytes) bulk_load(dst + p.off_v, p.v + row * p.v_stride, v_bytes, full);
       if (c_bytes) {
         const long long crow = row % p.cos_rows;
@@ -371,9 +462,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qknr_fused_kernel(const __grid
       const long long first = issued > S ? issued - S : 0;
       for (long long it = first; it < issued; ++it) {
         const uint32_t bar = full0 + 8 * static_cast<int>(it % S);
-        const uint32_t ph = static_cast<uint32_t>((it / S) & 1);
+        const uint32_t phase = static_cast<uint32_t>((it / S) & 1);
         const unsigned long long t0 = global_timer_ns();
-        while (!mbar_try_wait(bar, ph) && global_timer_ns() - t0 < limit) {
+        while (!mbar_try_wait(bar, phase) && global_timer_ns() - t0 < limit) {
         }
       }
     }
@@ -381,67 +472,33 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qknr_fused_kernel(const __grid
   }
 
   // ---------------- consumer warps
-  const int sub = lane % LPH;           // lane's slot inside its head
-  const int hslot = lane / LPH;         // which of the warp's HPW heads
-  const int d0 = sub * 8;
+  // Warps [0, warps_q) normalise Q heads and warps [NW - warps_k, NW) K
+  // heads (the ranges are disjoint unless there is a single consumer warp);
+  // all warps share the V copy.
   const int nq = (p.hq + HPW - 1) / HPW;                // Q passes per row
   const int nk = (p.hk + HPW - 1) / HPW;                // K passes per row
-  const int nv = (p.hv * D * ES + 511) / 512;           // V copy passes (512 B per warp)
-  const int ntask = nq + nk + nv;
+  const int v_row = p.hv * D * ES;                      // V bytes per row
+  const bool do_q = warp < p.warps_q;
+  const bool do_k = warp >= NW - p.warps_k;
   const float eps = p.eps, inv_d = p.inv_d;
 
   int s = 0;
   uint32_t ph = 0;
   for (long long row = blockIdx.x; row < p.tokens; row += gridDim.x) {
     if (!bounded_wait(full0 + 8 * s, ph, limit, abort_flag, p.status)) break;
-    const uint32_t st = stage0 + s * p.stage_bytes;
-
-    float aq[8], bq[8], ak[8], bk[8];
-    if (!EXPANDED && nq + nk > 0) {
-      // the row's shared cos/sin, read once by this lane for every head it visits
-      float c[8], sn[8];
-      load_table8<CT>(st + p.off_cos + d0 * CES, c);
-      load_table8<CT>(st + p.off_sin + d0 * CES, sn);
-      fold_coefficients<D, RH>(gam, d0, c, sn, aq, bq);
-      fold_coefficients<D, RH>(gam + D, d0, c, sn, ak, bk);
-    }
-
-    for (int task = warp; task < ntask; task += p.consumer_warps) {
-      if (task < nq + nk) {
-        const bool is_k = task >= nq;
-        const int h = (is_k ? task - nq : task) * HPW + hslot;   // head within its tensor
-        const int nh = is_k ? p.hk : p.hq;
-        const bool active = h < nh;
-        const int hc = active ? h : 0;
-        const uint32_t src = st + (is_k ? p.off_k : 0u) + (hc * D + d0) * ES;
-        const uint4 raw = lds128(src);
-        float a[8], b[8];
-        if (EXPANDED) {
-          float c[8], sn[8];
-          load_table8<CT>(st + p.off_cos + (hc * D + d0) * CES, c);
-          load_table8<CT>(st + p.off_sin + (hc * D + d0) * CES, sn);
-          fold_coefficients<D, RH>(is_k ? gam + D : gam, d0, c, sn, a, b);
-        } else {
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            a[j] = is_k ? ak[j] : aq[j];
-            b[j] = is_k ? bk[j] : bq[j];
-          }
-        }
-        float o[8];
-        head_math<T, D, RH>(raw, a, b, eps, inv_d, o);
-        if (active) {
-          char* dst = is_k ? p.k_out + row * p.k_out_stride : p.q_out + row * p.q_out_stride;
-          stg128(dst + (h * D + d0) * ES, Elem<T>::pack(o));
-        }
-      } else {
-        // V pass-through copy, 16 bytes per lane
-        const int off = (task - nq - nk) * 512 + lane * 16;
-        if (off < p.hv * D * ES) {
-          const uint4 raw = lds128(st + p.off_v + off);
-          stg128(p.v_out + row * p.v_out_stride + off, raw);
-        }
-      }
+    const unsigned char* st = smem + kOffStage0 + s * p.stage_bytes;
+    if (do_q && nq)
+      process_tensor<T, CT, D, RH, EXPANDED>(st, st + p.off_cos, st + p.off_sin, gam,
+                                             p.q_out + row * p.q_out_stride, p.hq, nq, warp, p.warps_q, lane,
+                                             eps, inv_d);
+    if (do_k && nk)
+      process_tensor<T, CT, D, RH, EXPANDED>(st + p.off_k, st + p.off_cos, st + p.off_sin, gam + D,
+                                             p.k_out + row * p.k_out_stride, p.hk, nk, warp - (NW - p.warps_k),
+                                             p.warps_k, lane, eps, inv_d);
+    // V pass-through copy, 16 bytes per lane
+    for (int off = (warp * 32 + lane) * 16; off < v_row; off += NW * 512) {
+      const uint4 raw = *reinterpret_cast<const uint4*>(st + p.off_v + off);
+      store16(p.v_out + row * p.v_out_stride + off, raw);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(empty0 + 8 * s);

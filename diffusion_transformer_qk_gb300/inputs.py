@@ -241,21 +241,24 @@ def split_packed(qkv: np.ndarray, hq: int, hk: int, hv: int, d: int):
     return (qkv[:, : hq * d], qkv[:, hq * d:(hq + hk) * d], qkv[:, (hq + hk) * d:(hq + hk + hv) * d])
 
 
-def algorithmic_bytes(w: Workload, v_copied: bool = False, launches: str = "all") -> int:
+def algorithmic_bytes(w: Workload, v_copied: bool = False, launches: str = "all",
+                      tokens: Optional[int] = None) -> int:
     """Bytes one call must move at minimum: Q and K read once and written
-    once, the cos/sin table read once (the expanded layout is charged its
-    full [T, H, D] table), V read and written once when copied, plus gamma.
+    once, the cos/sin table rows it uses read once (the expanded layout is
+    charged its full [T, H, D] table), V read and written once when copied,
+    plus gamma.
 
     ``launches="q"`` counts one per-tensor launch over Q only (FLUX.2 style).
+    ``tokens`` overrides the row count (a reduced case of the workload).
     """
     es = 2
-    T, D = w.tokens, w.head_dim
+    T, D = (w.tokens if tokens is None else int(tokens)), w.head_dim
     hq, hk = w.n_heads_q, w.n_heads_k
     if launches == "q":
         hk = 0
     cos_es = 4 if w.cos_dtype == "fp32" else 2
     if w.cos_layout == "shared_row":
-        cos_bytes = 2 * w.seq * D * cos_es
+        cos_bytes = 2 * min(w.seq, T) * D * cos_es
     else:
         cos_bytes = 2 * T * w.n_heads_q * D * cos_es
     qk = 2 * T * (hq + hk) * D * es
