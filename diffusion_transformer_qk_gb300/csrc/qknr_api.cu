@@ -100,7 +100,8 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 struct Plan {
   qknr::KernelParams kp;
   const void* fn = nullptr;
-  int grid = 0, block = 0, smem = 0, stages = 0, ctas_per_sm = 0, warps = 0, regs = 0, num_sms = 0;
+  int grid = 0, block = 0, smem = 0, stages = 0, ctas_per_sm = 0, warps = 0, group_warps = 0, regs = 0,
+      num_sms = 0;
   bool launch = false;   // false: nothing to do
   char name[96];
 };
@@ -125,9 +126,12 @@ qknr_status make_plan(const qknr_args* a, Plan* pl) {
   if (!(a->eps >= 0.0f)) return fail(QKNR_ERR_SHAPE, "eps must be >= 0");
   if (a->consumer_warps < 0 || a->consumer_warps > qknr::kMaxConsumerWarps)
     return fail(QKNR_ERR_SHAPE, "consumer_warps out of range 0..%d", qknr::kMaxConsumerWarps);
-  if (a->stages < 0 || a->stages == 1 || a->stages > qknr::kMaxStages)
-    return fail(QKNR_ERR_SHAPE, "stages must be 0 (auto) or 2..%d", qknr::kMaxStages);
+  if (a->stages < 0 || a->stages == 1 || a->stages > qknr::kMaxStages / 2)
+    return fail(QKNR_ERR_SHAPE, "stages must be 0 (auto) or 2..%d", qknr::kMaxStages / 2);
   if (a->ctas_per_sm < 0 || a->ctas_per_sm > 4) return fail(QKNR_ERR_SHAPE, "ctas_per_sm out of range 0..4");
+  if (a->group_warps < 0 || a->group_warps > qknr::kMaxConsumerWarps ||
+      (a->group_warps && a->consumer_warps && a->consumer_warps % a->group_warps))
+    return fail(QKNR_ERR_SHAPE, "group_warps must divide consumer_warps");
 
   const int es = 2;
   const int ces = a->cos_dtype == QKNR_FP32 ? 4 : 2;
@@ -279,10 +283,18 @@ qknr_status size_launch(const qknr_args* a, Plan* pl) {
   if (st != QKNR_OK) return st;
   pl->num_sms = di.num_sms;
 
-  // Defaults from sweeps on GB300: 12 consumer warps keep enough passes in
-  // flight to cover shuffle and rsqrt latencies; one CTA per SM (more do
-  // not fit beside 12 warps' registers) with about 128 KB of ring.
-  const int warps = a->consumer_warps ? a->consumer_warps : 12;
+  // Defaults from sweeps on GB300.  Rows of many heads (>= 32 passes of
+  // heads per row, e.g. Wan's 40 Q + 40 K heads of 128) run best with all
+  // 12 consumer warps on one row and a 4-deep ring: DRAM is the limit and
+  // more bytes in flight only queue.  Rows of few heads leave each warp too
+  // little work per row, so 16 warps form groups of about 6 passes per
+  // warp that each take whole rows, several rows in flight.  One CTA per SM
+  // (a second does not fit beside the first one's registers).
+  const int hpw = 32 / (a->head_dim / 8);
+  const int nq = (pl->kp.hq + hpw - 1) / hpw, nk = (pl->kp.hk + hpw - 1) / hpw;
+  const int passes = nq + nk;
+  const bool wide_rows = passes >= 32 || passes == 0;
+  const int warps = a->consumer_warps ? a->consumer_warps : (wide_rows ? 12 : 16);
   const int cps = a->ctas_per_sm ? a->ctas_per_sm : 1;
   const long long stage_bytes = pl->kp.stage_bytes;
   // shared memory one CTA may use when `cps` CTAs share an SM
@@ -290,22 +302,53 @@ qknr_status size_launch(const qknr_args* a, Plan* pl) {
   if (budget > di.smem_optin) budget = di.smem_optin;
   const long long ring = budget - qknr::kOffStage0;
   const long long fit = ring > 0 ? ring / stage_bytes : 0;
+  const long long grid0 = (long long)di.num_sms * cps;
+  const long long rows_per_cta = (a->tokens + grid0 - 1) / grid0;
+
+  int gw = a->group_warps;
+  if (gw == 0) {
+    int want = wide_rows ? warps : (passes + 5) / 6;      // about 6 passes per warp
+    if (want < 1) want = 1;
+    gw = warps;
+    for (int g = want; g <= warps; ++g)
+      if (warps % g == 0) {
+        gw = g;
+        break;
+      }
+    // every group needs a ring of at least two stages, and no more groups
+    // than the rows a CTA will see
+    while (gw < warps && (2LL * (warps / gw) > fit || 2 * (warps / gw) > qknr::kMaxStages ||
+                          warps / gw > rows_per_cta)) {
+      int g = gw + 1;
+      while (warps % g) ++g;
+      gw = g;
+    }
+  }
+  if (warps % gw) return fail(QKNR_ERR_SHAPE, "group_warps %d does not divide consumer_warps %d", gw, warps);
+  const int n_groups = warps / gw;
+
+  // ring depth per group: 4 for a single group, else about 128 KB of
+  // stages in all; at least two each
   int stages = a->stages;
   if (stages == 0) {
-    long long want = (128 * 1024) / stage_bytes;
-    if (want < 4) want = 4;
-    if (want > qknr::kMaxStages) want = qknr::kMaxStages;
-    stages = static_cast<int>(fit < want ? fit : want);
-    // no deeper than the rows one CTA will see
-    const long long grid0 = (long long)di.num_sms * cps;
-    const long long rows_per_cta = (a->tokens + grid0 - 1) / grid0;
-    if (rows_per_cta >= 2 && stages > rows_per_cta) stages = static_cast<int>(rows_per_cta);
+    long long want = n_groups == 1 ? 4 : (128 * 1024) / (stage_bytes * n_groups);
+    if (want < 2) want = 2;
+    if (want > 8) want = 8;
+    long long cap = fit / n_groups;
+    if (cap > qknr::kMaxStages / n_groups) cap = qknr::kMaxStages / n_groups;
+    stages = static_cast<int>(cap < want ? cap : want);
+    // no deeper than the rows one group will see
+    const long long rows_per_group = (rows_per_cta + n_groups - 1) / n_groups;
+    if (rows_per_group >= 2 && stages > rows_per_group) stages = static_cast<int>(rows_per_group);
     if (stages < 2) stages = 2;
   }
-  const long long smem = qknr::kOffStage0 + stages * stage_bytes;
+  if (stages * n_groups > qknr::kMaxStages)
+    return fail(QKNR_ERR_SHAPE, "%d groups x %d stages exceeds %d stages", n_groups, stages, qknr::kMaxStages);
+  const long long smem = qknr::kOffStage0 + static_cast<long long>(stages) * n_groups * stage_bytes;
   if (smem > di.smem_optin)
-    return fail(QKNR_ERR_UNSUPPORTED, "a %d-stage ring of %lld-byte rows needs %lld B of shared memory (max %d)",
-                stages, stage_bytes, smem, di.smem_optin);
+    return fail(QKNR_ERR_UNSUPPORTED,
+                "%d groups x %d stages of %lld-byte rows need %lld B of shared memory (max %d)", n_groups, stages,
+                stage_bytes, smem, di.smem_optin);
   const int block = 32 * (warps + 1);
   int occ = 0;
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, pl->fn, block, static_cast<size_t>(smem));
@@ -316,19 +359,18 @@ qknr_status size_launch(const qknr_args* a, Plan* pl) {
   if (grid > a->tokens) grid = a->tokens;
   pl->kp.stages = stages;
   pl->kp.consumer_warps = warps;
-  // split the consumer warps between Q and K in proportion to their passes
-  const int hpw = 32 / (a->head_dim / 8);
-  const int nq = (pl->kp.hq + hpw - 1) / hpw, nk = (pl->kp.hk + hpw - 1) / hpw;
+  pl->kp.group_warps = gw;
+  // split a group's warps between Q and K in proportion to their passes
   if (nq == 0 || nk == 0) {
-    pl->kp.warps_q = nq ? warps : 0;
-    pl->kp.warps_k = nk ? warps : 0;
-  } else if (warps == 1) {
+    pl->kp.warps_q = nq ? gw : 0;
+    pl->kp.warps_k = nk ? gw : 0;
+  } else if (gw == 1) {
     pl->kp.warps_q = pl->kp.warps_k = 1;
   } else {
-    int wq = static_cast<int>((static_cast<long long>(warps) * nq + (nq + nk) / 2) / (nq + nk));
-    wq = wq < 1 ? 1 : (wq > warps - 1 ? warps - 1 : wq);
+    int wq = static_cast<int>((static_cast<long long>(gw) * nq + (nq + nk) / 2) / (nq + nk));
+    wq = wq < 1 ? 1 : (wq > gw - 1 ? gw - 1 : wq);
     pl->kp.warps_q = wq;
-    pl->kp.warps_k = warps - wq;
+    pl->kp.warps_k = gw - wq;
   }
   pl->grid = static_cast<int>(grid);
   pl->block = block;
@@ -336,6 +378,7 @@ qknr_status size_launch(const qknr_args* a, Plan* pl) {
   pl->stages = stages;
   pl->ctas_per_sm = per_sm;
   pl->warps = warps;
+  pl->group_warps = gw;
   return QKNR_OK;
 }
 
@@ -371,6 +414,7 @@ qknr_status qknr_query(const qknr_args* args, qknr_launch_info* info) {
   info->stages = pl.stages;
   info->ctas_per_sm = pl.ctas_per_sm;
   info->consumer_warps = pl.warps;
+  info->group_warps = pl.group_warps;
   info->registers = pl.regs;
   info->num_sms = pl.num_sms;
   return QKNR_OK;

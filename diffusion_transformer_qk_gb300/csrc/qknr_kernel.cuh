@@ -3,18 +3,23 @@
 // One persistent CTA per SM slot walks token rows t = blockIdx.x,
 // blockIdx.x + gridDim.x, ...  A producer warp streams each row's Q and K
 // heads (and V when it is copied), plus that row's cos and sin, from HBM
-// into a ring of shared-memory stages with 1-D bulk copies
-// (cp.async.bulk, completion counted on an mbarrier).  Consumer warps take
-// a stage, normalise and rotate every head in fp32 registers and store the
-// result with 16-byte stores, then hand the stage back.
+// into shared-memory stages with 1-D bulk copies (cp.async.bulk,
+// completion counted on an mbarrier).  The consumer warps form groups; the
+// CTA's rows go to the groups in turn and each group has its own ring of
+// stages, which it drains strictly in order (so a group never waits on a
+// stage phase more than one ahead of the barrier).  A group normalises and
+// rotates every head of its row in fp32 registers, stores the result with
+// 16-byte stores and hands the stage back.
 //
 // Lane mapping: a lane owns 8 consecutive dimensions (16 bytes) of a head,
 // so a head of D dims spans LPH = D/8 lanes and a warp covers HPW = 32/LPH
 // heads at once.  The per-head sum of squares is a shuffle-xor reduction
 // inside those LPH lanes; a rotate-half partner lives in lane ^ (LPH/2),
-// an interleaved partner in the same lane.  Consumer warps are split
-// between Q and K heads, so each folds only its own tensor's gain, and a
-// warp works on two passes of heads at a time to overlap their latencies.
+// an interleaved partner in the same lane.  Consumer warps form groups
+// that each take whole rows, so several rows are in flight at once; inside
+// a group the warps are split between Q and K heads, so each folds only its
+// own tensor's gain, and a warp works on two passes of heads at a time to
+// overlap their latencies.
 //
 // cos/sin (page 1, "VisualGen Wan: deduplicate shared RoPE SMEM staging",
 // Description): the shared layout stages one row per token and every head
@@ -41,12 +46,12 @@ namespace qknr {
 
 constexpr int kMaxConsumerWarps = 16;
 constexpr int kMaxThreads = 32 * (kMaxConsumerWarps + 1);
-constexpr int kMaxStages = 16;
+constexpr int kMaxStages = 32;        // all groups' rings together
 // dynamic shared memory map (bytes)
 constexpr int kOffBarriers = 0;       // full[kMaxStages], empty[kMaxStages]: 8 B each
-constexpr int kOffAbort = 256;        // int abort flag
-constexpr int kOffGamma = 512;        // gamma_q[D], gamma_k[D] fp32 (D <= 128)
-constexpr int kOffStage0 = 1536;      // stage ring
+constexpr int kOffAbort = 512;        // int abort flag
+constexpr int kOffGamma = 1024;       // gamma_q[D], gamma_k[D] fp32 (D <= 128)
+constexpr int kOffStage0 = 2048;      // stage rings
 constexpr int kStageAlign = 128;
 
 constexpr int kStatusTimeout = 6;     // QKNR_ERR_TIMEOUT
@@ -74,8 +79,9 @@ struct KernelParams {
   float inv_d;
   int hq, hk, hv;                                    // hv: V heads copied (0: V untouched)
   int consumer_warps;
-  int warps_q, warps_k;                              // consumer warps on Q heads / on K heads
-  int stages;
+  int group_warps;                                   // warps that share one row (divides consumer_warps)
+  int warps_q, warps_k;                              // warps of a group on Q heads / on K heads
+  int stages;                                        // ring depth of each group (stages per group)
   int qk_merged;                                     // K directly follows Q: one copy for both
   unsigned flags;
   // stage layout: [Q heads | K heads | V heads | cos row | sin row]
@@ -410,9 +416,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qknr_fused_kernel(const __grid
   float* gam = reinterpret_cast<float*>(smem + kOffGamma);   // [0,D): gamma_q, [D,2D): gamma_k
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < S; ++s) {
+    for (int s = 0; s < S * (NW / p.group_warps); ++s) {
       mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, NW);
+      mbar_init(empty0 + 8 * s, p.group_warps);
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -431,38 +437,69 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qknr_fused_kernel(const __grid
     const uint32_t q_bytes = p.hq * D * ES, k_bytes = p.hk * D * ES, v_bytes = p.hv * D * ES;
     const uint32_t c_bytes = static_cast<uint32_t>(p.cos_row_bytes);
     const uint32_t stage0 = base + kOffStage0;
+    const int n_groups = NW / p.group_warps;
+    // Row `issued` of this CTA goes to group g = issued % n_groups, slot
+    // j % S of that group's ring with phase (j / S) & 1, where j counts the
+    // group's rows.  All of it is kept as running counters: this one thread
+    // issues every copy of the CTA, so its per-row cost bounds the rate.
     long long issued = 0;
-    int s = 0;
+    int g = 0, js = 0;
     uint32_t ph = 0;
+    const long long step = gridDim.x;
+    const long long crow_step = step % p.cos_rows;
+    long long crow = blockIdx.x % p.cos_rows;
+    // source addresses as integers: unused tensors may have null bases
+    unsigned long long qsrc = reinterpret_cast<unsigned long long>(p.q) + blockIdx.x * p.q_stride;
+    unsigned long long ksrc = reinterpret_cast<unsigned long long>(p.k) + blockIdx.x * p.k_stride;
+    unsigned long long vsrc = reinterpret_cast<unsigned long long>(p.v) + blockIdx.x * p.v_stride;
+    const unsigned long long qstep = step * p.q_stride, kstep = step * p.k_stride, vstep = step * p.v_stride;
     bool ok = true;
-    for (long long row = blockIdx.x; row < p.tokens; row += gridDim.x) {
-      if (!bounded_wait(empty0 + 8 * s, ph ^ 1u, limit, abort_flag, p.status)) { ok = false; break; }
+    for (long long row = blockIdx.x; row < p.tokens; row += step) {
+      const int s = g * S + js;
+      const uint32_t empty = empty0 + 8 * s;
+      if (!mbar_try_wait(empty, ph ^ 1u) && !bounded_wait(empty, ph ^ 1u, limit, abort_flag, p.status)) {
+        ok = false;
+        break;
+      }
       if (p.flags & kFlagTestStall) break;   // issue nothing: the consumers' waits run out
       const uint32_t full = full0 + 8 * s;
       const uint32_t dst = stage0 + s * p.stage_bytes;
       mbar_arrive_expect_tx(full, p.tx_bytes);
       if (p.qk_merged) {
-        bulk_load(dst, p.q + row * p.q_stride, q_bytes + k_bytes, full);
+        bulk_load(dst, reinterpret_cast<const void*>(qsrc), q_bytes + k_bytes, full);
       } else {
-        if (q_bytes) bulk_load(dst, p.q + row * p.q_stride, q_bytes, full);
-        if (k_bytes) bulk_load(dst + p.off_k, p.k + row * p.k_stride, k_bytes, full);
+        if (q_bytes) bulk_load(dst, reinterpret_cast<const void*>(qsrc), q_bytes, full);
+        if (k_bytes) bulk_load(dst + p.off_k, reinterpret_cast<const void*>(ksrc), k_bytes, full);
       }
-      if (v_bytes) bulk_load(dst + p.off_v, p.v + row * p.v_stride, v_bytes, full);
+      if (v_bytes) bulk_load(dst + p.off_v, reinterpret_cast<const void*>(vsrc), v_bytes, full);
       if (c_bytes) {
-        const long long crow = row % p.cos_rows;
         bulk_load(dst + p.off_cos, p.cos + crow * p.cos_row_bytes, c_bytes, full);
         bulk_load(dst + p.off_sin, p.sin + crow * p.cos_row_bytes, c_bytes, full);
       }
       ++issued;
-      if (++s == S) { s = 0; ph ^= 1u; }
+      qsrc += qstep;
+      ksrc += kstep;
+      vsrc += vstep;
+      crow += crow_step;
+      if (crow >= p.cos_rows) crow -= p.cos_rows;
+      if (++g == n_groups) {
+        g = 0;
+        if (++js == S) {
+          js = 0;
+          ph ^= 1u;
+        }
+      }
     }
     if (!ok || *abort_flag) {
-      // copies of the last (up to S) issued stages may still be landing:
-      // wait for them before this CTA's shared memory is released
-      const long long first = issued > S ? issued - S : 0;
+      // copies of the last n_groups * S issued rows (the latest use of every
+      // stage) may still be landing: wait for them before this CTA's shared
+      // memory is released
+      const long long total = static_cast<long long>(n_groups) * S;
+      const long long first = issued > total ? issued - total : 0;
       for (long long it = first; it < issued; ++it) {
-        const uint32_t bar = full0 + 8 * static_cast<int>(it % S);
-        const uint32_t phase = static_cast<uint32_t>((it / S) & 1);
+        const long long j = it / n_groups;
+        const uint32_t bar = full0 + 8 * (static_cast<int>(it % n_groups) * S + static_cast<int>(j % S));
+        const uint32_t phase = static_cast<uint32_t>((j / S) & 1);
         const unsigned long long t0 = global_timer_ns();
         while (!mbar_try_wait(bar, phase) && global_timer_ns() - t0 < limit) {
         }
@@ -472,36 +509,44 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qknr_fused_kernel(const __grid
   }
 
   // ---------------- consumer warps
-  // Warps [0, warps_q) normalise Q heads and warps [NW - warps_k, NW) K
-  // heads (the ranges are disjoint unless there is a single consumer warp);
-  // all warps share the V copy.
+  // The consumer warps form NW / GW groups of GW warps; group g takes the
+  // CTA's rows g, g + NW/GW, ... so several rows are in flight at once.
+  // Inside a group, warps [0, warps_q) normalise Q heads and warps
+  // [GW - warps_k, GW) K heads (disjoint unless GW == 1); all of the
+  // group's warps share the V copy.
+  const int GW = p.group_warps;
+  const int n_groups = NW / GW;
+  const int grp = warp / GW, gw = warp % GW;
   const int nq = (p.hq + HPW - 1) / HPW;                // Q passes per row
   const int nk = (p.hk + HPW - 1) / HPW;                // K passes per row
   const int v_row = p.hv * D * ES;                      // V bytes per row
-  const bool do_q = warp < p.warps_q;
-  const bool do_k = warp >= NW - p.warps_k;
+  const bool do_q = gw < p.warps_q;
+  const bool do_k = gw >= GW - p.warps_k;
   const float eps = p.eps, inv_d = p.inv_d;
 
+  const int ring0 = grp * S;                            // this group's ring
   int s = 0;
   uint32_t ph = 0;
-  for (long long row = blockIdx.x; row < p.tokens; row += gridDim.x) {
-    if (!bounded_wait(full0 + 8 * s, ph, limit, abort_flag, p.status)) break;
-    const unsigned char* st = smem + kOffStage0 + s * p.stage_bytes;
+  for (long long row = blockIdx.x + static_cast<long long>(grp) * gridDim.x; row < p.tokens;
+       row += static_cast<long long>(n_groups) * gridDim.x) {
+    const uint32_t full = full0 + 8 * (ring0 + s);
+    if (!mbar_try_wait(full, ph) && !bounded_wait(full, ph, limit, abort_flag, p.status)) break;
+    const unsigned char* st = smem + kOffStage0 + (ring0 + s) * p.stage_bytes;
     if (do_q && nq)
       process_tensor<T, CT, D, RH, EXPANDED>(st, st + p.off_cos, st + p.off_sin, gam,
-                                             p.q_out + row * p.q_out_stride, p.hq, nq, warp, p.warps_q, lane,
-                                             eps, inv_d);
+                                             p.q_out + row * p.q_out_stride, p.hq, nq, gw, p.warps_q, lane, eps,
+                                             inv_d);
     if (do_k && nk)
       process_tensor<T, CT, D, RH, EXPANDED>(st + p.off_k, st + p.off_cos, st + p.off_sin, gam + D,
-                                             p.k_out + row * p.k_out_stride, p.hk, nk, warp - (NW - p.warps_k),
+                                             p.k_out + row * p.k_out_stride, p.hk, nk, gw - (GW - p.warps_k),
                                              p.warps_k, lane, eps, inv_d);
     // V pass-through copy, 16 bytes per lane
-    for (int off = (warp * 32 + lane) * 16; off < v_row; off += NW * 512) {
+    for (int off = (gw * 32 + lane) * 16; off < v_row; off += GW * 512) {
       const uint4 raw = *reinterpret_cast<const uint4*>(st + p.off_v + off);
       store16(p.v_out + row * p.v_out_stride + off, raw);
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(empty0 + 8 * s);
+    if (lane == 0) mbar_arrive(empty0 + 8 * (ring0 + s));
     if (++s == S) { s = 0; ph ^= 1u; }
   }
 }

@@ -57,7 +57,7 @@ class QknrArgs(ctypes.Structure):
         ("rope_style", c_int32),
         ("dev_status", c_void_p),
         ("ctas_per_sm", c_int32), ("stages", c_int32), ("consumer_warps", c_int32),
-        ("flags", c_uint32), ("wait_limit_ns", c_uint64),
+        ("group_warps", c_int32), ("flags", c_uint32), ("wait_limit_ns", c_uint64),
     ]
 
 
@@ -66,7 +66,8 @@ class QknrLaunchInfo(ctypes.Structure):
 
     _fields_ = [
         ("grid", c_int32), ("block", c_int32), ("dyn_smem", c_int32), ("stages", c_int32),
-        ("ctas_per_sm", c_int32), ("consumer_warps", c_int32), ("stage_bytes", c_int32),
+        ("ctas_per_sm", c_int32), ("consumer_warps", c_int32), ("group_warps", c_int32),
+        ("stage_bytes", c_int32),
         ("registers", c_int32), ("num_sms", c_int32), ("kernel", c_char * 96),
     ]
 
@@ -200,6 +201,7 @@ def make_args(
     ctas_per_sm: int = 0,
     stages: int = 0,
     consumer_warps: int = 0,
+    group_warps: int = 0,
     flags: int = 0,
     wait_limit_ns: int = 0,
 ) -> QknrArgs:
@@ -246,7 +248,7 @@ def make_args(
     a.cos_rows = cos_rows or 0
     a.rope_style = ROPE[rope_style]
     a.dev_status = _ptr(dev_status)
-    a.ctas_per_sm, a.stages, a.consumer_warps = ctas_per_sm, stages, consumer_warps
+    a.ctas_per_sm, a.stages, a.consumer_warps, a.group_warps = ctas_per_sm, stages, consumer_warps, group_warps
     a.flags, a.wait_limit_ns = flags, wait_limit_ns
     return a
 

@@ -130,8 +130,9 @@ typedef struct qknr_args {
 
   /* Launch tuning; 0 = automatic.  See qknr_query(). */
   int32_t ctas_per_sm;        /* persistent CTAs per SM (1..4) */
-  int32_t stages;             /* shared-memory ring depth (2..16) */
+  int32_t stages;             /* shared-memory ring depth per row group (2..16) */
   int32_t consumer_warps;     /* compute warps per CTA (1..16) */
+  int32_t group_warps;        /* warps sharing one row; divides consumer_warps */
   uint32_t flags;             /* QKNR_FLAG_* */
   uint64_t wait_limit_ns;     /* bound on every in-kernel wait; 0 = 2 s */
 } qknr_args;
@@ -141,9 +142,10 @@ typedef struct qknr_launch_info {
   int32_t grid;               /* CTAs (persistent) */
   int32_t block;              /* threads per CTA: consumer warps + 1 producer warp */
   int32_t dyn_smem;           /* dynamic shared memory per CTA, bytes */
-  int32_t stages;
+  int32_t stages;             /* ring depth per group */
   int32_t ctas_per_sm;
   int32_t consumer_warps;
+  int32_t group_warps;        /* consumer warps per row; consumer_warps/group_warps rows in flight */
   int32_t stage_bytes;        /* bytes staged per token row */
   int32_t registers;          /* registers per thread of the chosen kernel */
   int32_t num_sms;

@@ -97,6 +97,8 @@ def test_null_args(lib):
     (lambda a: setattr(a, "stages", 17), 2),
     (lambda a: setattr(a, "consumer_warps", 17), 2),
     (lambda a: setattr(a, "ctas_per_sm", 5), 2),
+    (lambda a: (setattr(a, "consumer_warps", 12), setattr(a, "group_warps", 5)), 2),
+    (lambda a: setattr(a, "group_warps", 17), 2),
     (lambda a: setattr(a, "eps", -1.0), 2),
     (lambda a: setattr(a, "gamma_q", None), 1),
     (lambda a: setattr(a, "k", None), 1),

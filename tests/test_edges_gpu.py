@@ -175,8 +175,12 @@ def test_largest_row_that_fits_two_stages():
     assert e.value.status == 4
 
 
-@pytest.mark.parametrize("tune", [dict(stages=2), dict(stages=16), dict(ctas_per_sm=2), dict(ctas_per_sm=4),
-                                  dict(consumer_warps=1), dict(consumer_warps=3), dict(consumer_warps=16)])
+@pytest.mark.parametrize("tune", [dict(stages=2), dict(stages=8, group_warps=16),
+                                  dict(consumer_warps=12, group_warps=6, stages=8),
+                                  dict(ctas_per_sm=2), dict(ctas_per_sm=4),
+                                  dict(consumer_warps=8, group_warps=1), dict(group_warps=2), dict(group_warps=4),
+                                  dict(consumer_warps=1), dict(consumer_warps=3), dict(consumer_warps=16),
+                                  dict(consumer_warps=8, group_warps=1, stages=2)])
 def test_result_does_not_depend_on_launch_shape(tune):
     T, H, D = 2000, 12, 128
     c = make_case(T, H, H, H, D, style="rotate_half", seed=10)
@@ -193,8 +197,11 @@ def test_query_reports_the_launch():
     info = Q.query(a)
     assert info["num_sms"] > 0 and 0 < info["grid"] <= 1000
     assert info["block"] == 32 * (info["consumer_warps"] + 1)
+    assert info["consumer_warps"] % info["group_warps"] == 0
+    groups = info["consumer_warps"] // info["group_warps"]
     assert info["stage_bytes"] == 80 * 256 + 1024
-    assert info["dyn_smem"] >= 2 * info["stage_bytes"] and info["registers"] > 0
+    assert info["dyn_smem"] >= 2 * groups * info["stage_bytes"] and info["registers"] > 0
+    assert info["stages"] * groups <= 32
 
 
 def test_bounded_wait_reports_timeout_and_leaves_context_usable():
