@@ -346,3 +346,100 @@ def qk_norm_rope_separate(q, k, n_heads, head_dim, gamma_q, gamma_k, cos, sin, *
     launch(make_args(q=q, k=k, v=v if hv else None, q_out=q_out, k_out=k_out, v_out=v_out if hv else None,
                      n_heads_q=n_heads, n_heads_k=n_heads, n_heads_v=hv, head_dim=head_dim,
                      gamma_q=gamma_q, gamma_k=gamma_k, cos=cos, sin=sin, **kw), stream)
+
+
+# ---------------------------------------------------------------------------
+# host-resident activations: chunked, overlapped copies around the kernel
+
+class HostPipeline:
+    """Runs the fused QK-RMSNorm + RoPE on a packed QKV activation that lives
+    in (pinned) host memory.  Token rows go through the device in chunks:
+    the host-to-device copy of chunk i+1, the kernel on chunk i and the
+    device-to-host copy of chunk i-1 run on three streams at once, so the
+    call costs about one direction of copy traffic instead of both plus the
+    kernel.
+
+    The device staging ring (``n_buffers`` chunks) and the device copies of
+    gamma and the cos/sin table are allocated once, here, by torch; the
+    library itself still allocates nothing.  Results are bitwise those of
+    ``qk_norm_rope_packed`` on the whole activation: every row is processed
+    by the same kernel with the same table row.
+    """
+
+    def __init__(self, width: int, dtype: torch.dtype, chunk_rows: int = 4096, n_buffers: int = 3,
+                 device=None):
+        self.device = torch.device("cuda", torch.cuda.current_device() if device is None
+                                   else torch.device(device).index)
+        self.chunk_rows = int(chunk_rows)
+        self.width = int(width)
+        self.bufs = [torch.empty((self.chunk_rows, self.width), dtype=dtype, device=self.device)
+                     for _ in range(n_buffers)]
+        self.h2d = torch.cuda.Stream(self.device)
+        self.d2h = torch.cuda.Stream(self.device)
+        self.freed = [None] * n_buffers          # event: the buffer's last D2H finished
+        self.status = torch.zeros(1, dtype=torch.int32, device=self.device)
+
+    def _stage_tables(self, gamma_q, gamma_k, cos, sin, stream, user):
+        """Device copies of the gains and tables (copied every call, on
+        `stream`; marked as used by `user` so the allocator keeps them until
+        the kernels that read them are done)."""
+        with torch.cuda.stream(stream):
+            dev = [None if t is None else t.to(self.device, non_blocking=True) for t in (gamma_q, gamma_k, cos, sin)]
+        for t in dev:
+            if t is not None:
+                t.record_stream(user)
+        return dev
+
+    def read_status(self) -> int:
+        """Synchronise and return (then clear) the kernels' status word."""
+        v = int(self.status.item())
+        if v:
+            self.status.zero_()
+        return v
+
+    def __call__(self, qkv_host, n_heads_q, n_heads_k, n_heads_v, head_dim, gamma_q, gamma_k, cos, sin, *,
+                 out_host=None, rope_style="interleaved", cos_layout="shared_row", eps=1e-6, **tune):
+        if qkv_host.is_cuda or qkv_host.dim() != 2 or qkv_host.shape[1] != self.width:
+            raise ValueError("qkv_host must be a 2-D host tensor of the pipeline's width")
+        out_host = qkv_host if out_host is None else out_host
+        T = qkv_host.shape[0]
+        compute = torch.cuda.current_stream(self.device)
+        gq, gk, cos_d, sin_d = self._stage_tables(gamma_q, gamma_k, cos, sin, self.h2d, compute)
+        tables_ready = torch.cuda.Event()
+        tables_ready.record(self.h2d)
+        rows = cos_d.shape[0]
+        if rows < T and self.chunk_rows % rows:
+            raise ValueError("with a batch-broadcast table the chunk must be a multiple of its rows")
+        n = len(self.bufs)
+        done = torch.cuda.Event()
+        for i, r0 in enumerate(range(0, T, self.chunk_rows)):
+            r1 = min(T, r0 + self.chunk_rows)
+            b = i % n
+            buf = self.bufs[b][: r1 - r0]
+            with torch.cuda.stream(self.h2d):
+                if self.freed[b] is not None:
+                    self.h2d.wait_event(self.freed[b])
+                buf.copy_(qkv_host[r0:r1], non_blocking=True)
+                loaded = torch.cuda.Event()
+                loaded.record(self.h2d)
+            compute.wait_event(loaded)
+            if i == 0:
+                compute.wait_event(tables_ready)
+            # the chunk's table rows: its own slice of a per-token table, or
+            # the whole batch-broadcast table (chunks start on a multiple of it)
+            c, s = (cos_d[r0:r1], sin_d[r0:r1]) if rows >= T else (cos_d, sin_d)
+            launch(packed_args(buf, n_heads_q, n_heads_k, n_heads_v, head_dim, gq, gk, c, s,
+                               rope_style=rope_style, cos_layout=cos_layout, eps=eps, dev_status=self.status,
+                               **tune), compute)
+            computed = torch.cuda.Event()
+            computed.record(compute)
+            with torch.cuda.stream(self.d2h):
+                self.d2h.wait_event(computed)
+                out_host[r0:r1].copy_(buf, non_blocking=True)
+                freed = torch.cuda.Event()
+                freed.record(self.d2h)
+                self.freed[b] = freed
+        # the caller's stream sees the results once every D2H copy is done
+        done.record(self.d2h)
+        compute.wait_event(done)
+        return out_host

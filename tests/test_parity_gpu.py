@@ -190,3 +190,48 @@ def test_shared_fp32_matches_expanded_matrix(style, H, D):
     np.testing.assert_array_equal(sb, eb)
     np.testing.assert_array_equal(sb[:, 2 * H * D:], inp["qkv"][:, 2 * H * D:])
     check_packed(w, sb, inp)
+
+
+# ---------------------------------------------------------------------------
+# host-resident activations through the chunked pipeline
+
+@pytest.mark.parametrize("T,chunk", [(10000, 4096), (4096, 4096), (777, 256)])
+def test_host_pipeline_matches_device_path(T, chunk):
+    w = I.WORKLOADS["wan_32760x40x128"].with_(n_heads_q=8, n_heads_k=8, n_heads_v=8)
+    inp = I.make_inputs(w, tokens=T)
+    ref, _ = run_packed(w, inp)
+    host = torch.from_numpy(inp["qkv"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    cos = torch.from_numpy(inp["cos"]).pin_memory()
+    sin = torch.from_numpy(inp["sin"]).pin_memory()
+    gq = torch.from_numpy(inp["gamma_q"]).pin_memory()
+    gk = torch.from_numpy(inp["gamma_k"]).pin_memory()
+    pipe = Q.HostPipeline(host.shape[1], torch.bfloat16, chunk_rows=chunk)
+    out = torch.empty_like(host).pin_memory()
+    pipe(host, 8, 8, 8, 128, gq, gk, cos, sin, out_host=out, rope_style=w.rope_style)
+    torch.cuda.synchronize()
+    assert pipe.read_status() == 0
+    assert torch.equal(out.view(torch.int16), ref.cpu().view(torch.int16))
+    np.testing.assert_array_equal(host.view(torch.int16).numpy().view(np.uint16), inp["qkv"])   # input kept
+    # in place, twice in a row through the same staging ring
+    for _ in range(2):
+        h2 = torch.from_numpy(inp["qkv"].view(np.int16)).view(torch.bfloat16).pin_memory()
+        pipe(h2, 8, 8, 8, 128, gq, gk, cos, sin, rope_style=w.rope_style)
+        torch.cuda.synchronize()
+        assert torch.equal(h2.view(torch.int16), out.view(torch.int16))
+
+
+def test_host_pipeline_batch_broadcast_table():
+    w = I.WORKLOADS["dense_4096x24x128"].with_(seq=500, batch=4, positions="1d")
+    T = w.tokens
+    inp = I.make_inputs(w)
+    ref, _ = run_packed(w, inp)
+    host = torch.from_numpy(inp["qkv"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    pipe = Q.HostPipeline(host.shape[1], torch.bfloat16, chunk_rows=1000)
+    pipe(host, 24, 24, 24, 128, torch.from_numpy(inp["gamma_q"]), torch.from_numpy(inp["gamma_k"]),
+         torch.from_numpy(inp["cos"]), torch.from_numpy(inp["sin"]), rope_style=w.rope_style)
+    torch.cuda.synchronize()
+    assert torch.equal(host.view(torch.int16), ref.cpu().view(torch.int16))
+    with pytest.raises(ValueError):
+        Q.HostPipeline(host.shape[1], torch.bfloat16, chunk_rows=700)(
+            host, 24, 24, 24, 128, torch.from_numpy(inp["gamma_q"]), torch.from_numpy(inp["gamma_k"]),
+            torch.from_numpy(inp["cos"]), torch.from_numpy(inp["sin"]))
