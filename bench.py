@@ -40,7 +40,7 @@ METRIC = "fused QK-RMSNorm+RoPE µs/call and achieved HBM GB/s (% of peak), Wan 
 UNIT = "us/call"
 DEFAULT_WORKLOAD = "wan_32760x40x128"
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SOURCES = ("qknr_kernel.cuh", "qknr_api.cu", "qknr_internal.h")
+KERNEL_SOURCES = ("qknr_kernel.cuh", "qknr_ptx.cuh", "qknr_api.cu", "qknr_internal.h")
 
 
 # ---------------------------------------------------------------------------
@@ -257,11 +257,16 @@ def run_reference(args, w):
 
 
 def workload_config(w, world, tokens=None):
+    if isinstance(w, I.AdaLNWorkload):
+        return {"workload": w.name, "tokens": w.tokens if tokens is None else tokens, "hidden": w.hidden,
+                "rows_per_batch": w.seq, "mod_dtype": w.mod_dtype, "in_place": True,
+                "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}"}
     return {
         "workload": w.name, "tokens": w.tokens if tokens is None else tokens, "n_heads_q": w.n_heads_q, "n_heads_k": w.n_heads_k,
         "n_heads_v": w.n_heads_v, "head_dim": w.head_dim, "layout": "packed_qkv" if w.packed else "separate",
         "rope": w.rope_style, "cos_layout": w.cos_layout, "cos_dtype": w.cos_dtype,
-        "rope_axes": list(w.axes_dim), "in_place": True,
+        "rope_axes": list(w.axes_dim), "in_place": not w.out_of_place,
+        "launch_form": ("packed" if w.packed else ("q+k in one launch" if w.single_launch else "one launch per tensor")),
         "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}",
     }
 
@@ -314,10 +319,20 @@ class Runner:
         kw = dict(rope_style=w.rope_style, cos_layout=w.cos_layout, eps=w.eps, dev_status=status, **tune)
         d = self.d
         if w.packed:
+            out = None
+            if w.out_of_place:
+                self.d["out"] = torch.empty_like(d["qkv"])
+                self.host["out"] = torch.empty_like(self.host["qkv"])
+                out = self.d["out"]
             self.args = [Q.packed_args(d["qkv"], w.n_heads_q, w.n_heads_k, w.n_heads_v, D, d["gamma_q"],
-                                       d["gamma_k"], d["cos"], d["sin"], **kw)]
+                                       d["gamma_k"], d["cos"], d["sin"], out=out, **kw)]
             self.bytes_per_launch = I.algorithmic_bytes(w, tokens=self.tokens)
-            self.outputs = ["qkv"]
+            self.outputs = ["out" if w.out_of_place else "qkv"]
+        elif w.single_launch:
+            self.args = [Q.make_args(q=d["q"], k=d["k"], n_heads_q=w.n_heads_q, n_heads_k=w.n_heads_k, head_dim=D,
+                                     gamma_q=d["gamma_q"], gamma_k=d["gamma_k"], cos=d["cos"], sin=d["sin"], **kw)]
+            self.bytes_per_launch = I.algorithmic_bytes(w, tokens=self.tokens)
+            self.outputs = ["q", "k"]
         else:
             self.args = [Q.make_args(q=d["q"], n_heads_q=w.n_heads_q, head_dim=D, gamma_q=d["gamma_q"],
                                      cos=d["cos"], sin=d["sin"], **kw),
@@ -326,6 +341,7 @@ class Runner:
             self.bytes_per_launch = I.algorithmic_bytes(w, launches="q", tokens=self.tokens)
             self.outputs = ["q", "k"]
         self.info = Q.query(self.args[0])
+        self.launch = Q.launch
 
     def step(self, stream):
         for a in self.args:
@@ -336,12 +352,13 @@ class Runner:
         through the binding's chunked host pipeline (copies in, kernel and
         copies out overlapped on three streams); separate tensors are copied
         in, processed and copied out on one stream."""
-        self.pinned = {k: v.pin_memory() for k, v in self.host.items()}
+        self.pinned = {k: v.pin_memory() for k, v in self.host.items() if k not in self.outputs or k in
+                       ("qkv", "q", "k")}
         self.pinned_out = {k: torch_empty_pinned_like(self.host[k]) for k in self.outputs}
         h2d = sum(t.numel() * t.element_size() for t in self.pinned.values())
         d2h = sum(t.numel() * t.element_size() for t in self.pinned_out.values())
         self.pipe = None
-        if self.w.packed:
+        if self.w.packed and not self.w.out_of_place:
             qkv = self.pinned["qkv"]
             self.pipe = self.Q.HostPipeline(qkv.shape[1], qkv.dtype, chunk_rows=chunk_rows, device=self.dev)
         return h2d, d2h
@@ -358,6 +375,54 @@ class Runner:
         self.step(stream)
         for k, t in self.pinned_out.items():
             t.copy_(self.d[k], non_blocking=True)
+
+
+class AdaLNRunner:
+    """Device buffers and launch arguments of an AdaLN scale/shift workload
+    (one launch per step, in place)."""
+
+    def __init__(self, w, dev, tune, status, tokens=None):
+        import torch
+
+        from diffusion_transformer_qk_gb300 import qknr as Q
+
+        self.Q, self.w, self.dev, self.tune = Q, w, dev, tune
+        self.tokens = w.tokens if tokens is None else tokens
+        self.inp = I.make_adaln_inputs(w, tokens=self.tokens)
+        act = torch.bfloat16 if w.dtype == "bf16" else torch.float16
+
+        def bits(a, dt):
+            return torch.from_numpy(a.view(np.int16)).view(dt)
+
+        self.host = {"x": bits(self.inp["x"], act)}
+        for k in ("scale", "shift"):
+            m = self.inp[k]
+            self.host[k] = torch.from_numpy(m) if w.mod_dtype == "fp32" else bits(m, act)
+        self.d = {k: v.to(dev) for k, v in self.host.items()}
+        self.args = [Q.adaln_args(self.d["x"], self.d["scale"], self.d["shift"], rows_per_batch=w.seq, eps=w.eps,
+                                  dev_status=status, **tune)]
+        self.launch = Q.adaln_launch
+        self.bytes_per_launch = I.adaln_algorithmic_bytes(w, tokens=self.tokens)
+        self.outputs = ["x"]
+        self.info = Q.adaln_query(self.args[0])
+        self.pipe = None
+
+    def step(self, stream):
+        for a in self.args:
+            self.launch(a, stream)
+
+    def e2e_buffers(self, chunk_rows):
+        self.pinned = {k: v.pin_memory() for k, v in self.host.items()}
+        self.pinned_out = {"x": torch_empty_pinned_like(self.host["x"])}
+        h2d = sum(t.numel() * t.element_size() for t in self.pinned.values())
+        d2h = self.pinned_out["x"].numel() * self.pinned_out["x"].element_size()
+        return h2d, d2h
+
+    def e2e_step(self, stream):
+        for k, t in self.pinned.items():
+            self.d[k].copy_(t, non_blocking=True)
+        self.step(stream)
+        self.pinned_out["x"].copy_(self.d["x"], non_blocking=True)
 
 
 def torch_empty_pinned_like(t):
@@ -380,7 +445,7 @@ def run_ours(args, w):
 
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     tune = dict(ctas_per_sm=args.ctas_per_sm, stages=args.stages, consumer_warps=args.consumer_warps)
-    run = Runner(w, dev, tune, status, args.tokens)
+    run = (AdaLNRunner if isinstance(w, I.AdaLNWorkload) else Runner)(w, dev, tune, status, args.tokens)
     stream = torch.cuda.current_stream(dev)
     L = len(run.args)
 
@@ -416,7 +481,7 @@ def run_ours(args, w):
             flush.fill_(1.0)
         for a in run.args:
             starts[j].record(stream)
-            Q.launch(a, stream)
+            run.launch(a, stream)
             ends[j].record(stream)
             j += 1
     e1.record(stream)
@@ -460,10 +525,10 @@ def run_ours(args, w):
                         "device->host copy overlapped on three streams" % args.e2e_chunk_rows) if run.pipe else
                        "pinned host -> device copies, qknr_forward via the Python binding, device -> pinned host, "
                        "one stream"}
-        if w.packed:
+        if getattr(w, "packed", False):
             # each e2e step starts from the host input, so V comes back unchanged
             D3 = (w.n_heads_q + w.n_heads_k) * w.head_dim
-            back = run.pinned_out["qkv"].view(torch.int16).numpy().view(np.uint16)
+            back = run.pinned_out[run.outputs[0]].view(torch.int16).numpy().view(np.uint16)
             if not np.array_equal(back[:, D3:], run.inp["qkv"][:, D3:]):
                 raise RuntimeError("e2e: V slice changed")
         if int(status.item()) != 0 or (run.pipe is not None and run.pipe.read_status() != 0):
@@ -497,7 +562,7 @@ def run_ours(args, w):
     }
     if e2e:
         line["e2e"] = e2e
-    if world == 1 and not args.no_cpu_baseline:
+    if world == 1 and not args.no_cpu_baseline and not isinstance(w, I.AdaLNWorkload):
         us, n, dt = time_oracle_workload(w, run.inp, args.cpu_seconds, run.tokens)
         line["cpu_baseline"] = {"value": us, "unit": UNIT, "cores": 1, "kind": "oracle",
                                 "sample": f"first {n} of {w.tokens} token rows, {dt:.1f} s, fp64 numpy, "
@@ -512,7 +577,7 @@ def main(argv=None):
     p.add_argument("--steps", type=int, default=5000)
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(I.WORKLOADS))
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(I.WORKLOADS) + sorted(I.ADALN_WORKLOADS))
     p.add_argument("--tokens", type=int, default=None,
                    help="run the first N token rows of the workload (small profiling cases)")
     p.add_argument("--ctas-per-sm", type=int, default=0)
@@ -527,8 +592,10 @@ def main(argv=None):
     args = p.parse_args(argv)
     if args.warmup < 3:
         p.error("--warmup must be >= 3")
-    w = I.WORKLOADS[args.workload]
+    w = I.WORKLOADS.get(args.workload) or I.ADALN_WORKLOADS[args.workload]
     if args.impl == "reference":
+        if isinstance(w, I.AdaLNWorkload):
+            p.error("--impl reference times the QK-norm + RoPE oracle; pick a QK workload")
         return run_reference(args, w)
     return run_ours(args, w)
 

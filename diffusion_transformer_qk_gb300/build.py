@@ -32,6 +32,8 @@ SOURCES = [
     "qknr_inst_bf16_bf16.cu",
     "qknr_inst_fp16_f32.cu",
     "qknr_inst_fp16_bf16.cu",
+    "adaln_api.cu",
+    "adaln_inst.cu",
 ]
 
 
@@ -53,7 +55,7 @@ def cuda_lib_dir() -> str:
 def _inputs() -> List[str]:
     files = [os.path.join(CSRC, f) for f in sorted(os.listdir(CSRC))
              if f.endswith((".cu", ".cuh", ".h"))]
-    files.append(os.path.join(INCLUDE, "qknr.h"))
+    files.extend(os.path.join(INCLUDE, f) for f in sorted(os.listdir(INCLUDE)) if f.endswith(".h"))
     files.append(os.path.abspath(__file__))
     return files
 

@@ -1,0 +1,278 @@
+// AdaLN scale/shift kernel for sm_103a: per token row, a layer norm without
+// affine over the hidden dimension followed by the per-sample modulation
+//
+//     out[c] = (x[c] - mean) * rsqrt(var + eps) * (1 + scale[b, c]) + shift[b, c]
+//
+// ("fused qknorm rope Flux 2.0", section "Not in this PR — follow-ups":
+// AdaLN's fuse_scale_shift, 81 calls per FLUX.2 step).
+//
+// Same streaming structure as the QK kernel: a persistent CTA per SM, one
+// producer lane bulk-copying token rows into per-group shared-memory rings,
+// consumer warps in groups that each take whole rows.  A group of GW warps
+// covers one row: lane l of warp w holds the 16-byte chunks
+// k = (w*32 + l) + i*32*GW, i < CPL, in fp32 registers.  Mean and variance
+// are exact two-pass sums (mean first, then centred squares from the
+// registers), each reduced by shuffles inside a warp and through shared
+// memory plus a named barrier across the group.  A warp hands the stage
+// back as soon as its chunks are in registers.
+//
+// Every mbarrier wait is bounded.  The decision to continue is collective:
+// each warp posts whether its wait succeeded with its first partial sum,
+// and the group leaves the row loop together when any warp failed, so no
+// warp can be left waiting at a named barrier for one that gave up.
+#pragma once
+
+#include "qknr_ptx.cuh"
+
+namespace qknr {
+
+constexpr int kAdaMaxWarps = 16;
+constexpr int kAdaMaxThreads = 32 * (kAdaMaxWarps + 1);
+constexpr int kAdaMaxStages = 32;                 // all groups' rings together
+constexpr int kAdaMaxGroups = 8;                  // named barriers 1..8
+// dynamic shared memory map (bytes)
+constexpr int kAdaOffBarriers = 0;                // full[32], empty[32]
+constexpr int kAdaOffAbort = 512;
+constexpr int kAdaOffPartial = 1024;              // per group: [3][kAdaMaxWarps] floats (two sums, ok flags)
+constexpr int kAdaOffStage0 = 1024 + kAdaMaxGroups * 3 * kAdaMaxWarps * 4 + 512;   // 3072
+constexpr int kAdaStageAlign = 128;
+
+struct AdaLNParams {
+  const char* x;
+  char* out;
+  long long x_stride, out_stride;                 // bytes per row
+  long long tokens;
+  long long rows_per_batch;
+  const char* scale;
+  const char* shift;
+  long long mod_stride;                           // bytes between samples' rows
+  int* status;
+  unsigned long long wait_limit_ns;
+  float eps;
+  float inv_c;
+  int hidden;                                     // C (multiple of 8)
+  int consumer_warps;
+  int group_warps;
+  int stages;                                     // ring depth per group
+  unsigned flags;
+  unsigned row_bytes;                             // C * 2
+  unsigned stage_bytes;
+};
+
+__device__ __forceinline__ void named_barrier(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// 8 modulation values of chunk k as fp32 pairs
+template <typename MT>
+__device__ __forceinline__ void load_mod8(const char* row, int k, float2 (&m)[4]);
+
+template <>
+__device__ __forceinline__ void load_mod8<float>(const char* row, int k, float2 (&m)[4]) {
+  const float4 a = __ldg(reinterpret_cast<const float4*>(row) + 2 * k);
+  const float4 b = __ldg(reinterpret_cast<const float4*>(row) + 2 * k + 1);
+  m[0] = make_float2(a.x, a.y); m[1] = make_float2(a.z, a.w);
+  m[2] = make_float2(b.x, b.y); m[3] = make_float2(b.z, b.w);
+}
+
+template <>
+__device__ __forceinline__ void load_mod8<__nv_bfloat16>(const char* row, int k, float2 (&m)[4]) {
+  Elem<__nv_bfloat16>::unpack(__ldg(reinterpret_cast<const uint4*>(row) + k), m);
+}
+
+template <>
+__device__ __forceinline__ void load_mod8<__half>(const char* row, int k, float2 (&m)[4]) {
+  Elem<__half>::unpack(__ldg(reinterpret_cast<const uint4*>(row) + k), m);
+}
+
+template <typename T, typename MT, int CPL>
+__global__ void __launch_bounds__(kAdaMaxThreads, 1) adaln_kernel(const __grid_constant__ AdaLNParams p) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int NW = p.consumer_warps;
+  const int GW = p.group_warps;
+  const int n_groups = NW / GW;
+  const int S = p.stages;
+  const uint32_t base = smem_addr(smem);
+  const uint32_t full0 = base + kAdaOffBarriers;
+  const uint32_t empty0 = base + kAdaOffBarriers + 8 * kAdaMaxStages;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kAdaOffAbort);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S * n_groups; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, GW);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  const unsigned long long limit = p.wait_limit_ns;
+
+  if (warp == NW) {
+    // ---------------- producer: one lane, one bulk copy per row
+    if (lane != 0) return;
+    const uint32_t stage0 = base + kAdaOffStage0;
+    long long issued = 0;
+    int g = 0, js = 0;
+    uint32_t ph = 0;
+    const long long step = gridDim.x;
+    unsigned long long src = reinterpret_cast<unsigned long long>(p.x) + blockIdx.x * p.x_stride;
+    const unsigned long long src_step = step * p.x_stride;
+    bool ok = true;
+    for (long long row = blockIdx.x; row < p.tokens; row += step) {
+      const int s = g * S + js;
+      const uint32_t empty = empty0 + 8 * s;
+      if (!mbar_try_wait(empty, ph ^ 1u) && !bounded_wait(empty, ph ^ 1u, limit, abort_flag, p.status)) {
+        ok = false;
+        break;
+      }
+      if (p.flags & 1u) break;                    // test only: issue nothing
+      const uint32_t full = full0 + 8 * s;
+      mbar_arrive_expect_tx(full, p.row_bytes);
+      bulk_load(stage0 + s * p.stage_bytes, reinterpret_cast<const void*>(src), p.row_bytes, full);
+      ++issued;
+      src += src_step;
+      if (++g == n_groups) {
+        g = 0;
+        if (++js == S) {
+          js = 0;
+          ph ^= 1u;
+        }
+      }
+    }
+    if (!ok || *abort_flag) {
+      // wait (bounded) for the copies of the latest use of every stage
+      const long long total = static_cast<long long>(n_groups) * S;
+      const long long first = issued > total ? issued - total : 0;
+      for (long long it = first; it < issued; ++it) {
+        const long long j = it / n_groups;
+        const uint32_t bar = full0 + 8 * (static_cast<int>(it % n_groups) * S + static_cast<int>(j % S));
+        const uint32_t phase = static_cast<uint32_t>((j / S) & 1);
+        const unsigned long long t0 = global_timer_ns();
+        while (!mbar_try_wait(bar, phase) && global_timer_ns() - t0 < limit) {
+        }
+      }
+    }
+    return;
+  }
+
+  // ---------------- consumer warps
+  const int grp = warp / GW, gw = warp % GW;
+  const int gthreads = GW * 32;
+  const int bar_id = 1 + grp;
+  float* part = reinterpret_cast<float*>(smem + kAdaOffPartial) + grp * 3 * kAdaMaxWarps;   // [3][GW]
+  const int n_chunks = p.hidden / 8;
+  const int lane_g = gw * 32 + lane;
+  const float eps = p.eps, inv_c = p.inv_c;
+  const int ring0 = grp * S;
+
+  int s = 0;
+  uint32_t ph = 0;
+  const long long step = static_cast<long long>(n_groups) * gridDim.x;
+  long long row = blockIdx.x + static_cast<long long>(grp) * gridDim.x;
+  // sample of the current row, kept as a running quotient and remainder
+  long long batch = row / p.rows_per_batch;
+  long long in_batch = row - batch * p.rows_per_batch;
+  const long long step_b = step / p.rows_per_batch, step_r = step - step_b * p.rows_per_batch;
+  for (; row < p.tokens; row += step) {
+    const uint32_t full = full0 + 8 * (ring0 + s);
+    const bool ok = mbar_try_wait(full, ph) || bounded_wait(full, ph, limit, abort_flag, p.status);
+
+    float2 X[CPL][4];                             // this lane's chunks of the row
+    float s1 = 0.0f;
+    if (ok) {
+      const unsigned char* st = smem + kAdaOffStage0 + (ring0 + s) * p.stage_bytes;
+#pragma unroll
+      for (int i = 0; i < CPL; ++i) {
+        const int k = lane_g + i * gthreads;
+        if (k < n_chunks) {
+          Elem<T>::unpack(*reinterpret_cast<const uint4*>(st + k * 16), X[i]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) X[i][j] = make_float2(0.0f, 0.0f);
+        }
+      }
+      // the row is in registers: hand the stage back
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty0 + 8 * (ring0 + s));
+      float2 a = make_float2(0.0f, 0.0f);
+#pragma unroll
+      for (int i = 0; i < CPL; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) a = __fadd2_rn(a, X[i][j]);
+      s1 = __fadd_rn(a.x, a.y);
+#pragma unroll
+      for (int off = 16; off >= 1; off >>= 1) s1 = __fadd_rn(s1, __shfl_xor_sync(0xffffffffu, s1, off));
+    }
+    // pass 1: post the warp's sum and whether its wait succeeded
+    if (lane == 0) {
+      part[gw] = s1;
+      part[2 * kAdaMaxWarps + gw] = ok ? 1.0f : 0.0f;
+    }
+    named_barrier(bar_id, gthreads);
+    bool all_ok = true;
+    float sum = 0.0f;
+    for (int w = 0; w < GW; ++w) {
+      sum = __fadd_rn(sum, part[w]);
+      all_ok = all_ok && part[2 * kAdaMaxWarps + w] != 0.0f;
+    }
+    if (!all_ok) break;                           // every warp of the group leaves together
+    const float mu = __fmul_rn(sum, inv_c);
+    const float2 nmu = make_float2(-mu, -mu);
+    // pass 2: centred squares from the registers
+    float2 q = make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) {
+      if (lane_g + i * gthreads < n_chunks) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float2 d = __fadd2_rn(X[i][j], nmu);
+          q = __ffma2_rn(d, d, q);
+        }
+      }
+    }
+    float s2 = __fadd_rn(q.x, q.y);
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) s2 = __fadd_rn(s2, __shfl_xor_sync(0xffffffffu, s2, off));
+    if (lane == 0) part[kAdaMaxWarps + gw] = s2;
+    named_barrier(bar_id, gthreads);
+    float ssq = 0.0f;
+    for (int w = 0; w < GW; ++w) ssq = __fadd_rn(ssq, part[kAdaMaxWarps + w]);
+    const float r = rsqrtf(__fmaf_rn(ssq, inv_c, eps));
+    const float2 R = make_float2(r, r);
+    // modulation rows of this row's sample: the same two rows for every row
+    // of the sample, so these reads hit L1/L2
+    const char* srow = p.scale + batch * p.mod_stride;
+    const char* hrow = p.shift + batch * p.mod_stride;
+    char* orow = p.out + row * p.out_stride;
+#pragma unroll
+    for (int i = 0; i < CPL; ++i) {
+      const int k = lane_g + i * gthreads;
+      if (k < n_chunks) {
+        float2 sc[4], sh[4], o[4];
+        load_mod8<MT>(srow, k, sc);
+        load_mod8<MT>(hrow, k, sh);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float2 sc1 = __fadd2_rn(sc[j], make_float2(1.0f, 1.0f));
+          o[j] = __ffma2_rn(__fmul2_rn(__fadd2_rn(X[i][j], nmu), R), sc1, sh[j]);
+        }
+        store16(orow + k * 16, Elem<T>::pack(o));
+      }
+    }
+    if (++s == S) {
+      s = 0;
+      ph ^= 1u;
+    }
+    batch += step_b;
+    in_batch += step_r;
+    if (in_batch >= p.rows_per_batch) {
+      in_batch -= p.rows_per_batch;
+      ++batch;
+    }
+  }
+}
+
+}  // namespace qknr

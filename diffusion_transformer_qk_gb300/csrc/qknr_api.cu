@@ -11,8 +11,9 @@
 
 #include "../../include/qknr.h"
 #include "qknr_internal.h"
+#include "qknr_host.h"
 
-namespace {
+namespace qknr_host {
 
 thread_local char g_err[512] = "";
 
@@ -28,17 +29,12 @@ qknr_status cuda_fail(cudaError_t e, const char* what) {
   return fail(QKNR_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
-struct DeviceInfo {
-  int num_sms = 0;
-  int smem_optin = 0;       // max dynamic shared memory per block (opt-in)
-  int smem_per_sm = 0;
-  int smem_reserved = 0;    // per-block reservation
-};
-
+namespace {
 std::mutex g_mu;
 std::unordered_map<int, DeviceInfo> g_dev;
 std::unordered_map<const void*, int> g_configured;   // kernel -> device mask with attribute set
 std::unordered_map<const void*, int> g_regs;
+}  // namespace
 
 qknr_status device_info(int dev, DeviceInfo* out) {
   std::lock_guard<std::mutex> lk(g_mu);
@@ -65,8 +61,6 @@ qknr_status device_info(int dev, DeviceInfo* out) {
   return QKNR_OK;
 }
 
-// Set the kernel's dynamic shared memory ceiling to the device maximum
-// (once per kernel and device) and return its register count.
 qknr_status configure_kernel(const void* fn, int dev, const DeviceInfo& di, int* regs) {
   std::lock_guard<std::mutex> lk(g_mu);
   int& mask = g_configured[fn];
@@ -83,10 +77,6 @@ qknr_status configure_kernel(const void* fn, int dev, const DeviceInfo& di, int*
   return QKNR_OK;
 }
 
-struct Span {
-  uintptr_t lo, hi;   // [lo, hi)
-};
-
 Span span_of(const void* base, long long rows, long long stride_bytes, long long row_bytes) {
   uintptr_t lo = reinterpret_cast<uintptr_t>(base);
   if (!base || rows <= 0 || row_bytes <= 0) return {lo, lo};
@@ -94,6 +84,19 @@ Span span_of(const void* base, long long rows, long long stride_bytes, long long
 }
 
 bool overlaps(Span a, Span b) { return a.lo < a.hi && b.lo < b.hi && a.lo < b.hi && b.lo < a.hi; }
+
+}  // namespace qknr_host
+
+namespace {
+
+using qknr_host::cuda_fail;
+using qknr_host::DeviceInfo;
+using qknr_host::fail;
+using qknr_host::overlaps;
+using qknr_host::Span;
+using qknr_host::span_of;
+using qknr_host::device_info;
+using qknr_host::configure_kernel;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -448,7 +451,7 @@ const char* qknr_status_string(int32_t s) {
   }
 }
 
-const char* qknr_last_error(void) { return g_err; }
+const char* qknr_last_error(void) { return qknr_host::g_err; }
 
 int32_t qknr_abi_version(void) { return QKNR_ABI_VERSION; }
 

@@ -1,0 +1,171 @@
+// PTX helpers shared by the library's kernels (sm_100 family): mbarriers,
+// 1-D bulk copies into shared memory, %globaltimer-bounded waits, streaming
+// stores and 16-byte <-> fp32-pair conversions of bf16/fp16 storage.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace qknr {
+
+constexpr int kStatusTimeout = 6;     // QKNR_ERR_TIMEOUT
+
+// ---------------------------------------------------------------------------
+// PTX helpers
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ unsigned long long global_timer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// 1-D bulk copy global -> this CTA's shared memory, completion counted in
+// bytes on `bar`.  Both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// Wait for phase `parity` of `bar` to complete, giving up at the deadline
+// or when another warp of the CTA has aborted.  Returns false on give-up.
+static __device__ __noinline__ bool bounded_wait(uint32_t bar, uint32_t parity,
+                                          unsigned long long limit_ns, volatile int* abort_flag,
+                                          int* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_timer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (global_timer_ns() - t0 > limit_ns) {
+      *abort_flag = 1;
+      if (status) atomicCAS(status, 0, kStatusTimeout);
+      return false;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// element conversions: 16 bytes of storage <-> 4 fp32 pairs (elements 2i, 2i+1)
+// Arithmetic runs on Blackwell's paired fp32 instructions (__ffma2_rn and
+// friends), each half rounded exactly as the scalar instruction would.
+
+template <typename T>
+struct Elem;
+
+template <>
+struct Elem<__nv_bfloat16> {
+  // X[i] = (x[2i], x[2i+1])
+  static __device__ __forceinline__ void unpack(const uint4& r, float2 (&X)[4]) {
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) X[i] = make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u));
+  }
+  // X[i] = (x[2i+1], x[2i])
+  static __device__ __forceinline__ void unpack_swapped(const uint4& r, float2 (&X)[4]) {
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) X[i] = make_float2(__uint_as_float(w[i] & 0xffff0000u), __uint_as_float(w[i] << 16));
+  }
+  static __device__ __forceinline__ uint4 pack(const float2 (&O)[4]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      __nv_bfloat162 h = __floats2bfloat162_rn(O[i].x, O[i].y);
+      w[i] = *reinterpret_cast<uint32_t*>(&h);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+  }
+};
+
+template <>
+struct Elem<__half> {
+  static __device__ __forceinline__ void unpack(const uint4& r, float2 (&X)[4]) {
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) X[i] = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
+  }
+  static __device__ __forceinline__ void unpack_swapped(const uint4& r, float2 (&X)[4]) {
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __half2 h = *reinterpret_cast<const __half2*>(&w[i]);
+      X[i] = make_float2(__high2float(h), __low2float(h));
+    }
+  }
+  static __device__ __forceinline__ uint4 pack(const float2 (&O)[4]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      __half2 h = __floats2half2_rn(O[i].x, O[i].y);
+      w[i] = *reinterpret_cast<uint32_t*>(&h);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+  }
+};
+
+// 8 consecutive cos (or sin) values from shared memory, widened to fp32 pairs.
+template <typename CT>
+__device__ __forceinline__ void load_table8(const unsigned char* p, float2 (&c)[4]);
+
+template <>
+__device__ __forceinline__ void load_table8<float>(const unsigned char* p, float2 (&c)[4]) {
+  const float4 a = *reinterpret_cast<const float4*>(p);
+  const float4 b = *reinterpret_cast<const float4*>(p + 16);
+  c[0] = make_float2(a.x, a.y); c[1] = make_float2(a.z, a.w);
+  c[2] = make_float2(b.x, b.y); c[3] = make_float2(b.z, b.w);
+}
+
+template <>
+__device__ __forceinline__ void load_table8<__nv_bfloat16>(const unsigned char* p, float2 (&c)[4]) {
+  Elem<__nv_bfloat16>::unpack(*reinterpret_cast<const uint4*>(p), c);
+}
+
+
+// 16-byte streaming store to global memory (written once, not re-read).
+__device__ __forceinline__ void store16(char* dst, const uint4& v) {
+  __stcs(reinterpret_cast<uint4*>(dst), v);
+}
+
+}  // namespace qknr

@@ -58,6 +58,8 @@ class Workload:
     scale: float = 1.0             # activations are scale * N(0,1)
     eps: float = 1e-6
     seed: int = 0
+    single_launch: bool = False    # separate tensors: Q and K in one launch
+    out_of_place: bool = False     # write Q/K (and copy V) to a second buffer
 
     @property
     def tokens(self) -> int:
@@ -95,6 +97,20 @@ WORKLOADS: Dict[str, Workload] = {
         "rotate_half", "fp32", "shared_row", "flux2d1d", (512, 64, 64),
         (32, 48, 48)),
 }
+
+# Variants of the same workloads for the staging and launch-form comparisons:
+# bf16 tables (shared and expanded), out-of-place with V copied once, and
+# FLUX.2's Q and K in one launch instead of one launch per tensor.
+WORKLOADS.update({
+    "wan_32760x40x128_bf16cos": WORKLOADS["wan_32760x40x128"].with_(
+        name="wan_32760x40x128_bf16cos", cos_dtype="bf16"),
+    "wan_32760x40x128_expanded_bf16cos": WORKLOADS["wan_32760x40x128_expanded"].with_(
+        name="wan_32760x40x128_expanded_bf16cos", cos_dtype="bf16"),
+    "wan_32760x40x128_out_of_place": WORKLOADS["wan_32760x40x128"].with_(
+        name="wan_32760x40x128_out_of_place", out_of_place=True),
+    "flux2_2x4608x48x128_single_launch": WORKLOADS["flux2_2x4608x48x128"].with_(
+        name="flux2_2x4608x48x128_single_launch", single_launch=True),
+})
 
 
 # --------------------------------------------------------------------------
@@ -256,6 +272,7 @@ def algorithmic_bytes(w: Workload, v_copied: bool = False, launches: str = "all"
     hq, hk = w.n_heads_q, w.n_heads_k
     if launches == "q":
         hk = 0
+    v_copied = v_copied or w.out_of_place
     cos_es = 4 if w.cos_dtype == "fp32" else 2
     if w.cos_layout == "shared_row":
         cos_bytes = 2 * min(w.seq, T) * D * cos_es
@@ -265,3 +282,61 @@ def algorithmic_bytes(w: Workload, v_copied: bool = False, launches: str = "all"
     v = 2 * T * w.n_heads_v * D * es if v_copied else 0
     gam = (2 if hk else 1) * D * 4
     return qk + cos_bytes + v + gam
+
+
+# --------------------------------------------------------------------------
+# AdaLN scale/shift workloads (the next fused step named by "fused qknorm
+# rope Flux 2.0", section "Not in this PR — follow-ups": fuse_scale_shift,
+# 81 calls per FLUX.2 step)
+
+@dataclass(frozen=True)
+class AdaLNWorkload:
+    """Token rows [batch*seq, hidden] with one modulation row per sample."""
+
+    name: str
+    batch: int
+    seq: int                       # rows per sample (one scale/shift row each)
+    hidden: int
+    dtype: str = "bf16"            # activations
+    mod_dtype: str = "bf16"        # scale / shift storage: "fp32" or the activation dtype
+    scale: float = 1.0             # activations are scale * N(0,1)
+    mod_scale: float = 0.1         # scale and shift are mod_scale * N(0,1)
+    eps: float = 1e-6
+    seed: int = 0
+
+    @property
+    def tokens(self) -> int:
+        return self.batch * self.seq
+
+    def with_(self, **kw) -> "AdaLNWorkload":
+        return replace(self, **kw)
+
+
+ADALN_WORKLOADS: Dict[str, AdaLNWorkload] = {
+    # FLUX.2 single-stream block: 2 x (512 text + 4096 image) tokens, hidden 48*128
+    "adaln_flux2_2x4608x6144": AdaLNWorkload("adaln_flux2_2x4608x6144", 2, 4608, 6144),
+    # Wan-A14B: 32760 latent tokens, hidden 40*128
+    "adaln_wan_32760x5120": AdaLNWorkload("adaln_wan_32760x5120", 1, 32760, 5120),
+}
+
+
+def make_adaln_inputs(w: AdaLNWorkload, tokens: Optional[int] = None) -> Dict[str, np.ndarray]:
+    """Seeded instance: draw order x, scale, shift (numpy PCG64(w.seed)).
+    ``x`` is [T, C] uint16 bits; ``scale``/``shift`` are [B, C] fp32 or
+    uint16 bits of the activation dtype.  ``tokens`` overrides T."""
+    T = w.tokens if tokens is None else int(tokens)
+    B = max(1, -(-T // w.seq))
+    g = np.random.Generator(np.random.PCG64(w.seed))
+    out = {"x": to_storage_bits(_normal(g, (T, w.hidden), w.scale), w.dtype)}
+    for k in ("scale", "shift"):
+        m = _normal(g, (B, w.hidden), w.mod_scale)
+        out[k] = m if w.mod_dtype == "fp32" else to_storage_bits(m, w.mod_dtype)
+    return out
+
+
+def adaln_algorithmic_bytes(w: AdaLNWorkload, tokens: Optional[int] = None) -> int:
+    """x read once and written once, plus every sample's scale and shift rows."""
+    T = w.tokens if tokens is None else int(tokens)
+    B = max(1, -(-T // w.seq))
+    mes = 4 if w.mod_dtype == "fp32" else 2
+    return 2 * T * w.hidden * 2 + 2 * B * w.hidden * mes

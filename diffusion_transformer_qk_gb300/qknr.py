@@ -36,6 +36,7 @@ ABI_VERSION = 1
 EXPORTS = (
     "qknr_args_init", "qknr_forward", "qknr_query", "qknr_status_string",
     "qknr_last_error", "qknr_abi_version", "qknr_sizeof_args", "qknr_sizeof_launch_info",
+    "qknr_adaln_args_init", "qknr_adaln_forward", "qknr_adaln_query", "qknr_adaln_sizeof_args",
 )
 
 
@@ -77,6 +78,21 @@ class QknrLaunchInfo(ctypes.Structure):
         return d
 
 
+class QknrAdaLNArgs(ctypes.Structure):
+    """Mirror of ``qknr_adaln_args``."""
+
+    _fields_ = [
+        ("abi_version", c_uint32), ("dtype", c_int32),
+        ("x", c_void_p), ("out", c_void_p),
+        ("x_stride", c_int64), ("out_stride", c_int64),
+        ("tokens", c_int64), ("hidden", c_int32), ("rows_per_batch", c_int64),
+        ("scale", c_void_p), ("shift", c_void_p), ("mod_dtype", c_int32), ("mod_stride", c_int64),
+        ("eps", c_float), ("dev_status", c_void_p),
+        ("ctas_per_sm", c_int32), ("stages", c_int32), ("consumer_warps", c_int32), ("group_warps", c_int32),
+        ("flags", c_uint32), ("wait_limit_ns", c_uint64),
+    ]
+
+
 class QknrError(RuntimeError):
     def __init__(self, status: int, message: str):
         super().__init__(f"{STATUS.get(status, status)}: {message}")
@@ -116,10 +132,18 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         lib.qknr_abi_version.restype = c_int32
         lib.qknr_sizeof_args.restype = c_size_t
         lib.qknr_sizeof_launch_info.restype = c_size_t
+        lib.qknr_adaln_args_init.argtypes = [ctypes.POINTER(QknrAdaLNArgs)]
+        lib.qknr_adaln_args_init.restype = None
+        lib.qknr_adaln_forward.argtypes = [ctypes.POINTER(QknrAdaLNArgs), c_void_p]
+        lib.qknr_adaln_forward.restype = c_int32
+        lib.qknr_adaln_query.argtypes = [ctypes.POINTER(QknrAdaLNArgs), ctypes.POINTER(QknrLaunchInfo)]
+        lib.qknr_adaln_query.restype = c_int32
+        lib.qknr_adaln_sizeof_args.restype = c_size_t
         if lib.qknr_abi_version() != ABI_VERSION:
             raise RuntimeError("libqknr.so ABI version mismatch")
         if lib.qknr_sizeof_args() != ctypes.sizeof(QknrArgs) or \
-                lib.qknr_sizeof_launch_info() != ctypes.sizeof(QknrLaunchInfo):
+                lib.qknr_sizeof_launch_info() != ctypes.sizeof(QknrLaunchInfo) or \
+                lib.qknr_adaln_sizeof_args() != ctypes.sizeof(QknrAdaLNArgs):
             raise RuntimeError("libqknr.so struct layout differs from the binding")
         if path is None:
             _lib = lib
@@ -443,3 +467,68 @@ class HostPipeline:
         done.record(self.d2h)
         compute.wait_event(done)
         return out_host
+
+
+# ---------------------------------------------------------------------------
+# AdaLN scale/shift (include/qknr_adaln.h)
+
+def adaln_args(x, scale, shift, *, rows_per_batch=None, out=None, eps=1e-6, dev_status=None, ctas_per_sm=0,
+               stages=0, consumer_warps=0, group_warps=0, flags=0, wait_limit_ns=0) -> QknrAdaLNArgs:
+    """Arguments for ``out = LN(x) * (1 + scale[b]) + shift[b]`` over token
+    rows ``x`` [T, C]; ``scale``/``shift`` are [B, C] (fp32 or x's dtype);
+    row t belongs to sample t // rows_per_batch (default: one sample)."""
+    a = QknrAdaLNArgs()
+    load().qknr_adaln_args_init(ctypes.byref(a))
+    if x.dtype not in _ACT:
+        raise ValueError("x must be bfloat16 or float16")
+    a.dtype = _ACT[x.dtype]
+    a.x, a.x_stride = x.data_ptr(), _rows(x, "x")
+    if out is not None:
+        if out.dtype != x.dtype or out.shape != x.shape:
+            raise ValueError("out must match x's shape and dtype")
+        a.out, a.out_stride = out.data_ptr(), _rows(out, "out")
+    a.tokens, a.hidden = x.shape[0], x.shape[1]
+    a.rows_per_batch = rows_per_batch or 0
+    for m, name in ((scale, "scale"), (shift, "shift")):
+        if m.dim() != 2 or m.shape[1] != x.shape[1] or m.dtype != scale.dtype:
+            raise ValueError(f"{name} must be [B, C] like scale")
+    if scale.dtype == torch.float32:
+        a.mod_dtype = FP32
+    elif scale.dtype == x.dtype:
+        a.mod_dtype = a.dtype
+    else:
+        raise ValueError("scale/shift must be float32 or x's dtype")
+    a.scale, a.shift = scale.data_ptr(), shift.data_ptr()
+    if _rows(scale, "scale") != _rows(shift, "shift"):
+        raise ValueError("scale and shift need the same row stride")
+    a.mod_stride = _rows(scale, "scale")
+    a.eps = eps
+    a.dev_status = _ptr(dev_status)
+    a.ctas_per_sm, a.stages, a.consumer_warps, a.group_warps = ctas_per_sm, stages, consumer_warps, group_warps
+    a.flags, a.wait_limit_ns = flags, wait_limit_ns
+    return a
+
+
+def adaln_launch(a: QknrAdaLNArgs, stream: Optional[torch.cuda.Stream] = None) -> None:
+    lib = load()
+    s = torch.cuda.current_stream() if stream is None else stream
+    st = lib.qknr_adaln_forward(ctypes.byref(a), c_void_p(s.cuda_stream))
+    if st != OK:
+        raise QknrError(st, lib.qknr_last_error().decode())
+
+
+def adaln_query(a: QknrAdaLNArgs) -> dict:
+    lib = load()
+    info = QknrLaunchInfo()
+    st = lib.qknr_adaln_query(ctypes.byref(a), ctypes.byref(info))
+    if st != OK:
+        raise QknrError(st, lib.qknr_last_error().decode())
+    return info.as_dict()
+
+
+def adaln_modulate(x, scale, shift, *, rows_per_batch=None, out=None, stream=None, status=True, **kw):
+    """AdaLN scale/shift on token rows ``x``; in place unless ``out`` is given."""
+    if status and "dev_status" not in kw:
+        kw["dev_status"] = status_buffer(x.device)
+    adaln_launch(adaln_args(x, scale, shift, rows_per_batch=rows_per_batch, out=out, **kw), stream)
+    return x if out is None else out

@@ -11,7 +11,7 @@ import pytest
 from diffusion_transformer_qk_gb300 import qknr as Q
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-HEADER = os.path.join(ROOT, "include", "qknr.h")
+INCLUDE = os.path.join(ROOT, "include")
 
 
 @pytest.fixture(scope="module")
@@ -20,9 +20,12 @@ def lib(built_lib):
 
 
 def declared_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(qknr_[a-z_]+)\s*\(", text)))
+    names = set()
+    for f in sorted(os.listdir(INCLUDE)):
+        if f.endswith(".h"):
+            text = re.sub(r"/\*.*?\*/", "", open(os.path.join(INCLUDE, f)).read(), flags=re.S)
+            names.update(re.findall(r"\b(qknr_[a-z_]+)\s*\(", text))
+    return sorted(names)
 
 
 def test_header_declares_the_binding_exports():
@@ -35,6 +38,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_struct_layouts_match(lib):
+    assert lib.qknr_adaln_sizeof_args() == ctypes.sizeof(Q.QknrAdaLNArgs)
     assert lib.qknr_sizeof_args() == ctypes.sizeof(Q.QknrArgs)
     assert lib.qknr_sizeof_launch_info() == ctypes.sizeof(Q.QknrLaunchInfo)
     assert lib.qknr_abi_version() == Q.ABI_VERSION
@@ -161,3 +165,60 @@ def test_query_validates_too(lib):
 def test_product_path_fails_loudly_without_library(tmp_path):
     with pytest.raises(RuntimeError):
         Q.load(str(tmp_path / "libqknr.so"))
+
+
+# ---------------------------------------------------------------------------
+# AdaLN scale/shift host validation
+
+def valid_adaln(T=64, C=6144):
+    a = Q.QknrAdaLNArgs()
+    Q.load().qknr_adaln_args_init(ctypes.byref(a))
+    a.x, a.tokens, a.hidden = FAKE, T, C
+    a.scale, a.shift = FAKE + (1 << 30), FAKE + (2 << 30)
+    return a
+
+
+def adaln_call(lib, a):
+    return lib.qknr_adaln_forward(ctypes.byref(a), None), lib.qknr_last_error().decode()
+
+
+def test_adaln_args_init_defaults(lib):
+    a = Q.QknrAdaLNArgs()
+    ctypes.memset(ctypes.byref(a), 0xFF, ctypes.sizeof(a))
+    lib.qknr_adaln_args_init(ctypes.byref(a))
+    assert a.abi_version == Q.ABI_VERSION and a.dtype == Q.BF16 and a.mod_dtype == Q.BF16
+    assert abs(a.eps - 1e-6) < 1e-12 and a.x is None and a.tokens == 0
+
+
+@pytest.mark.parametrize("mutate,expect", [
+    (lambda a: setattr(a, "abi_version", 3), 8),
+    (lambda a: setattr(a, "dtype", 2), 4),
+    (lambda a: setattr(a, "mod_dtype", 1), 4),            # fp16 modulation for bf16 activations
+    (lambda a: setattr(a, "hidden", 100), 4),             # not a multiple of 8
+    (lambda a: setattr(a, "hidden", 16384), 4),
+    (lambda a: setattr(a, "tokens", -1), 2),
+    (lambda a: setattr(a, "rows_per_batch", -5), 2),
+    (lambda a: setattr(a, "eps", -0.5), 2),
+    (lambda a: setattr(a, "x", None), 1),
+    (lambda a: setattr(a, "shift", None), 1),
+    (lambda a: setattr(a, "x_stride", 6000), 2),
+    (lambda a: setattr(a, "x", FAKE + 8), 3),
+    (lambda a: setattr(a, "x_stride", 6148), 3),          # 8-byte row stride
+    (lambda a: setattr(a, "scale", FAKE + (1 << 30) + 4), 3),
+    (lambda a: setattr(a, "out", FAKE + 2 * 6144 * 2), 7),  # out lands inside x
+    (lambda a: setattr(a, "out", FAKE + (2 << 30)), 7),   # out on shift
+    (lambda a: setattr(a, "stages", 1), 2),
+    (lambda a: (setattr(a, "consumer_warps", 16), setattr(a, "group_warps", 3)), 2),
+])
+def test_adaln_validation_rejects(lib, mutate, expect):
+    a = valid_adaln()
+    mutate(a)
+    st, msg = adaln_call(lib, a)
+    assert st == expect, (st, msg)
+    assert msg
+
+
+def test_adaln_zero_tokens_is_ok_without_cuda(lib):
+    a = valid_adaln(T=0)
+    a.x = a.scale = a.shift = None
+    assert adaln_call(lib, a)[0] == 0

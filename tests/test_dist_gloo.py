@@ -36,7 +36,7 @@ def _rank_main(rank, world, port, out):
 def test_two_rank_max_and_whole_job_rate():
     world = 2
     port = _free_port()
-    mgr = mp.Manager()
+    mgr = mp.get_context("spawn").Manager()
     out = mgr.dict()
     mp.start_processes(_rank_main, args=(world, port, out), nprocs=world, start_method="spawn", join=True)
     assert out[0] == out[1]
