@@ -37,7 +37,7 @@ qknr_status plan(const qknr_adaln_args* a, AdaPlan* pl, bool size_device) {
   if (a->mod_dtype != QKNR_FP32 && a->mod_dtype != a->dtype)
     return fail(QKNR_ERR_UNSUPPORTED, "scale/shift dtype must be FP32 or the activation dtype");
   const int C = a->hidden;
-  if (C < 8 || C % 8 || C > 12288) return fail(QKNR_ERR_UNSUPPORTED, "hidden %d (a multiple of 8, <= 12288)", C);
+  if (C < 8 || C % 8 || C > 32768) return fail(QKNR_ERR_UNSUPPORTED, "hidden %d (a multiple of 8, <= 32768)", C);
   if (a->tokens < 0 || a->rows_per_batch < 0) return fail(QKNR_ERR_SHAPE, "negative tokens or rows_per_batch");
   if (!(a->eps >= 0.0f)) return fail(QKNR_ERR_SHAPE, "eps must be >= 0");
   if (a->consumer_warps < 0 || a->consumer_warps > qknr::kAdaMaxWarps)
@@ -112,16 +112,18 @@ qknr_status plan(const qknr_adaln_args* a, AdaPlan* pl, bool size_device) {
   const long long fit = (budget - qknr::kAdaOffStage0) / kp.stage_bytes;
   const long long grid0 = (long long)di.num_sms * cps;
   const long long rows_per_cta = (T + grid0 - 1) / grid0;
-  // Group size: the fewest warps that hold a row in at most 3 chunks of 16
-  // bytes per lane, with at most 8 groups, two stages each, that fit.
+  // Group size (sweeps on GB300, hidden 5120 and 6144): about 12 chunks of
+  // 16 bytes per lane, i.e. 2 warps per row and 8 rows in flight with 16
+  // warps; at most 8 groups, two stages each that fit, and no more groups
+  // than the rows a CTA sees.
   int gw = a->group_warps;
   if (gw == 0) {
+    const int want = (n_chunks + 32 * 12 - 1) / (32 * 12);
     gw = warps;
-    for (int g = 1; g <= warps; ++g) {
+    for (int g = want < 1 ? 1 : want; g <= warps; ++g) {
       if (warps % g) continue;
-      const int cpl = (n_chunks + 32 * g - 1) / (32 * g);
       const int ng = warps / g;
-      if (cpl <= 3 && ng <= qknr::kAdaMaxGroups && 2LL * ng <= fit && ng <= rows_per_cta) {
+      if (ng <= qknr::kAdaMaxGroups && 2LL * ng <= fit && ng <= rows_per_cta) {
         gw = g;
         break;
       }
@@ -131,16 +133,12 @@ qknr_status plan(const qknr_adaln_args* a, AdaPlan* pl, bool size_device) {
   const int n_groups = warps / gw;
   if (n_groups > qknr::kAdaMaxGroups) return fail(QKNR_ERR_SHAPE, "more than %d row groups", qknr::kAdaMaxGroups);
   const int cpl = (n_chunks + 32 * gw - 1) / (32 * gw);
-  if (cpl > 3)
-    return fail(QKNR_ERR_UNSUPPORTED, "hidden %d needs more than 3 chunks per lane with %d warps per row", C, gw);
+  // ring depth per group: up to 4, at least 2
   int stages = a->stages;
   if (stages == 0) {
-    long long want = (96 * 1024) / (static_cast<long long>(kp.stage_bytes) * n_groups);
-    if (want < 2) want = 2;
-    if (want > 8) want = 8;
     long long cap = fit / n_groups;
     if (cap > qknr::kAdaMaxStages / n_groups) cap = qknr::kAdaMaxStages / n_groups;
-    stages = static_cast<int>(cap < want ? cap : want);
+    stages = static_cast<int>(cap < 4 ? cap : 4);
     const long long rows_per_group = (rows_per_cta + n_groups - 1) / n_groups;
     if (rows_per_group >= 2 && stages > rows_per_group) stages = static_cast<int>(rows_per_group);
     if (stages < 2) stages = 2;
@@ -151,7 +149,8 @@ qknr_status plan(const qknr_adaln_args* a, AdaPlan* pl, bool size_device) {
   if (smem > di.smem_optin)
     return fail(QKNR_ERR_UNSUPPORTED, "%d groups x %d stages of %u-byte rows need %lld B of shared memory (max %d)",
                 n_groups, stages, kp.stage_bytes, smem, di.smem_optin);
-  pl->fn = qknr::adaln_kernel_for(a->dtype == QKNR_BF16 ? 0 : 1, a->mod_dtype == QKNR_FP32, cpl);
+  const int unroll = cpl >= 4 ? 4 : (cpl >= 2 ? 2 : 1);
+  pl->fn = qknr::adaln_kernel_for(a->dtype == QKNR_BF16 ? 0 : 1, a->mod_dtype == QKNR_FP32, unroll);
   if (!pl->fn) return fail(QKNR_ERR_UNSUPPORTED, "no kernel instance for this combination");
   st = qknr_host::configure_kernel(pl->fn, dev, di, &pl->regs);
   if (st != QKNR_OK) return st;

@@ -8,18 +8,23 @@
 //
 // Same streaming structure as the QK kernel: a persistent CTA per SM, one
 // producer lane bulk-copying token rows into per-group shared-memory rings,
-// consumer warps in groups that each take whole rows.  A group of GW warps
-// covers one row: lane l of warp w holds the 16-byte chunks
-// k = (w*32 + l) + i*32*GW, i < CPL, in fp32 registers.  Mean and variance
-// are exact two-pass sums (mean first, then centred squares from the
-// registers), each reduced by shuffles inside a warp and through shared
-// memory plus a named barrier across the group.  A warp hands the stage
-// back as soon as its chunks are in registers.
+// consumer warps in groups that each take whole rows, so several rows are
+// in flight.  Lane l of warp w of a group of GW warps handles the 16-byte
+// chunks k = (w*32 + l) + i*32*GW of the staged row.
+//
+// Statistics in one pass over the staged row, around a shift K = x[0] of
+// the row: S1 = sum (x - K), S2 = sum (x - K)^2, so mean = K + S1/C and
+// var = S2/C - (S1/C)^2.  Shifting by an element of the row keeps the
+// subtraction well conditioned (it cancels only the spread of the row
+// around one of its own values).  The sums are reduced by shuffles inside
+// a warp and through shared memory and one named barrier across the group;
+// a second pass over the staged row writes the output, and the stage goes
+// back to the producer after that pass.
 //
 // Every mbarrier wait is bounded.  The decision to continue is collective:
-// each warp posts whether its wait succeeded with its first partial sum,
-// and the group leaves the row loop together when any warp failed, so no
-// warp can be left waiting at a named barrier for one that gave up.
+// each warp posts whether its wait succeeded with its partial sums, and
+// the group leaves the row loop together when any warp failed, so no warp
+// can be left waiting at a named barrier for one that gave up.
 #pragma once
 
 #include "qknr_ptx.cuh"
@@ -33,8 +38,10 @@ constexpr int kAdaMaxGroups = 8;                  // named barriers 1..8
 // dynamic shared memory map (bytes)
 constexpr int kAdaOffBarriers = 0;                // full[32], empty[32]
 constexpr int kAdaOffAbort = 512;
-constexpr int kAdaOffPartial = 1024;              // per group: [3][kAdaMaxWarps] floats (two sums, ok flags)
-constexpr int kAdaOffStage0 = 1024 + kAdaMaxGroups * 3 * kAdaMaxWarps * 4 + 512;   // 3072
+// per group: two row-parity buffers of [3][kAdaMaxWarps] floats (two sums, ok flags)
+constexpr int kAdaOffPartial = 1024;
+constexpr int kAdaPartialFloats = 2 * 3 * kAdaMaxWarps;
+constexpr int kAdaOffStage0 = kAdaOffPartial + kAdaMaxGroups * kAdaPartialFloats * 4;   // 4096
 constexpr int kAdaStageAlign = 128;
 
 struct AdaLNParams {
@@ -85,7 +92,7 @@ __device__ __forceinline__ void load_mod8<__half>(const char* row, int k, float2
   Elem<__half>::unpack(__ldg(reinterpret_cast<const uint4*>(row) + k), m);
 }
 
-template <typename T, typename MT, int CPL>
+template <typename T, typename MT, int UNROLL>
 __global__ void __launch_bounds__(kAdaMaxThreads, 1) adaln_kernel(const __grid_constant__ AdaLNParams p) {
   extern __shared__ __align__(128) unsigned char smem[];
   const int warp = threadIdx.x >> 5;
@@ -162,7 +169,7 @@ __global__ void __launch_bounds__(kAdaMaxThreads, 1) adaln_kernel(const __grid_c
   const int grp = warp / GW, gw = warp % GW;
   const int gthreads = GW * 32;
   const int bar_id = 1 + grp;
-  float* part = reinterpret_cast<float*>(smem + kAdaOffPartial) + grp * 3 * kAdaMaxWarps;   // [3][GW]
+  float* part_base = reinterpret_cast<float*>(smem + kAdaOffPartial) + grp * kAdaPartialFloats;
   const int n_chunks = p.hidden / 8;
   const int lane_g = gw * 32 + lane;
   const float eps = p.eps, inv_c = p.inv_c;
@@ -170,6 +177,7 @@ __global__ void __launch_bounds__(kAdaMaxThreads, 1) adaln_kernel(const __grid_c
 
   int s = 0;
   uint32_t ph = 0;
+  int parity = 0;                                 // partial-sum buffer of this row
   const long long step = static_cast<long long>(n_groups) * gridDim.x;
   long long row = blockIdx.x + static_cast<long long>(grp) * gridDim.x;
   // sample of the current row, kept as a running quotient and remainder
@@ -179,89 +187,83 @@ __global__ void __launch_bounds__(kAdaMaxThreads, 1) adaln_kernel(const __grid_c
   for (; row < p.tokens; row += step) {
     const uint32_t full = full0 + 8 * (ring0 + s);
     const bool ok = mbar_try_wait(full, ph) || bounded_wait(full, ph, limit, abort_flag, p.status);
+    const unsigned char* st = smem + kAdaOffStage0 + (ring0 + s) * p.stage_bytes;
 
-    float2 X[CPL][4];                             // this lane's chunks of the row
-    float s1 = 0.0f;
+    float2 a1 = make_float2(0.0f, 0.0f), a2 = make_float2(0.0f, 0.0f);
     if (ok) {
-      const unsigned char* st = smem + kAdaOffStage0 + (ring0 + s) * p.stage_bytes;
+      // one pass: sums of (x - K) and (x - K)^2, K = the row's first element
+      float2 first[4];
+      Elem<T>::unpack(*reinterpret_cast<const uint4*>(st), first);
+      const float2 nk = make_float2(-first[0].x, -first[0].x);
+#pragma unroll UNROLL
+      for (int k = lane_g; k < n_chunks; k += gthreads) {
+        float2 X[4];
+        Elem<T>::unpack(*reinterpret_cast<const uint4*>(st + k * 16), X);
 #pragma unroll
-      for (int i = 0; i < CPL; ++i) {
-        const int k = lane_g + i * gthreads;
-        if (k < n_chunks) {
-          Elem<T>::unpack(*reinterpret_cast<const uint4*>(st + k * 16), X[i]);
-        } else {
-#pragma unroll
-          for (int j = 0; j < 4; ++j) X[i][j] = make_float2(0.0f, 0.0f);
+        for (int j = 0; j < 4; ++j) {
+          const float2 d = __fadd2_rn(X[j], nk);
+          a1 = __fadd2_rn(a1, d);
+          a2 = __ffma2_rn(d, d, a2);
         }
       }
-      // the row is in registers: hand the stage back
-      __syncwarp();
-      if (lane == 0) mbar_arrive(empty0 + 8 * (ring0 + s));
-      float2 a = make_float2(0.0f, 0.0f);
-#pragma unroll
-      for (int i = 0; i < CPL; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) a = __fadd2_rn(a, X[i][j]);
-      s1 = __fadd_rn(a.x, a.y);
-#pragma unroll
-      for (int off = 16; off >= 1; off >>= 1) s1 = __fadd_rn(s1, __shfl_xor_sync(0xffffffffu, s1, off));
     }
-    // pass 1: post the warp's sum and whether its wait succeeded
+    float s1 = __fadd_rn(a1.x, a1.y), s2 = __fadd_rn(a2.x, a2.y);
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+      s1 = __fadd_rn(s1, __shfl_xor_sync(0xffffffffu, s1, off));
+      s2 = __fadd_rn(s2, __shfl_xor_sync(0xffffffffu, s2, off));
+    }
+    // post the warp's sums and whether its wait succeeded.  Rows alternate
+    // between two buffers: a warp can start the next row's posting while a
+    // slower one still reads this row's sums, but cannot get two rows ahead
+    // without passing the next row's barrier.
+    float* part = part_base + parity * 3 * kAdaMaxWarps;
+    parity ^= 1;
     if (lane == 0) {
       part[gw] = s1;
+      part[kAdaMaxWarps + gw] = s2;
       part[2 * kAdaMaxWarps + gw] = ok ? 1.0f : 0.0f;
     }
+    // this row's sample's modulation rows (the same for every row of the
+    // sample: L1/L2 hits); their loads overlap the barrier
+    const char* srow = p.scale + batch * p.mod_stride;
+    const char* hrow = p.shift + batch * p.mod_stride;
     named_barrier(bar_id, gthreads);
     bool all_ok = true;
-    float sum = 0.0f;
+    float t1 = 0.0f, t2 = 0.0f;
     for (int w = 0; w < GW; ++w) {
-      sum = __fadd_rn(sum, part[w]);
+      t1 = __fadd_rn(t1, part[w]);
+      t2 = __fadd_rn(t2, part[kAdaMaxWarps + w]);
       all_ok = all_ok && part[2 * kAdaMaxWarps + w] != 0.0f;
     }
     if (!all_ok) break;                           // every warp of the group leaves together
-    const float mu = __fmul_rn(sum, inv_c);
-    const float2 nmu = make_float2(-mu, -mu);
-    // pass 2: centred squares from the registers
-    float2 q = make_float2(0.0f, 0.0f);
-#pragma unroll
-    for (int i = 0; i < CPL; ++i) {
-      if (lane_g + i * gthreads < n_chunks) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float2 d = __fadd2_rn(X[i][j], nmu);
-          q = __ffma2_rn(d, d, q);
-        }
-      }
-    }
-    float s2 = __fadd_rn(q.x, q.y);
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) s2 = __fadd_rn(s2, __shfl_xor_sync(0xffffffffu, s2, off));
-    if (lane == 0) part[kAdaMaxWarps + gw] = s2;
-    named_barrier(bar_id, gthreads);
-    float ssq = 0.0f;
-    for (int w = 0; w < GW; ++w) ssq = __fadd_rn(ssq, part[kAdaMaxWarps + w]);
-    const float r = rsqrtf(__fmaf_rn(ssq, inv_c, eps));
+    const float m1 = __fmul_rn(t1, inv_c);        // mean of (x - K)
+    float var = __fmaf_rn(-m1, m1, __fmul_rn(t2, inv_c));
+    var = var > 0.0f ? var : 0.0f;
+    const float r = rsqrtf(__fadd_rn(var, eps));
     const float2 R = make_float2(r, r);
-    // modulation rows of this row's sample: the same two rows for every row
-    // of the sample, so these reads hit L1/L2
-    const char* srow = p.scale + batch * p.mod_stride;
-    const char* hrow = p.shift + batch * p.mod_stride;
+    float2 first[4];
+    Elem<T>::unpack(*reinterpret_cast<const uint4*>(st), first);
+    const float mu = __fadd_rn(first[0].x, m1);
+    const float2 nmu = make_float2(-mu, -mu);
+    // second pass over the staged row: normalise, modulate, store
     char* orow = p.out + row * p.out_stride;
+#pragma unroll UNROLL
+    for (int k = lane_g; k < n_chunks; k += gthreads) {
+      float2 X[4], sc[4], sh[4], o[4];
+      Elem<T>::unpack(*reinterpret_cast<const uint4*>(st + k * 16), X);
+      load_mod8<MT>(srow, k, sc);
+      load_mod8<MT>(hrow, k, sh);
 #pragma unroll
-    for (int i = 0; i < CPL; ++i) {
-      const int k = lane_g + i * gthreads;
-      if (k < n_chunks) {
-        float2 sc[4], sh[4], o[4];
-        load_mod8<MT>(srow, k, sc);
-        load_mod8<MT>(hrow, k, sh);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const float2 sc1 = __fadd2_rn(sc[j], make_float2(1.0f, 1.0f));
-          o[j] = __ffma2_rn(__fmul2_rn(__fadd2_rn(X[i][j], nmu), R), sc1, sh[j]);
-        }
-        store16(orow + k * 16, Elem<T>::pack(o));
+      for (int j = 0; j < 4; ++j) {
+        const float2 sc1 = __fadd2_rn(sc[j], make_float2(1.0f, 1.0f));
+        o[j] = __ffma2_rn(__fmul2_rn(__fadd2_rn(X[j], nmu), R), sc1, sh[j]);
       }
+      store16(orow + k * 16, Elem<T>::pack(o));
     }
+    // the row has been read for the last time: hand the stage back
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty0 + 8 * (ring0 + s));
     if (++s == S) {
       s = 0;
       ph ^= 1u;

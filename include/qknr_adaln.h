@@ -7,11 +7,13 @@
  * layer normalisation: for every token row t of a hidden state x [T, C]
  * belonging to sample b = t / rows_per_batch,
  *
- *     mean = sum_c x[c] / C,   var = sum_c (x[c] - mean)^2 / C      (fp32)
+ *     mean = sum_c x[c] / C,   var = sum_c (x[c] - mean)^2 / C
  *     out[c] = (x[c] - mean) * rsqrt(var + eps) * (1 + scale[b, c]) + shift[b, c]
  *
- * rounded once, to nearest even, into the activation dtype.  Mean and
- * variance are exact two-pass fp32 sums over the row held in registers.
+ * rounded once, to nearest even, into the activation dtype.  The kernel
+ * takes mean and variance in fp32 from one pass of sums around a shift K =
+ * x[0] of the row: S1 = sum (x - K), S2 = sum (x - K)^2, mean = K + S1/C,
+ * var = S2/C - (S1/C)^2.
  *
  * Ownership and errors follow qknr.h: the caller owns every buffer, the
  * library allocates nothing and never synchronises; argument errors return
@@ -34,7 +36,7 @@ typedef struct qknr_adaln_args {
   void *out;                  /* device [T, C]; NULL or x (same stride) = in place */
   int64_t x_stride, out_stride;   /* elements per row; 0 = C (out: x's) */
   int64_t tokens;             /* T; 0 is a no-op */
-  int32_t hidden;             /* C: a multiple of 8, at most 12288 */
+  int32_t hidden;             /* C: a multiple of 8, at most 32768 */
   int64_t rows_per_batch;     /* rows sharing one modulation row; 0 = tokens */
   const void *scale, *shift;  /* device [B, C], B = ceil(T / rows_per_batch) */
   int32_t mod_dtype;          /* QKNR_FP32, or the activation dtype */

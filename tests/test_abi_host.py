@@ -195,7 +195,7 @@ def test_adaln_args_init_defaults(lib):
     (lambda a: setattr(a, "dtype", 2), 4),
     (lambda a: setattr(a, "mod_dtype", 1), 4),            # fp16 modulation for bf16 activations
     (lambda a: setattr(a, "hidden", 100), 4),             # not a multiple of 8
-    (lambda a: setattr(a, "hidden", 16384), 4),
+    (lambda a: setattr(a, "hidden", 32776), 4),
     (lambda a: setattr(a, "tokens", -1), 2),
     (lambda a: setattr(a, "rows_per_batch", -5), 2),
     (lambda a: setattr(a, "eps", -0.5), 2),
