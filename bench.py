@@ -257,6 +257,9 @@ def run_reference(args, w):
 
 
 def workload_config(w, world, tokens=None):
+    if isinstance(w, I.GroupNormWorkload):
+        return {"workload": w.name, "shape_nchw": [w.n, w.c, w.h, w.w], "groups": w.groups, "in_place": True,
+                "l2": "inputs larger than L2 (no flush)", "parallelism": f"replicas x{world}"}
     if isinstance(w, I.AdaLNWorkload):
         return {"workload": w.name, "tokens": w.tokens if tokens is None else tokens, "hidden": w.hidden,
                 "rows_per_batch": w.seq, "mod_dtype": w.mod_dtype, "in_place": True,
@@ -425,6 +428,55 @@ class AdaLNRunner:
         self.pinned_out["x"].copy_(self.d["x"], non_blocking=True)
 
 
+class GroupNormRunner:
+    """Device buffers and arguments of a VAE group-norm + SiLU workload.  One
+    step is one call: two launches (statistics, apply) per L2-sized batch of
+    groups; the caller-owned workspace is allocated once here."""
+
+    def __init__(self, w, dev, tune, status, tokens=None):
+        import torch
+
+        from diffusion_transformer_qk_gb300 import qknr as Q
+
+        self.Q, self.w, self.dev, self.tune = Q, w, dev, tune
+        self.tokens = w.elements
+        self.inp = I.make_gn_inputs(w)
+        act = torch.bfloat16 if w.dtype == "bf16" else torch.float16
+        self.host = {"x": torch.from_numpy(self.inp["x"].view(np.int16)).view(act),
+                     "gamma": torch.from_numpy(self.inp["gamma"]), "beta": torch.from_numpy(self.inp["beta"])}
+        self.d = {k: v.to(dev) for k, v in self.host.items()}
+        a = Q.gn_args(self.d["x"], w.groups, self.d["gamma"], self.d["beta"], eps=w.eps)
+        self.workspace = torch.empty(Q.gn_workspace_bytes(a), dtype=torch.uint8, device=dev)
+        a.workspace, a.workspace_bytes = self.workspace.data_ptr(), self.workspace.numel()
+        self.args = [a]
+        self.launch = Q.gn_launch
+        self.bytes_per_launch = I.gn_algorithmic_bytes(w)
+        self.outputs = ["x"]
+        self.pipe = None
+        span = w.elements // (w.n * w.groups) * 2
+        batch = max(1, (48 << 20) // span)
+        self.launches_per_call = 2 * (-(-(w.n * w.groups) // batch))
+        self.info = {"grid": 0, "block": 256, "dyn_smem": 0, "stages": 0, "ctas_per_sm": 0, "consumer_warps": 0,
+                     "stage_bytes": 0, "registers": 0, "num_sms": 0,
+                     "kernel": "gn_stats_kernel + gn_apply_kernel (%d launches)" % self.launches_per_call}
+
+    def step(self, stream):
+        for a in self.args:
+            self.launch(a, stream)
+
+    def e2e_buffers(self, chunk_rows):
+        self.pinned = {k: v.pin_memory() for k, v in self.host.items()}
+        self.pinned_out = {"x": torch_empty_pinned_like(self.host["x"])}
+        h2d = sum(t.numel() * t.element_size() for t in self.pinned.values())
+        return h2d, self.pinned_out["x"].numel() * self.pinned_out["x"].element_size()
+
+    def e2e_step(self, stream):
+        for k, t in self.pinned.items():
+            self.d[k].copy_(t, non_blocking=True)
+        self.step(stream)
+        self.pinned_out["x"].copy_(self.d["x"], non_blocking=True)
+
+
 def torch_empty_pinned_like(t):
     import torch
 
@@ -445,7 +497,8 @@ def run_ours(args, w):
 
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     tune = dict(ctas_per_sm=args.ctas_per_sm, stages=args.stages, consumer_warps=args.consumer_warps)
-    run = (AdaLNRunner if isinstance(w, I.AdaLNWorkload) else Runner)(w, dev, tune, status, args.tokens)
+    runner = {I.AdaLNWorkload: AdaLNRunner, I.GroupNormWorkload: GroupNormRunner}.get(type(w), Runner)
+    run = runner(w, dev, tune, status, args.tokens)
     stream = torch.cuda.current_stream(dev)
     L = len(run.args)
 
@@ -555,14 +608,14 @@ def run_ours(args, w):
                      "traffic": traffic, "peak_source": f"{peak_kind} copy bandwidth (hbm_gbs)",
                      "algorithmic_bytes_per_launch": run.bytes_per_launch, "kernel_us": max_kernel_ms * 1e3,
                      "launches_per_step": L, "kernel": info["kernel"]},
-        "gpu_launches": K * L,
+        "gpu_launches": K * L * getattr(run, "launches_per_call", 1),
         "clocks": clocks,
         "launch": {k: info[k] for k in ("grid", "block", "dyn_smem", "stages", "ctas_per_sm", "consumer_warps",
                                         "stage_bytes", "registers", "num_sms")},
     }
     if e2e:
         line["e2e"] = e2e
-    if world == 1 and not args.no_cpu_baseline and not isinstance(w, I.AdaLNWorkload):
+    if world == 1 and not args.no_cpu_baseline and isinstance(w, I.Workload):
         us, n, dt = time_oracle_workload(w, run.inp, args.cpu_seconds, run.tokens)
         line["cpu_baseline"] = {"value": us, "unit": UNIT, "cores": 1, "kind": "oracle",
                                 "sample": f"first {n} of {w.tokens} token rows, {dt:.1f} s, fp64 numpy, "
@@ -577,7 +630,8 @@ def main(argv=None):
     p.add_argument("--steps", type=int, default=5000)
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(I.WORKLOADS) + sorted(I.ADALN_WORKLOADS))
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                   choices=sorted(I.WORKLOADS) + sorted(I.ADALN_WORKLOADS) + sorted(I.GN_WORKLOADS))
     p.add_argument("--tokens", type=int, default=None,
                    help="run the first N token rows of the workload (small profiling cases)")
     p.add_argument("--ctas-per-sm", type=int, default=0)
@@ -592,9 +646,9 @@ def main(argv=None):
     args = p.parse_args(argv)
     if args.warmup < 3:
         p.error("--warmup must be >= 3")
-    w = I.WORKLOADS.get(args.workload) or I.ADALN_WORKLOADS[args.workload]
+    w = I.WORKLOADS.get(args.workload) or I.ADALN_WORKLOADS.get(args.workload) or I.GN_WORKLOADS[args.workload]
     if args.impl == "reference":
-        if isinstance(w, I.AdaLNWorkload):
+        if not isinstance(w, I.Workload):
             p.error("--impl reference times the QK-norm + RoPE oracle; pick a QK workload")
         return run_reference(args, w)
     return run_ours(args, w)

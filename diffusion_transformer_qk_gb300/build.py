@@ -34,6 +34,7 @@ SOURCES = [
     "qknr_inst_fp16_bf16.cu",
     "adaln_api.cu",
     "adaln_inst.cu",
+    "gn_api.cu",
 ]
 
 

@@ -340,3 +340,58 @@ def adaln_algorithmic_bytes(w: AdaLNWorkload, tokens: Optional[int] = None) -> i
     B = max(1, -(-T // w.seq))
     mes = 4 if w.mod_dtype == "fp32" else 2
     return 2 * T * w.hidden * 2 + 2 * B * w.hidden * mes
+
+
+# --------------------------------------------------------------------------
+# VAE group-norm + SiLU workloads ("fused qknorm rope Flux 2.0", section
+# "Not in this PR — follow-ups": group_norm_silu for the VAE).  Decoder
+# feature maps of a 1024 x 1024 image: 512 channels at 128^2 and 256^2,
+# 256 at 512^2, 128 at 1024^2; 32 groups.
+
+@dataclass(frozen=True)
+class GroupNormWorkload:
+    name: str
+    n: int
+    c: int
+    h: int
+    w: int
+    groups: int = 32
+    dtype: str = "bf16"
+    scale: float = 1.0             # x = scale * N(0,1) + offset
+    offset: float = 0.0
+    eps: float = 1e-6
+    seed: int = 0
+
+    @property
+    def elements(self) -> int:
+        return self.n * self.c * self.h * self.w
+
+    def with_(self, **kw) -> "GroupNormWorkload":
+        return replace(self, **kw)
+
+
+GN_WORKLOADS: Dict[str, GroupNormWorkload] = {
+    "gn_vae_1x512x128x128": GroupNormWorkload("gn_vae_1x512x128x128", 1, 512, 128, 128),
+    "gn_vae_1x512x256x256": GroupNormWorkload("gn_vae_1x512x256x256", 1, 512, 256, 256),
+    "gn_vae_1x256x512x512": GroupNormWorkload("gn_vae_1x256x512x512", 1, 256, 512, 512),
+    "gn_vae_1x128x1024x1024": GroupNormWorkload("gn_vae_1x128x1024x1024", 1, 128, 1024, 1024),
+}
+
+
+def make_gn_inputs(w: GroupNormWorkload) -> Dict[str, np.ndarray]:
+    """Seeded instance: draw order x, gamma, beta.  x is [N, C, H, W] uint16
+    bits; gamma = 1 + 0.1 N(0,1), beta = 0.1 N(0,1), fp32 [C]."""
+    g = np.random.Generator(np.random.PCG64(w.seed))
+    x = _normal(g, (w.n, w.c, w.h, w.w), w.scale)
+    if w.offset:
+        x += np.float32(w.offset)
+    return {
+        "x": to_storage_bits(x, w.dtype),
+        "gamma": (1.0 + 0.1 * g.standard_normal(w.c)).astype(np.float32),
+        "beta": (0.1 * g.standard_normal(w.c)).astype(np.float32),
+    }
+
+
+def gn_algorithmic_bytes(w: GroupNormWorkload) -> int:
+    """x read once and written once, plus gamma and beta."""
+    return 2 * w.elements * 2 + 2 * w.c * 4

@@ -37,6 +37,7 @@ EXPORTS = (
     "qknr_args_init", "qknr_forward", "qknr_query", "qknr_status_string",
     "qknr_last_error", "qknr_abi_version", "qknr_sizeof_args", "qknr_sizeof_launch_info",
     "qknr_adaln_args_init", "qknr_adaln_forward", "qknr_adaln_query", "qknr_adaln_sizeof_args",
+    "qknr_gn_args_init", "qknr_gn_workspace_bytes", "qknr_gn_silu_forward", "qknr_gn_sizeof_args",
 )
 
 
@@ -93,6 +94,19 @@ class QknrAdaLNArgs(ctypes.Structure):
     ]
 
 
+class QknrGnArgs(ctypes.Structure):
+    """Mirror of ``qknr_gn_args``."""
+
+    _fields_ = [
+        ("abi_version", c_uint32), ("dtype", c_int32),
+        ("x", c_void_p), ("out", c_void_p),
+        ("n", c_int32), ("c", c_int32), ("h", c_int32), ("w", c_int32), ("groups", c_int32),
+        ("gamma", c_void_p), ("beta", c_void_p), ("eps", c_float),
+        ("workspace", c_void_p), ("workspace_bytes", c_size_t),
+        ("piece_elems", c_int32), ("l2_batch_bytes", c_int64),
+    ]
+
+
 class QknrError(RuntimeError):
     def __init__(self, status: int, message: str):
         super().__init__(f"{STATUS.get(status, status)}: {message}")
@@ -139,11 +153,19 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         lib.qknr_adaln_query.argtypes = [ctypes.POINTER(QknrAdaLNArgs), ctypes.POINTER(QknrLaunchInfo)]
         lib.qknr_adaln_query.restype = c_int32
         lib.qknr_adaln_sizeof_args.restype = c_size_t
+        lib.qknr_gn_args_init.argtypes = [ctypes.POINTER(QknrGnArgs)]
+        lib.qknr_gn_args_init.restype = None
+        lib.qknr_gn_workspace_bytes.argtypes = [ctypes.POINTER(QknrGnArgs), ctypes.POINTER(c_size_t)]
+        lib.qknr_gn_workspace_bytes.restype = c_int32
+        lib.qknr_gn_silu_forward.argtypes = [ctypes.POINTER(QknrGnArgs), c_void_p]
+        lib.qknr_gn_silu_forward.restype = c_int32
+        lib.qknr_gn_sizeof_args.restype = c_size_t
         if lib.qknr_abi_version() != ABI_VERSION:
             raise RuntimeError("libqknr.so ABI version mismatch")
         if lib.qknr_sizeof_args() != ctypes.sizeof(QknrArgs) or \
                 lib.qknr_sizeof_launch_info() != ctypes.sizeof(QknrLaunchInfo) or \
-                lib.qknr_adaln_sizeof_args() != ctypes.sizeof(QknrAdaLNArgs):
+                lib.qknr_adaln_sizeof_args() != ctypes.sizeof(QknrAdaLNArgs) or \
+                lib.qknr_gn_sizeof_args() != ctypes.sizeof(QknrGnArgs):
             raise RuntimeError("libqknr.so struct layout differs from the binding")
         if path is None:
             _lib = lib
@@ -531,4 +553,62 @@ def adaln_modulate(x, scale, shift, *, rows_per_batch=None, out=None, stream=Non
     if status and "dev_status" not in kw:
         kw["dev_status"] = status_buffer(x.device)
     adaln_launch(adaln_args(x, scale, shift, rows_per_batch=rows_per_batch, out=out, **kw), stream)
+    return x if out is None else out
+
+
+# ---------------------------------------------------------------------------
+# group norm + SiLU (include/qknr_gn.h)
+
+def gn_args(x, groups, gamma, beta, *, out=None, eps=1e-6, workspace=None, piece_elems=0,
+            l2_batch_bytes=0) -> QknrGnArgs:
+    """Arguments for ``silu(group_norm(x))`` on an NCHW tensor ``x``."""
+    if x.dim() != 4 or not x.is_contiguous() or not x.is_cuda or x.dtype not in _ACT:
+        raise ValueError("x must be a contiguous 4-D (NCHW) bfloat16/float16 CUDA tensor")
+    a = QknrGnArgs()
+    load().qknr_gn_args_init(ctypes.byref(a))
+    a.dtype = _ACT[x.dtype]
+    a.x = x.data_ptr()
+    if out is not None:
+        if out.shape != x.shape or out.dtype != x.dtype or not out.is_contiguous():
+            raise ValueError("out must be contiguous and match x")
+        a.out = out.data_ptr()
+    a.n, a.c, a.h, a.w = x.shape
+    a.groups = groups
+    for t, name in ((gamma, "gamma"), (beta, "beta")):
+        if t.dtype != torch.float32 or not t.is_cuda or t.numel() != x.shape[1] or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous float32 CUDA tensor of C values")
+    a.gamma, a.beta = gamma.data_ptr(), beta.data_ptr()
+    a.eps = eps
+    a.piece_elems, a.l2_batch_bytes = piece_elems, l2_batch_bytes
+    if workspace is not None:
+        a.workspace, a.workspace_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    return a
+
+
+def gn_workspace_bytes(a: QknrGnArgs) -> int:
+    lib = load()
+    n = c_size_t(0)
+    st = lib.qknr_gn_workspace_bytes(ctypes.byref(a), ctypes.byref(n))
+    if st != OK:
+        raise QknrError(st, lib.qknr_last_error().decode())
+    return n.value
+
+
+def gn_launch(a: QknrGnArgs, stream: Optional[torch.cuda.Stream] = None) -> None:
+    lib = load()
+    s = torch.cuda.current_stream() if stream is None else stream
+    st = lib.qknr_gn_silu_forward(ctypes.byref(a), c_void_p(s.cuda_stream))
+    if st != OK:
+        raise QknrError(st, lib.qknr_last_error().decode())
+
+
+def group_norm_silu(x, groups, gamma, beta, *, out=None, workspace=None, stream=None, **kw):
+    """silu(group_norm(x)) on NCHW ``x``; in place unless ``out`` is given.
+    ``workspace`` (a CUDA tensor of at least gn_workspace_bytes) is created
+    by this binding when not given."""
+    a = gn_args(x, groups, gamma, beta, out=out, **kw)
+    if workspace is None:
+        workspace = torch.empty(gn_workspace_bytes(a), dtype=torch.uint8, device=x.device)
+    a.workspace, a.workspace_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    gn_launch(a, stream)
     return x if out is None else out

@@ -39,3 +39,27 @@ def group_norm_silu(x: np.ndarray, dtype: str, groups: int, gamma: np.ndarray, b
     y = (d / np.sqrt(var + e)).reshape(N, C, H, W)
     y = y * decode(gamma, "fp32")[None, :, None, None] + decode(beta, "fp32")[None, :, None, None]
     return y / (1.0 + np.exp(-y))
+
+
+def group_norm_silu_at(x: np.ndarray, dtype: str, groups: int, gamma: np.ndarray, beta: np.ndarray, eps: float,
+                       index: tuple) -> np.ndarray:
+    """The same values as ``group_norm_silu`` at the elements ``x[index]``
+    (a tuple of four integer arrays n, c, h, w), computing the statistics of
+    only the groups those elements belong to."""
+    N, C, H, W = x.shape
+    n, c, h, w = (np.asarray(i) for i in index)
+    gsize = C // groups
+    e = float(np.float32(eps))
+    g = c // gsize
+    stats = {}
+    for key in set(zip(n.tolist(), g.tolist())):
+        ni, gi = key
+        xd = decode(x[ni, gi * gsize:(gi + 1) * gsize], dtype)
+        mu = xd.mean()
+        var = ((xd - mu) ** 2).mean()
+        stats[key] = (mu, var)
+    mu = np.array([stats[(a, b)][0] for a, b in zip(n.tolist(), g.tolist())])
+    var = np.array([stats[(a, b)][1] for a, b in zip(n.tolist(), g.tolist())])
+    xv = decode(x[n, c, h, w], dtype)
+    y = (xv - mu) / np.sqrt(var + e) * decode(gamma, "fp32")[c] + decode(beta, "fp32")[c]
+    return y / (1.0 + np.exp(-y))

@@ -7,8 +7,14 @@ import os
 import re
 
 import pytest
+import torch
 
 from diffusion_transformer_qk_gb300 import qknr as Q
+
+# These tests hand the library fake device addresses and rely on it
+# rejecting every call before a launch; they never run where a GPU is
+# visible, so a call that validation let through cannot touch a device.
+pytestmark = pytest.mark.skipif(torch.cuda.is_available(), reason="host-only tests with fake device addresses")
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 INCLUDE = os.path.join(ROOT, "include")
@@ -38,6 +44,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_struct_layouts_match(lib):
+    assert lib.qknr_gn_sizeof_args() == ctypes.sizeof(Q.QknrGnArgs)
     assert lib.qknr_adaln_sizeof_args() == ctypes.sizeof(Q.QknrAdaLNArgs)
     assert lib.qknr_sizeof_args() == ctypes.sizeof(Q.QknrArgs)
     assert lib.qknr_sizeof_launch_info() == ctypes.sizeof(Q.QknrLaunchInfo)
@@ -222,3 +229,52 @@ def test_adaln_zero_tokens_is_ok_without_cuda(lib):
     a = valid_adaln(T=0)
     a.x = a.scale = a.shift = None
     assert adaln_call(lib, a)[0] == 0
+
+
+# ---------------------------------------------------------------------------
+# group norm + SiLU host validation
+
+def valid_gn():
+    a = Q.QknrGnArgs()
+    Q.load().qknr_gn_args_init(ctypes.byref(a))
+    a.x = FAKE
+    a.n, a.c, a.h, a.w, a.groups = 1, 64, 16, 16, 32
+    a.gamma, a.beta = FAKE + (1 << 30), FAKE + (1 << 30) + 4096
+    a.workspace, a.workspace_bytes = FAKE + (2 << 30), 1 << 20
+    return a
+
+
+def test_gn_workspace_bytes(lib):
+    a = valid_gn()
+    n = ctypes.c_size_t(0)
+    assert lib.qknr_gn_workspace_bytes(ctypes.byref(a), ctypes.byref(n)) == 0
+    # 32 spans of 2*16*16 = 512 elements: one piece each, plus the shift record
+    assert n.value == 32 * 2 * 16
+    a.piece_elems = 64
+    assert lib.qknr_gn_workspace_bytes(ctypes.byref(a), ctypes.byref(n)) == 0
+    assert n.value == 32 * (8 + 1) * 16
+
+
+@pytest.mark.parametrize("mutate,expect", [
+    (lambda a: setattr(a, "abi_version", 0), 8),
+    (lambda a: setattr(a, "dtype", 2), 4),
+    (lambda a: setattr(a, "groups", 5), 2),                 # does not divide 64
+    (lambda a: (setattr(a, "w", 3), setattr(a, "h", 3)), 4),  # H*W = 9, not a multiple of 8
+    (lambda a: setattr(a, "n", 0), 2),
+    (lambda a: setattr(a, "eps", -1.0), 2),
+    (lambda a: setattr(a, "piece_elems", 12), 2),
+    (lambda a: setattr(a, "l2_batch_bytes", -7), 2),
+    (lambda a: setattr(a, "x", None), 1),
+    (lambda a: setattr(a, "workspace", None), 1),
+    (lambda a: setattr(a, "workspace_bytes", 100), 2),
+    (lambda a: setattr(a, "x", FAKE + 8), 3),
+    (lambda a: setattr(a, "workspace", FAKE + (2 << 30) + 8), 3),
+    (lambda a: setattr(a, "gamma", FAKE + (1 << 30) + 2), 3),
+    (lambda a: setattr(a, "out", FAKE + 1024), 7),          # out inside x
+    (lambda a: setattr(a, "workspace", FAKE + 4096), 7),    # workspace inside x
+])
+def test_gn_validation_rejects(lib, mutate, expect):
+    a = valid_gn()
+    mutate(a)
+    st = lib.qknr_gn_silu_forward(ctypes.byref(a), None)
+    assert st == expect, (st, lib.qknr_last_error().decode())

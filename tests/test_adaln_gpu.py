@@ -109,7 +109,8 @@ def test_degenerate_rows():
 
 
 @pytest.mark.parametrize("tune", [dict(consumer_warps=16, group_warps=2), dict(consumer_warps=8, group_warps=2),
-                                  dict(consumer_warps=4, group_warps=2, stages=4), dict(ctas_per_sm=2),
+                                  dict(consumer_warps=4, group_warps=2, stages=4),
+                                  dict(consumer_warps=4, group_warps=2, ctas_per_sm=2),
                                   dict(consumer_warps=2, group_warps=2, stages=6)])
 def test_same_group_size_gives_the_same_bits(tune):
     # the fp32 sums' order is fixed by the warps per row (2 here by default),

@@ -68,3 +68,15 @@ def test_groups_are_independent():
     part = G.group_norm_silu(_bits(x2), "bf16", 3, gamma, beta, 1e-6)
     mask = np.ones_like(full, bool); mask[1, 2:4] = False
     np.testing.assert_array_equal(full[mask], part[mask])
+
+
+def test_sampled_values_equal_the_full_oracle():
+    g = np.random.Generator(np.random.PCG64(4))
+    N, C, H, W, groups = 2, 16, 6, 5, 4
+    x = _bits(g.standard_normal((N, C, H, W)))
+    gamma = (1 + 0.1 * g.standard_normal(C)).astype(np.float32)
+    beta = (0.1 * g.standard_normal(C)).astype(np.float32)
+    full = G.group_norm_silu(x, "bf16", groups, gamma, beta, 1e-6)
+    idx = tuple(g.integers(0, s, 40) for s in (N, C, H, W))
+    np.testing.assert_allclose(G.group_norm_silu_at(x, "bf16", groups, gamma, beta, 1e-6, idx), full[idx],
+                               rtol=1e-13, atol=1e-15)
