@@ -3,6 +3,7 @@
 #include <cuda_runtime.h>
 
 #include <cstring>
+#include <mutex>
 
 #include "../../include/qknr_gn.h"
 #include "gn_kernel.cuh"
@@ -149,3 +150,65 @@ qknr_status qknr_gn_silu_forward(const qknr_gn_args* args, qknr_stream_t stream)
 size_t qknr_gn_sizeof_args(void) { return sizeof(qknr_gn_args); }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// The same call for callers that may not allocate device memory.
+//
+// Some callers cannot hand the library a workspace: code that runs inside a
+// host framework's enqueue step with no allocator of its own, a plugin
+// whose workspace size had to be fixed before the shapes were known, or a
+// runtime that keeps a fixed device-memory budget and forbids cudaMalloc
+// (which also synchronises the device) on its execution path.  For them the
+// statistics go to this fixed array, which every device that loads the
+// library holds until the process exits.
+
+namespace {
+
+// Room for the per-piece sums of QKNR_GN_NOALLOC_SCRATCH_BYTES / 16
+// (sample, group, piece) records.
+static __device__ __align__(256) double g_gn_noalloc_scratch[QKNR_GN_NOALLOC_SCRATCH_BYTES / sizeof(double)];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_addr[kMaxDevices] = {};   // device address of the array, per device
+
+// Device address of the array on the current device, looked up once per
+// device (with that device current) and cached.
+qknr_status scratch_address(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return qknr_host::cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(QKNR_ERR_UNSUPPORTED, "device ordinal %d >= %d", dev, kMaxDevices);
+  std::lock_guard<std::mutex> lk(g_scratch_mu);
+  if (!g_scratch_addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_gn_noalloc_scratch);
+    if (e != cudaSuccess) return qknr_host::cuda_fail(e, "cudaGetSymbolAddress(group-norm scratch)");
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return QKNR_OK;
+}
+
+}  // namespace
+
+extern "C" qknr_status qknr_gn_silu_forward_noalloc(const qknr_gn_args* args, qknr_stream_t stream) {
+  if (!args) return fail(QKNR_ERR_NULL, "args is NULL");
+  qknr_gn_args a = *args;
+  a.workspace = nullptr;
+  a.workspace_bytes = 0;
+  size_t need = 0;
+  qknr_status st = qknr_gn_workspace_bytes(&a, &need);
+  if (st != QKNR_OK) return st;
+  if (need > QKNR_GN_NOALLOC_SCRATCH_BYTES)
+    return fail(QKNR_ERR_UNSUPPORTED,
+                "this shape needs %zu bytes of statistics scratch; the no-allocation entry point has %d "
+                "(use fewer pieces per group, or qknr_gn_silu_forward with a workspace)",
+                need, QKNR_GN_NOALLOC_SCRATCH_BYTES);
+  void* scratch = nullptr;
+  st = scratch_address(&scratch);
+  if (st != QKNR_OK) return st;
+  a.workspace = scratch;
+  a.workspace_bytes = QKNR_GN_NOALLOC_SCRATCH_BYTES;
+  return qknr_gn_silu_forward(&a, stream);
+}

@@ -38,7 +38,9 @@ EXPORTS = (
     "qknr_last_error", "qknr_abi_version", "qknr_sizeof_args", "qknr_sizeof_launch_info",
     "qknr_adaln_args_init", "qknr_adaln_forward", "qknr_adaln_query", "qknr_adaln_sizeof_args",
     "qknr_gn_args_init", "qknr_gn_workspace_bytes", "qknr_gn_silu_forward", "qknr_gn_sizeof_args",
+    "qknr_gn_silu_forward_noalloc",
 )
+GN_NOALLOC_SCRATCH_BYTES = 1 << 20
 
 
 class QknrArgs(ctypes.Structure):
@@ -160,6 +162,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         lib.qknr_gn_silu_forward.argtypes = [ctypes.POINTER(QknrGnArgs), c_void_p]
         lib.qknr_gn_silu_forward.restype = c_int32
         lib.qknr_gn_sizeof_args.restype = c_size_t
+        lib.qknr_gn_silu_forward_noalloc.argtypes = [ctypes.POINTER(QknrGnArgs), c_void_p]
+        lib.qknr_gn_silu_forward_noalloc.restype = c_int32
         if lib.qknr_abi_version() != ABI_VERSION:
             raise RuntimeError("libqknr.so ABI version mismatch")
         if lib.qknr_sizeof_args() != ctypes.sizeof(QknrArgs) or \
@@ -612,3 +616,15 @@ def group_norm_silu(x, groups, gamma, beta, *, out=None, workspace=None, stream=
     a.workspace, a.workspace_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
     gn_launch(a, stream)
     return x if out is None else out
+
+
+def gn_launch_noalloc(a: QknrGnArgs, stream: Optional[torch.cuda.Stream] = None) -> None:
+    """qknr_gn_silu_forward_noalloc: the group-norm + SiLU call for callers
+    that cannot allocate device memory; its statistics scratch is a fixed
+    array inside the library (GN_NOALLOC_SCRATCH_BYTES), shared by every
+    call on the device, and a.workspace is ignored."""
+    lib = load()
+    s = torch.cuda.current_stream() if stream is None else stream
+    st = lib.qknr_gn_silu_forward_noalloc(ctypes.byref(a), c_void_p(s.cuda_stream))
+    if st != OK:
+        raise QknrError(st, lib.qknr_last_error().decode())

@@ -63,6 +63,29 @@ qknr_status qknr_gn_silu_forward(const qknr_gn_args *args, qknr_stream_t stream)
 /* sizeof(qknr_gn_args) as compiled into the library. */
 size_t qknr_gn_sizeof_args(void);
 
+/*
+ * The same operation for callers that cannot allocate device memory — a
+ * plugin or runtime with no allocator on its execution path, a fixed
+ * device-memory budget, or a workspace size fixed before the shapes were
+ * known.  The pages have no counterpart of this entry point.
+ *
+ * It ignores args->workspace and args->workspace_bytes: the statistics go
+ * to a fixed array of QKNR_GN_NOALLOC_SCRATCH_BYTES inside the library,
+ * which every GPU that loads the library holds until the process exits.
+ * A shape whose qknr_gn_workspace_bytes() exceeds that size is rejected
+ * with QKNR_ERR_UNSUPPORTED before anything runs (larger pieces need
+ * fewer bytes).  It calls no allocator.
+ *
+ * The first call on a device looks up the array's device address (with
+ * that device current) and caches it; make that first call before any
+ * stream capture.  Every call on a device shares the one array and every
+ * call writes all the scratch it reads, so nothing needs clearing, but
+ * calls whose kernels overlap on the GPU (different streams, no ordering
+ * between them) race on it.
+ */
+#define QKNR_GN_NOALLOC_SCRATCH_BYTES (1 << 20)
+qknr_status qknr_gn_silu_forward_noalloc(const qknr_gn_args *args, qknr_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
