@@ -453,9 +453,7 @@ class GroupNormRunner:
         self.bytes_per_launch = I.gn_algorithmic_bytes(w)
         self.outputs = ["x"]
         self.pipe = None
-        span = w.elements // (w.n * w.groups) * 2
-        batch = max(1, (48 << 20) // span)
-        self.launches_per_call = 2 * (-(-(w.n * w.groups) // batch))
+        self.launches_per_call = 2                 # one statistics and one apply launch
         self.info = {"grid": 0, "block": 256, "dyn_smem": 0, "stages": 0, "ctas_per_sm": 0, "consumer_warps": 0,
                      "stage_bytes": 0, "registers": 0, "num_sms": 0,
                      "kernel": "gn_stats_kernel + gn_apply_kernel (%d launches)" % self.launches_per_call}

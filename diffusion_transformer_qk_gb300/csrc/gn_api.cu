@@ -16,8 +16,12 @@ using qknr_host::fail;
 using qknr_host::Span;
 using qknr_host::span_of;
 
-constexpr long long kDefaultPiece = 32768;
-constexpr long long kDefaultBatchBytes = 48ll << 20;
+// Defaults from sweeps on GB300 (VAE decoder maps of 16 MB to 268 MB):
+// about 1024 CTAs per launch, and all groups in one launch pair (smaller
+// batches that keep the apply pass's re-read in L2 cost more in extra
+// launches than they save).
+constexpr long long kTargetCtas = 1024;
+constexpr long long kMinPiece = 65536;
 
 struct GnPlan {
   qknr::GnParams kp;
@@ -46,7 +50,13 @@ qknr_status plan(const qknr_gn_args* a, GnPlan* pl) {
   if (a->l2_batch_bytes < -1) return fail(QKNR_ERR_SHAPE, "l2_batch_bytes must be >= -1");
 
   pl->spans = (long long)a->n * a->groups;
-  long long piece = a->piece_elems ? a->piece_elems : kDefaultPiece;
+  long long piece = a->piece_elems;
+  if (piece == 0) {
+    const long long want_p = (kTargetCtas + pl->spans - 1) / pl->spans;
+    piece = (L + want_p - 1) / want_p;
+    if (piece < kMinPiece) piece = kMinPiece;
+    piece = (piece + 7) / 8 * 8;
+  }
   if (piece > L) piece = (L + 7) / 8 * 8;
   const long long P = (L + piece - 1) / piece;
   if (P > 65535) return fail(QKNR_ERR_UNSUPPORTED, "more than 65535 pieces per group");
@@ -54,8 +64,8 @@ qknr_status plan(const qknr_gn_args* a, GnPlan* pl) {
   pl->pieces = static_cast<int>(P);
   pl->workspace = static_cast<size_t>(pl->spans * (P + 1) * 2 * sizeof(double));
   const long long span_bytes = L * 2;
-  const long long batch_bytes = a->l2_batch_bytes == 0 ? kDefaultBatchBytes : a->l2_batch_bytes;
-  long long bs = batch_bytes < 0 ? pl->spans : batch_bytes / span_bytes;
+  const long long batch_bytes = a->l2_batch_bytes;
+  long long bs = batch_bytes <= 0 ? pl->spans : batch_bytes / span_bytes;
   if (bs < 1) bs = 1;
   if (bs > pl->spans) bs = pl->spans;
   if (bs > 65535) bs = 65535;

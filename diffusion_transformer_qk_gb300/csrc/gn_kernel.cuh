@@ -16,8 +16,8 @@
 //          a = gamma[c]/sqrt(var + eps), b = beta[c] - mean*a per channel,
 //          and writes silu(x*a + b) = y / (1 + exp(-y)).
 //
-// The host issues the pair per batch of groups small enough to stay in L2,
-// so the apply launch re-reads the activations from L2, not from HBM.
+// The host issues the pair once for all groups, or per batch of groups
+// (a batch small enough for L2 lets the apply launch re-read from L2).
 #pragma once
 
 #include "qknr_ptx.cuh"
@@ -25,6 +25,7 @@
 namespace qknr {
 
 constexpr int kGnThreads = 256;
+constexpr int kGnBatch = 8;          // 16-byte loads a thread keeps in flight
 
 struct GnParams {
   const char* x;
@@ -70,15 +71,27 @@ __global__ void __launch_bounds__(kGnThreads) gn_stats_kernel(const __grid_const
   Elem<T>::unpack(__ldg(reinterpret_cast<const uint4*>(base)), first);
   const float2 nk = make_float2(-first[0].x, -first[0].x);
   float2 a1 = make_float2(0.0f, 0.0f), a2 = make_float2(0.0f, 0.0f);
-#pragma unroll 4
-  for (long long e = lo + threadIdx.x * 8; e < hi; e += kGnThreads * 8) {
-    float2 X[4];
-    Elem<T>::unpack(__ldg(reinterpret_cast<const uint4*>(base + e * 2)), X);
+  // kGnBatch independent 16-byte loads in flight per thread before any is used
+  constexpr long long kStride = kGnThreads * 8;
+  for (long long e0 = lo + threadIdx.x * 8; e0 < hi; e0 += kStride * kGnBatch) {
+    uint4 v[kGnBatch];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float2 d = __fadd2_rn(X[j], nk);
-      a1 = __fadd2_rn(a1, d);
-      a2 = __ffma2_rn(d, d, a2);
+    for (int b = 0; b < kGnBatch; ++b) {
+      const long long e = e0 + b * kStride;
+      v[b] = e < hi ? __ldg(reinterpret_cast<const uint4*>(base + e * 2)) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int b = 0; b < kGnBatch; ++b) {
+      if (e0 + b * kStride < hi) {
+        float2 X[4];
+        Elem<T>::unpack(v[b], X);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float2 d = __fadd2_rn(X[j], nk);
+          a1 = __fadd2_rn(a1, d);
+          a2 = __ffma2_rn(d, d, a2);
+        }
+      }
     }
   }
   const double s1 = cta_sum(static_cast<double>(a1.x) + static_cast<double>(a1.y), red[0]);
@@ -125,29 +138,40 @@ __global__ void __launch_bounds__(kGnThreads) gn_apply_kernel(const __grid_const
   // channel of the current chunk (a 16-byte chunk never straddles a
   // channel: H*W is a multiple of 8), refreshed only when a chunk crosses
   // into the next channel, with its folded coefficients a and b
-  long long e = lo + threadIdx.x * 8;
   long long ch_end = -1;
   float2 A = make_float2(0.0f, 0.0f), B = make_float2(0.0f, 0.0f);
-#pragma unroll 4
-  for (; e < hi; e += kGnThreads * 8) {
-    if (e >= ch_end) {
-      const long long cl = e / p.hw;
-      ch_end = (cl + 1) * p.hw;
-      const int c = g * p.group_channels + static_cast<int>(cl);
-      const float a = __fmul_rn(__ldg(p.gamma + c), rstd);
-      const float b = __fmaf_rn(-mean, a, __ldg(p.beta + c));
-      A = make_float2(a, a);
-      B = make_float2(b, b);
-    }
-    float2 X[4], O[4];
-    // a plain load: with out == x this kernel writes what it reads
-    Elem<T>::unpack(*reinterpret_cast<const uint4*>(base + e * 2), X);
+  constexpr long long kStride = kGnThreads * 8;
+  for (long long e0 = lo + threadIdx.x * 8; e0 < hi; e0 += kStride * kGnBatch) {
+    // plain loads (with out == x this kernel writes what it reads), all in
+    // flight before the first is used
+    uint4 v[kGnBatch];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float2 y = __ffma2_rn(X[j], A, B);
-      O[j] = make_float2(__fdividef(y.x, 1.0f + __expf(-y.x)), __fdividef(y.y, 1.0f + __expf(-y.y)));
+    for (int b = 0; b < kGnBatch; ++b) {
+      const long long e = e0 + b * kStride;
+      v[b] = e < hi ? *reinterpret_cast<const uint4*>(base + e * 2) : make_uint4(0, 0, 0, 0);
     }
-    store16(obase + e * 2, Elem<T>::pack(O));
+#pragma unroll
+    for (int b = 0; b < kGnBatch; ++b) {
+      const long long e = e0 + b * kStride;
+      if (e >= hi) break;
+      if (e >= ch_end) {
+        const long long cl = e / p.hw;
+        ch_end = (cl + 1) * p.hw;
+        const int c = g * p.group_channels + static_cast<int>(cl);
+        const float a = __fmul_rn(__ldg(p.gamma + c), rstd);
+        const float bb = __fmaf_rn(-mean, a, __ldg(p.beta + c));
+        A = make_float2(a, a);
+        B = make_float2(bb, bb);
+      }
+      float2 X[4], O[4];
+      Elem<T>::unpack(v[b], X);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 y = __ffma2_rn(X[j], A, B);
+        O[j] = make_float2(__fdividef(y.x, 1.0f + __expf(-y.x)), __fdividef(y.y, 1.0f + __expf(-y.y)));
+      }
+      store16(obase + e * 2, Elem<T>::pack(O));
+    }
   }
 }
 

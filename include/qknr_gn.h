@@ -16,10 +16,10 @@
  * (S1/L)^2.
  *
  * A group is large and there are few of them, so each is cut into pieces
- * and the call runs two stream-ordered kernels per batch of groups (piece
- * statistics into a caller-provided device workspace, then the normalise +
- * SiLU pass).  Batches are sized so the second kernel re-reads x from L2.
- * No kernel waits for another CTA.
+ * and the call runs two stream-ordered kernels (piece statistics into a
+ * caller-provided device workspace, then the normalise + SiLU pass), once
+ * for all groups or once per batch of groups.  No kernel waits for another
+ * CTA.
  *
  * Ownership and errors follow qknr.h: the caller owns every buffer
  * (activations, gamma, beta and the workspace); the library allocates
@@ -46,8 +46,8 @@ typedef struct qknr_gn_args {
   float eps;                  /* default 1e-6 */
   void *workspace;            /* device, 16-byte aligned, qknr_gn_workspace_bytes() */
   size_t workspace_bytes;
-  int32_t piece_elems;        /* elements per piece (multiple of 8); 0 = 32768 */
-  int64_t l2_batch_bytes;     /* activation bytes per batch of groups; 0 = 48 MiB, -1 = one batch */
+  int32_t piece_elems;        /* elements per piece (multiple of 8); 0 = about 1024 pieces in all, >= 65536 each */
+  int64_t l2_batch_bytes;     /* activation bytes per batch of groups; 0 or -1 = one batch */
 } qknr_gn_args;
 
 /* Defaults: bf16, eps 1e-6, automatic pieces and batches, all else zero. */

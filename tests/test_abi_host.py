@@ -248,7 +248,8 @@ def test_gn_workspace_bytes(lib):
     a = valid_gn()
     n = ctypes.c_size_t(0)
     assert lib.qknr_gn_workspace_bytes(ctypes.byref(a), ctypes.byref(n)) == 0
-    # 32 spans of 2*16*16 = 512 elements: one piece each, plus the shift record
+    # 32 spans of 2*16*16 = 512 elements: one piece each (pieces are at least
+    # 65536 elements), plus the shift record
     assert n.value == 32 * 2 * 16
     a.piece_elems = 64
     assert lib.qknr_gn_workspace_bytes(ctypes.byref(a), ctypes.byref(n)) == 0
