@@ -99,9 +99,10 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(sources=KERNEL_SOURCES) -> str:
+    """sha256 over the given kernel source files (in order)."""
     h = hashlib.sha256()
-    for name in KERNEL_SOURCES:
+    for name in sources:
         with open(os.path.join(ROOT, "diffusion_transformer_qk_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
@@ -109,14 +110,14 @@ def kernel_source_hash() -> str:
 
 def recorded_traffic(workload: str):
     """DRAM bytes per launch from the committed ncu record, if it was taken
-    on the current kernel sources; else None."""
+    on the current sources of that kernel; else None."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             rec = json.load(f).get(workload)
+        if not rec or rec.get("kernel_src_sha256") != kernel_source_hash(rec.get("sources", KERNEL_SOURCES)):
+            return None
     except Exception:
-        return None
-    if not rec or rec.get("kernel_src_sha256") != kernel_source_hash():
         return None
     return rec.get("dram_bytes_per_launch")
 
