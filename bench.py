@@ -519,8 +519,15 @@ def run_ours(args, w):
     flush = None
     if args.l2_flush == "on" or (args.l2_flush == "auto" and run.bytes_per_launch * L < 2 * l2):
         flush = torch.empty(2 * l2 // 4, dtype=torch.float32, device=dev)
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K * L)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K * L)]
+    # A step of one launch with no flush runs back to back: the launch's
+    # average duration over the timed region is the region's time / K, and
+    # no event sits between launches (an event there makes each launch wait
+    # for the previous one to drain).  Otherwise every launch is bracketed
+    # by its own pair of events.
+    per_launch = L > 1 or flush is not None
+    n_ev = K * L if per_launch else 0
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize(dev)
     barrier()
@@ -532,9 +539,11 @@ def run_ours(args, w):
         if flush is not None:
             flush.fill_(1.0)
         for a in run.args:
-            starts[j].record(stream)
+            if per_launch:
+                starts[j].record(stream)
             run.launch(a, stream)
-            ends[j].record(stream)
+            if per_launch:
+                ends[j].record(stream)
             j += 1
     e1.record(stream)
     torch.cuda.synchronize(dev)
@@ -543,7 +552,10 @@ def run_ours(args, w):
     sampler.stop()
     clocks = sampler.summary(t0, t1)
 
-    kernel_ms = statistics.fmean(s.elapsed_time(e) for s, e in zip(starts, ends))
+    if per_launch:
+        kernel_ms = statistics.fmean(s.elapsed_time(e) for s, e in zip(starts, ends))
+    else:
+        kernel_ms = e0.elapsed_time(e1) / K
     if flush is None:
         elapsed = e0.elapsed_time(e1) / 1e3
     else:
@@ -606,7 +618,9 @@ def run_ours(args, w):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic, "peak_source": f"{peak_kind} copy bandwidth (hbm_gbs)",
                      "algorithmic_bytes_per_launch": run.bytes_per_launch, "kernel_us": max_kernel_ms * 1e3,
-                     "launches_per_step": L, "kernel": info["kernel"]},
+                     "launches_per_step": L, "kernel": info["kernel"],
+                     "kernel_timing": ("per-launch CUDA events" if per_launch else
+                                       "CUDA events around the back-to-back timed region / steps")},
         "gpu_launches": K * L * getattr(run, "launches_per_call", 1),
         "clocks": clocks,
         "launch": {k: info[k] for k in ("grid", "block", "dyn_smem", "stages", "ctas_per_sm", "consumer_warps",

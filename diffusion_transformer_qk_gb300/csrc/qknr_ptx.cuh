@@ -57,12 +57,15 @@ __device__ __forceinline__ unsigned long long global_timer_ns() {
 
 // 1-D bulk copy global -> this CTA's shared memory, completion counted in
 // bytes on `bar`.  Both addresses 16-byte aligned, bytes a multiple of 16.
+// The source is marked evict-first in L2: every byte is streamed once.
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
                                           uint32_t bar) {
+  uint64_t policy;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(policy));
   asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
           dst),
-      "l"(src), "r"(bytes), "r"(bar)
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
       : "memory");
 }
 
