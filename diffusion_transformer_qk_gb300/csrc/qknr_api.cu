@@ -298,6 +298,7 @@ qknr_status size_launch(const qknr_args* a, Plan* pl) {
   const int passes = nq + nk;
   const bool wide_rows = passes >= 32 || passes == 0;
   const int warps = a->consumer_warps ? a->consumer_warps : (wide_rows ? 12 : 16);
+  const long long rows_per_cta_1 = (a->tokens + di.num_sms - 1) / di.num_sms;   // at one CTA per SM
   const int cps = a->ctas_per_sm ? a->ctas_per_sm : 1;
   const long long stage_bytes = pl->kp.stage_bytes;
   // shared memory one CTA may use when `cps` CTAs share an SM
@@ -308,9 +309,14 @@ qknr_status size_launch(const qknr_args* a, Plan* pl) {
   const long long grid0 = (long long)di.num_sms * cps;
   const long long rows_per_cta = (a->tokens + grid0 - 1) / grid0;
 
+  // Wide rows that carry a V copy, or that a CTA sees few of, do better as
+  // two groups of two stages (sweeps: Wan out of place 329 vs 350 us,
+  // FLUX.2 Q+K in one launch 73.8 vs 76.1 us); a deeper ring than four
+  // stages in all only queues more reads (Wan 231 vs 211 us with six).
+  const bool two_groups = wide_rows && passes > 0 && (pl->kp.hv > 0 || rows_per_cta_1 < 128);
   int gw = a->group_warps;
   if (gw == 0) {
-    int want = wide_rows ? warps : (passes + 5) / 6;      // about 6 passes per warp
+    int want = two_groups ? warps / 2 : (wide_rows ? warps : (passes + 5) / 6);   // narrow: ~6 passes per warp
     if (want < 1) want = 1;
     gw = warps;
     for (int g = want; g <= warps; ++g)
@@ -330,11 +336,11 @@ qknr_status size_launch(const qknr_args* a, Plan* pl) {
   if (warps % gw) return fail(QKNR_ERR_SHAPE, "group_warps %d does not divide consumer_warps %d", gw, warps);
   const int n_groups = warps / gw;
 
-  // ring depth per group: 4 for a single group, else about 128 KB of
-  // stages in all; at least two each
+  // ring depth per group: four stages in all for wide rows (one group of 4
+  // or two of 2), else about 128 KB of stages in all; at least two each
   int stages = a->stages;
   if (stages == 0) {
-    long long want = n_groups == 1 ? 4 : (128 * 1024) / (stage_bytes * n_groups);
+    long long want = wide_rows ? 4 / n_groups : (128 * 1024) / (stage_bytes * n_groups);
     if (want < 2) want = 2;
     if (want > 8) want = 8;
     long long cap = fit / n_groups;
