@@ -1,0 +1,66 @@
+"""The fused calls inside a captured CUDA graph: a replay on new data in the
+same buffers gives the bits an eager call gives."""
+import numpy as np
+import pytest
+import torch
+
+from diffusion_transformer_qk_gb300 import inputs as I
+from diffusion_transformer_qk_gb300 import qknr as Q
+from tests.gpu_util import to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(built_lib, cuda_device):
+    Q.load()
+
+
+def test_qk_norm_rope_replays_in_a_cuda_graph():
+    w = I.WORKLOADS["wan_32760x40x128"]
+    T = 4000
+    a = I.make_inputs(w, tokens=T)
+    b = I.make_inputs(w.with_(seed=5), tokens=T)
+    gq, gk = torch.from_numpy(a["gamma_q"]).cuda(), torch.from_numpy(a["gamma_k"]).cuda()
+    cos, sin = torch.from_numpy(a["cos"]).cuda(), torch.from_numpy(a["sin"]).cuda()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    qkv = to_dev(a["qkv"], "bf16")
+    # eager reference on the second input
+    ref = to_dev(b["qkv"], "bf16")
+    Q.qk_norm_rope_packed(ref, 40, 40, 40, 128, gq, gk, cos, sin, dev_status=status)
+    # warm-up call (configures the kernel), then capture
+    Q.qk_norm_rope_packed(qkv.clone(), 40, 40, 40, 128, gq, gk, cos, sin, dev_status=status)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            Q.qk_norm_rope_packed(qkv, 40, 40, 40, 128, gq, gk, cos, sin, dev_status=status)
+    torch.cuda.synchronize()
+    qkv.copy_(to_dev(b["qkv"], "bf16"))
+    g.replay()
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert torch.equal(qkv.view(torch.int16), ref.view(torch.int16))
+
+
+def test_adaln_replays_in_a_cuda_graph():
+    w = I.ADALN_WORKLOADS["adaln_flux2_2x4608x6144"]
+    a = I.make_adaln_inputs(w, tokens=3000)
+    b = I.make_adaln_inputs(w.with_(seed=9), tokens=3000)
+    sc = to_dev(a["scale"], "bf16")
+    sh = to_dev(a["shift"], "bf16")
+    ref = to_dev(b["x"], "bf16")
+    Q.adaln_modulate(ref, sc, sh, rows_per_batch=w.seq)
+    x = to_dev(a["x"], "bf16")
+    Q.adaln_modulate(x.clone(), sc, sh, rows_per_batch=w.seq)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            Q.adaln_modulate(x, sc, sh, rows_per_batch=w.seq)
+    x.copy_(to_dev(b["x"], "bf16"))
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(x.view(torch.int16), ref.view(torch.int16))
