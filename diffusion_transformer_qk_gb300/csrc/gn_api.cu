@@ -215,6 +215,8 @@ extern "C" qknr_status qknr_gn_silu_forward_noalloc(const qknr_gn_args* args, qk
                 "this shape needs %zu bytes of statistics scratch; the no-allocation entry point has %d "
                 "(use fewer pieces per group, or qknr_gn_silu_forward with a workspace)",
                 need, QKNR_GN_NOALLOC_SCRATCH_BYTES);
+  // argument errors come back before the first CUDA call (the address lookup)
+  if (!a.x || !a.gamma || !a.beta) return fail(QKNR_ERR_NULL, "x, gamma and beta are required");
   void* scratch = nullptr;
   st = scratch_address(&scratch);
   if (st != QKNR_OK) return st;

@@ -6,8 +6,10 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <map>
 #include <mutex>
 #include <unordered_map>
+#include <utility>
 
 #include "../../include/qknr.h"
 #include "qknr_internal.h"
@@ -32,8 +34,7 @@ qknr_status cuda_fail(cudaError_t e, const char* what) {
 namespace {
 std::mutex g_mu;
 std::unordered_map<int, DeviceInfo> g_dev;
-std::unordered_map<const void*, int> g_configured;   // kernel -> device mask with attribute set
-std::unordered_map<const void*, int> g_regs;
+std::map<std::pair<const void*, int>, int> g_configured;   // (kernel, device) -> registers per thread
 }  // namespace
 
 qknr_status device_info(int dev, DeviceInfo* out) {
@@ -63,17 +64,17 @@ qknr_status device_info(int dev, DeviceInfo* out) {
 
 qknr_status configure_kernel(const void* fn, int dev, const DeviceInfo& di, int* regs) {
   std::lock_guard<std::mutex> lk(g_mu);
-  int& mask = g_configured[fn];
-  if (!(mask & (1 << (dev & 31)))) {
+  const auto key = std::make_pair(fn, dev);
+  auto it = g_configured.find(key);
+  if (it == g_configured.end()) {
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, di.smem_optin);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(MaxDynamicSharedMemorySize)");
     cudaFuncAttributes fa;
     e = cudaFuncGetAttributes(&fa, fn);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncGetAttributes");
-    g_regs[fn] = fa.numRegs;
-    mask |= 1 << (dev & 31);
+    it = g_configured.emplace(key, fa.numRegs).first;
   }
-  *regs = g_regs[fn];
+  *regs = it->second;
   return QKNR_OK;
 }
 
