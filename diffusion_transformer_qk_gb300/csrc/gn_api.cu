@@ -1,7 +1,10 @@
-// C-ABI launcher of the group-norm + SiLU kernels: validation, piece and
-// batch planning, and the launches.  No allocation, no synchronisation.
+// C-ABI launcher of the group-norm + SiLU kernels: validation, the choice
+// between the fused and the two-pass path, piece and batch planning, and
+// the launches.  No allocation, no synchronisation.
 #include <cuda_runtime.h>
 
+#include <atomic>
+#include <cstdio>
 #include <cstring>
 #include <mutex>
 
@@ -16,20 +19,30 @@ using qknr_host::fail;
 using qknr_host::Span;
 using qknr_host::span_of;
 
-// Defaults from sweeps on GB300 (VAE decoder maps of 16 MB to 268 MB):
-// about 1024 CTAs per launch, and all groups in one launch pair (smaller
-// batches that keep the apply pass's re-read in L2 cost more in extra
-// launches than they save).
+// Two-pass defaults from sweeps on GB300 (VAE decoder maps of 16 MB to
+// 268 MB): about 1024 CTAs per launch, and all groups in one launch pair
+// (smaller batches that keep the apply pass's re-read in L2 cost more in
+// extra launches than they save).
 constexpr long long kTargetCtas = 1024;
 constexpr long long kMinPiece = 65536;
+constexpr unsigned long long kDefaultWaitNs = 2000000000ull;
 
 struct GnPlan {
-  qknr::GnParams kp;
   long long spans = 0;          // N * G
+  long long L = 0;              // elements per span
+  // two-pass path
+  qknr::GnParams kp;
   long long piece_len = 0;
   int pieces = 0;
   long long batch_spans = 0;    // spans per launch pair
-  size_t workspace = 0;
+  size_t ws_two = 0;
+  // fused path (sizes that do not depend on the device)
+  bool fused_shape = false;     // chunk count in range
+  unsigned f_pieces = 0;        // P = ceil(L / kGnfChunk)
+  size_t f_records = 0;         // bytes of the [spans][P + 1] 16-byte records
+  size_t ws_fused = 0;
+  bool want_fused = false;      // AUTO without two-pass tuning, or FUSED
+  size_t workspace = 0;         // what qknr_gn_workspace_bytes reports
 };
 
 qknr_status plan(const qknr_gn_args* a, GnPlan* pl) {
@@ -38,6 +51,8 @@ qknr_status plan(const qknr_gn_args* a, GnPlan* pl) {
     return fail(QKNR_ERR_ABI, "abi_version %u, library expects %d", a->abi_version, QKNR_ABI_VERSION);
   if (a->dtype != QKNR_BF16 && a->dtype != QKNR_FP16)
     return fail(QKNR_ERR_UNSUPPORTED, "activation dtype must be BF16 or FP16");
+  if (a->mode != QKNR_GN_AUTO && a->mode != QKNR_GN_FUSED && a->mode != QKNR_GN_TWO_PASS)
+    return fail(QKNR_ERR_UNSUPPORTED, "unknown mode %d", a->mode);
   if (a->n <= 0 || a->c <= 0 || a->h <= 0 || a->w <= 0 || a->groups <= 0)
     return fail(QKNR_ERR_SHAPE, "n, c, h, w and groups must be positive");
   if (a->c % a->groups) return fail(QKNR_ERR_SHAPE, "groups must divide channels");
@@ -50,6 +65,9 @@ qknr_status plan(const qknr_gn_args* a, GnPlan* pl) {
   if (a->l2_batch_bytes < -1) return fail(QKNR_ERR_SHAPE, "l2_batch_bytes must be >= -1");
 
   pl->spans = (long long)a->n * a->groups;
+  pl->L = L;
+
+  // ---- two-pass path
   long long piece = a->piece_elems;
   if (piece == 0) {
     const long long want_p = (kTargetCtas + pl->spans - 1) / pl->spans;
@@ -59,10 +77,10 @@ qknr_status plan(const qknr_gn_args* a, GnPlan* pl) {
   }
   if (piece > L) piece = (L + 7) / 8 * 8;
   const long long P = (L + piece - 1) / piece;
-  if (P > 65535) return fail(QKNR_ERR_UNSUPPORTED, "more than 65535 pieces per group");
+  const bool two_ok = P <= 65535;
   pl->piece_len = piece;
-  pl->pieces = static_cast<int>(P);
-  pl->workspace = static_cast<size_t>(pl->spans * (P + 1) * 2 * sizeof(double));
+  pl->pieces = static_cast<int>(two_ok ? P : 0);
+  pl->ws_two = static_cast<size_t>(pl->spans * (P + 1) * 2 * sizeof(double));
   const long long span_bytes = L * 2;
   const long long batch_bytes = a->l2_batch_bytes;
   long long bs = batch_bytes <= 0 ? pl->spans : batch_bytes / span_bytes;
@@ -77,7 +95,7 @@ qknr_status plan(const qknr_gn_args* a, GnPlan* pl) {
   kp.out = static_cast<char*>(a->out ? a->out : const_cast<void*>(a->x));
   kp.gamma = a->gamma;
   kp.beta = a->beta;
-  kp.partial = static_cast<double*>(a->workspace);
+  kp.rec = static_cast<unsigned long long*>(a->workspace);
   kp.span_len = L;
   kp.hw = hw;
   kp.piece_len = piece;
@@ -86,6 +104,97 @@ qknr_status plan(const qknr_gn_args* a, GnPlan* pl) {
   kp.group_channels = a->c / a->groups;
   kp.pieces = pl->pieces;
   kp.eps = a->eps;
+
+  // ---- fused path
+  const long long fP = (L + qknr::kGnfChunk - 1) / qknr::kGnfChunk;
+  pl->fused_shape = pl->spans * fP < (1ll << 31);
+  pl->f_pieces = static_cast<unsigned>(fP);
+  pl->f_records = static_cast<size_t>(pl->spans * (fP + 1) * 2 * sizeof(double));
+  pl->ws_fused = pl->f_records + 16;   // + the abort word
+
+  const bool tuned = a->piece_elems != 0 || a->l2_batch_bytes != 0;
+  pl->want_fused = a->mode == QKNR_GN_FUSED || (a->mode == QKNR_GN_AUTO && !tuned);
+  if (a->mode == QKNR_GN_FUSED) {
+    if (!pl->fused_shape) return fail(QKNR_ERR_UNSUPPORTED, "2^31 or more pieces in all for the fused path");
+    pl->workspace = pl->ws_fused;
+  } else if (pl->want_fused && pl->fused_shape) {
+    if (!two_ok) {
+      pl->workspace = pl->ws_fused;   // only the fused path could run this shape
+    } else {
+      pl->workspace = pl->ws_two > pl->ws_fused ? pl->ws_two : pl->ws_fused;
+    }
+  } else {
+    pl->want_fused = false;
+    if (!two_ok) return fail(QKNR_ERR_UNSUPPORTED, "more than 65535 pieces per group");
+    pl->workspace = pl->ws_two;
+  }
+  return QKNR_OK;
+}
+
+// The fused launch on the current device, or why there is none.
+struct FusedLaunch {
+  bool ok = false;
+  const void* fn = nullptr;
+  int grid = 0;
+  int per_cta = 0;            // most pieces of one group a CTA holds
+  int regs = 0;
+  int num_sms = 0;
+  char why[160] = "";
+};
+
+qknr_status fused_launch(const qknr_gn_args* a, const GnPlan& pl, FusedLaunch* fl) {
+  fl->fn = a->dtype == QKNR_BF16 ? reinterpret_cast<const void*>(&qknr::gn_fused_kernel<__nv_bfloat16>)
+                                 : reinterpret_cast<const void*>(&qknr::gn_fused_kernel<__half>);
+  if (!pl.fused_shape) {
+    snprintf(fl->why, sizeof(fl->why), "2^31 or more pieces in all");
+    return QKNR_OK;
+  }
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return qknr_host::cuda_fail(e, "cudaGetDevice");
+  qknr_host::DeviceInfo di;
+  qknr_status st = qknr_host::device_info(dev, &di);
+  if (st != QKNR_OK) return st;
+  fl->num_sms = di.num_sms;
+  if (!di.cooperative) {
+    snprintf(fl->why, sizeof(fl->why), "the device has no cooperative launch");
+    return QKNR_OK;
+  }
+  if (di.smem_optin < qknr::kGnfSmemBytes) {
+    snprintf(fl->why, sizeof(fl->why), "%d bytes of shared memory per block, %d needed", di.smem_optin,
+             qknr::kGnfSmemBytes);
+    return QKNR_OK;
+  }
+  st = qknr_host::configure_kernel(fl->fn, dev, di, &fl->regs);
+  if (st != QKNR_OK) return st;
+  const long long chunks = pl.spans * static_cast<long long>(pl.f_pieces);
+  const long long G = chunks < di.num_sms ? chunks : di.num_sms;      // one CTA per SM
+  // a CTA holds at most ceil(P / G) pieces of a group; at most kGnfSlots
+  // keeps every wait finite
+  const long long per_cta = (pl.f_pieces + G - 1) / G;
+  if (per_cta > qknr::kGnfSlots) {
+    snprintf(fl->why, sizeof(fl->why), "a group of %u pieces needs %lld per CTA on %lld CTAs (at most %d)",
+             pl.f_pieces, per_cta, G, qknr::kGnfSlots);
+    return QKNR_OK;
+  }
+  fl->grid = static_cast<int>(G);
+  fl->per_cta = static_cast<int>(per_cta);
+  fl->ok = true;
+  return QKNR_OK;
+}
+
+// Resolve the path: *use_fused, with fl filled when it is true.
+qknr_status choose(const qknr_gn_args* a, const GnPlan& pl, FusedLaunch* fl, bool* use_fused) {
+  *use_fused = false;
+  if (!pl.want_fused) return QKNR_OK;
+  qknr_status st = fused_launch(a, pl, fl);
+  if (st != QKNR_OK) return st;
+  if (fl->ok) {
+    *use_fused = true;
+    return QKNR_OK;
+  }
+  if (a->mode == QKNR_GN_FUSED) return fail(QKNR_ERR_UNSUPPORTED, "fused group norm: %s", fl->why);
+  if (pl.pieces == 0) return fail(QKNR_ERR_UNSUPPORTED, "more than 65535 pieces per group (and fused: %s)", fl->why);
   return QKNR_OK;
 }
 
@@ -96,9 +205,11 @@ qknr_status check_buffers(const qknr_gn_args* a, const GnPlan& pl) {
     return fail(QKNR_ERR_SHAPE, "workspace of %zu bytes, %zu needed", a->workspace_bytes, pl.workspace);
   const void* out = a->out ? a->out : a->x;
   if (!aligned16(a->x) || !aligned16(out) || !aligned16(a->workspace) ||
-      (reinterpret_cast<uintptr_t>(a->gamma) & 3u) || (reinterpret_cast<uintptr_t>(a->beta) & 3u))
-    return fail(QKNR_ERR_ALIGN, "x / out / workspace not 16-byte aligned, or gamma / beta not 4-byte aligned");
-  const long long total = pl.spans * pl.kp.span_len * 2;
+      (reinterpret_cast<uintptr_t>(a->gamma) & 3u) || (reinterpret_cast<uintptr_t>(a->beta) & 3u) ||
+      (reinterpret_cast<uintptr_t>(a->dev_status) & 3u))
+    return fail(QKNR_ERR_ALIGN,
+                "x / out / workspace not 16-byte aligned, or gamma / beta / dev_status not 4-byte aligned");
+  const long long total = pl.spans * pl.L * 2;
   const Span sx = span_of(a->x, 1, 0, total), so = span_of(out, 1, 0, total);
   const Span sw = span_of(a->workspace, 1, 0, static_cast<long long>(pl.workspace));
   const Span sg = span_of(a->gamma, 1, 0, (long long)a->c * 4), sb = span_of(a->beta, 1, 0, (long long)a->c * 4);
@@ -107,6 +218,70 @@ qknr_status check_buffers(const qknr_gn_args* a, const GnPlan& pl) {
     return fail(QKNR_ERR_OVERLAP, "out overlaps an input without being in place");
   if (qknr_host::overlaps(sw, sx) || qknr_host::overlaps(sw, sg) || qknr_host::overlaps(sw, sb))
     return fail(QKNR_ERR_OVERLAP, "workspace overlaps an input");
+  return QKNR_OK;
+}
+
+// A per-call record tag: a bijective 32-bit mix of a process-wide call
+// counter (no tag repeats within 2^32 calls; tags do not look like small
+// integers or zeros left in a reused workspace), never 0 (the two-pass tag).
+unsigned next_tag() {
+  static std::atomic<unsigned> counter{0};
+  while (true) {
+    unsigned x = counter.fetch_add(1u, std::memory_order_relaxed) + 1u;
+    x *= 0x9E3779B1u;
+    x ^= x >> 16;
+    x *= 0x85EBCA6Bu;
+    x ^= x >> 13;
+    if (x != 0u) return x;
+  }
+}
+
+qknr_status launch_fused(const qknr_gn_args* a, const GnPlan& pl, const FusedLaunch& fl, cudaStream_t s) {
+  char* ws = static_cast<char*>(a->workspace);
+  qknr::GnFusedParams fp;
+  memset(&fp, 0, sizeof(fp));
+  fp.x = static_cast<const char*>(a->x);
+  fp.out = static_cast<char*>(a->out ? a->out : const_cast<void*>(a->x));
+  fp.gamma = a->gamma;
+  fp.beta = a->beta;
+  fp.rec = reinterpret_cast<unsigned long long*>(ws);
+  fp.abort_word = reinterpret_cast<unsigned*>(ws + pl.f_records);
+  fp.status = a->dev_status;
+  fp.span_len = pl.L;
+  fp.hw = (long long)a->h * a->w;
+  fp.pieces = pl.f_pieces;
+  fp.total_chunks = static_cast<unsigned>(pl.spans * static_cast<long long>(pl.f_pieces));
+  fp.groups = a->groups;
+  fp.group_channels = a->c / a->groups;
+  fp.channels = a->c;
+  fp.tag = next_tag();
+  fp.flags = a->flags & (qknr::kGnfFlagStallLoads | qknr::kGnfFlagStallRecords);
+  fp.wait_limit_ns = a->wait_limit_ns ? a->wait_limit_ns : kDefaultWaitNs;
+  fp.eps = a->eps;
+  void* kargs[] = {&fp};
+  cudaError_t e = cudaLaunchCooperativeKernel(fl.fn, dim3(fl.grid), dim3(qknr::kGnfThreads), kargs,
+                                              static_cast<size_t>(qknr::kGnfSmemBytes), s);
+  if (e != cudaSuccess) return qknr_host::cuda_fail(e, "cudaLaunchCooperativeKernel(fused group norm)");
+  return QKNR_OK;
+}
+
+qknr_status launch_two_pass(const qknr_gn_args* a, const GnPlan& pl, cudaStream_t s) {
+  const bool bf16 = a->dtype == QKNR_BF16;
+  const void* stats = bf16 ? reinterpret_cast<const void*>(&qknr::gn_stats_kernel<__nv_bfloat16>)
+                           : reinterpret_cast<const void*>(&qknr::gn_stats_kernel<__half>);
+  const void* apply = bf16 ? reinterpret_cast<const void*>(&qknr::gn_apply_kernel<__nv_bfloat16>)
+                           : reinterpret_cast<const void*>(&qknr::gn_apply_kernel<__half>);
+  for (long long s0 = 0; s0 < pl.spans; s0 += pl.batch_spans) {
+    qknr::GnParams kp = pl.kp;
+    kp.span0 = static_cast<int>(s0);
+    const long long nb = pl.spans - s0 < pl.batch_spans ? pl.spans - s0 : pl.batch_spans;
+    const dim3 grid(static_cast<unsigned>(pl.pieces), static_cast<unsigned>(nb));
+    void* kargs[] = {&kp};
+    cudaError_t e = cudaLaunchKernel(stats, grid, dim3(qknr::kGnThreads), kargs, 0, s);
+    if (e != cudaSuccess) return qknr_host::cuda_fail(e, "cudaLaunchKernel(group norm statistics)");
+    e = cudaLaunchKernel(apply, grid, dim3(qknr::kGnThreads), kargs, 0, s);
+    if (e != cudaSuccess) return qknr_host::cuda_fail(e, "cudaLaunchKernel(group norm apply)");
+  }
   return QKNR_OK;
 }
 
@@ -120,6 +295,7 @@ void qknr_gn_args_init(qknr_gn_args* a) {
   a->abi_version = QKNR_ABI_VERSION;
   a->dtype = QKNR_BF16;
   a->eps = 1e-6f;
+  a->mode = QKNR_GN_AUTO;
 }
 
 qknr_status qknr_gn_workspace_bytes(const qknr_gn_args* args, size_t* bytes) {
@@ -137,22 +313,44 @@ qknr_status qknr_gn_silu_forward(const qknr_gn_args* args, qknr_stream_t stream)
   if (st != QKNR_OK) return st;
   st = check_buffers(args, pl);
   if (st != QKNR_OK) return st;
-  const bool bf16 = args->dtype == QKNR_BF16;
-  const void* stats = bf16 ? reinterpret_cast<const void*>(&qknr::gn_stats_kernel<__nv_bfloat16>)
-                           : reinterpret_cast<const void*>(&qknr::gn_stats_kernel<__half>);
-  const void* apply = bf16 ? reinterpret_cast<const void*>(&qknr::gn_apply_kernel<__nv_bfloat16>)
-                           : reinterpret_cast<const void*>(&qknr::gn_apply_kernel<__half>);
+  FusedLaunch fl;
+  bool fused = false;
+  st = choose(args, pl, &fl, &fused);
+  if (st != QKNR_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  for (long long s0 = 0; s0 < pl.spans; s0 += pl.batch_spans) {
-    qknr::GnParams kp = pl.kp;
-    kp.span0 = static_cast<int>(s0);
-    const long long nb = pl.spans - s0 < pl.batch_spans ? pl.spans - s0 : pl.batch_spans;
-    const dim3 grid(static_cast<unsigned>(pl.pieces), static_cast<unsigned>(nb));
-    void* kargs[] = {&kp};
-    cudaError_t e = cudaLaunchKernel(stats, grid, dim3(qknr::kGnThreads), kargs, 0, s);
-    if (e != cudaSuccess) return qknr_host::cuda_fail(e, "cudaLaunchKernel(group norm statistics)");
-    e = cudaLaunchKernel(apply, grid, dim3(qknr::kGnThreads), kargs, 0, s);
-    if (e != cudaSuccess) return qknr_host::cuda_fail(e, "cudaLaunchKernel(group norm apply)");
+  return fused ? launch_fused(args, pl, fl, s) : launch_two_pass(args, pl, s);
+}
+
+qknr_status qknr_gn_query(const qknr_gn_args* args, qknr_launch_info* info) {
+  if (!info) return fail(QKNR_ERR_NULL, "info is NULL");
+  memset(info, 0, sizeof(*info));
+  GnPlan pl;
+  qknr_status st = plan(args, &pl);
+  if (st != QKNR_OK) return st;
+  FusedLaunch fl;
+  bool fused = false;
+  st = choose(args, pl, &fl, &fused);
+  if (st != QKNR_OK) return st;
+  const char* dt = args->dtype == QKNR_BF16 ? "bf16" : "fp16";
+  if (fused) {
+    info->grid = fl.grid;
+    info->block = qknr::kGnfThreads;
+    info->dyn_smem = qknr::kGnfSmemBytes;
+    info->stages = qknr::kGnfSlots;
+    info->ctas_per_sm = 1;
+    info->consumer_warps = qknr::kGnfStatsWarps + qknr::kGnfApplyWarps;
+    info->stage_bytes = qknr::kGnfChunkBytes;
+    info->registers = fl.regs;
+    info->num_sms = fl.num_sms;
+    snprintf(info->kernel, sizeof(info->kernel), "gn_fused<%s>, %u pieces per group, %d per CTA", dt,
+             pl.f_pieces, fl.per_cta);
+  } else {
+    const long long nb = pl.batch_spans;
+    info->grid = static_cast<int32_t>(pl.pieces * nb);
+    info->block = qknr::kGnThreads;
+    info->stage_bytes = static_cast<int32_t>(pl.piece_len * 2);
+    snprintf(info->kernel, sizeof(info->kernel), "gn_stats+gn_apply<%s> x%lld, %d pieces per group", dt,
+             (pl.spans + nb - 1) / nb, pl.pieces);
   }
   return QKNR_OK;
 }

@@ -3,21 +3,29 @@
 //
 // Activations are NCHW, so the (C/G)*H*W elements of sample n, group g are
 // one contiguous span.  A group has few and large spans (32 groups of up to
-// millions of elements in a VAE decoder), so each span is cut into P pieces
-// and the work runs in two stream-ordered launches, with no CTA ever
-// waiting for another:
+// millions of elements in a VAE decoder), so each span is cut into P pieces.
+// Per piece: fp32 sums S1 = sum (x - K) and S2 = sum (x - K)^2 around the
+// span's first element K (per-thread sums over 16-byte vectors, an fp32
+// xor tree in each warp, the warps' sums added in order).  Per span: the P
+// pieces' sums added in compensated fp32 in one fixed order (combine_span),
+// mean = K + S1/L, var = S2/L - (S1/L)^2, then per channel a = gamma[c] * rstd,
+// b = beta[c] - mean * a, and out = silu(x*a + b) = y / (1 + exp(-y)).
+// (exp and the reciprocal on the special-function unit: ex2.approx and
+// rcp.approx, about 2 ulp.)
 //
-//   stats: one CTA per piece; 16-byte loads; per-thread fp32 sums of
-//          (x - K) and (x - K)^2 around the span's first element K, then an
-//          fp64 reduction over the CTA into workspace[span][piece] = (S1, S2);
-//          piece 0 also records K in workspace[span][P].
-//   apply: one CTA per piece; it adds its span's P partials in fixed order
-//          (fp64), forms mean = K + S1/L and var = S2/L - (S1/L)^2, folds
-//          a = gamma[c]/sqrt(var + eps), b = beta[c] - mean*a per channel,
-//          and writes silu(x*a + b) = y / (1 + exp(-y)).
+// Two paths, with the same arithmetic (equal bits for equal pieces):
+//   two-pass: gn_stats_kernel (one CTA per piece) writes the pieces' sums
+//     to the workspace, gn_apply_kernel (one CTA per piece) combines and
+//     writes; x is read twice and no CTA waits for another.
+//   fused: gn_fused_kernel, one persistent launch that reads x once (see
+//     the comment above it).
 //
-// The host issues the pair once for all groups, or per batch of groups
-// (a batch small enough for L2 lets the apply launch re-read from L2).
+// Workspace records, 16 bytes per piece and one more per span: two 8-byte
+// words, each (tag << 32) | the bits of an fp32 value: (S1, S2) for piece
+// i < P, (K, 0) at index P.  An 8-byte store is single-copy atomic, so a
+// word that carries the expected tag also carries its value: the fused
+// path's waits look for its per-call tag, with no counter and no fence.
+// The two-pass path writes tag 0 and does not look at tags.
 #pragma once
 
 #include "qknr_ptx.cuh"
@@ -25,6 +33,7 @@
 namespace qknr {
 
 constexpr int kGnThreads = 256;
+constexpr int kGnWarps = kGnThreads / 32;
 constexpr int kGnBatch = 8;          // 16-byte loads a thread keeps in flight
 
 struct GnParams {
@@ -32,7 +41,7 @@ struct GnParams {
   char* out;
   const float* gamma;
   const float* beta;
-  double* partial;             // [spans][pieces + 1][2]: S1, S2 of each piece; then (K, 0)
+  unsigned long long* rec;     // [spans][pieces + 1][2] tagged words
   long long span_len;          // L = (C/G) * H * W elements
   long long hw;                // H * W (a multiple of 8)
   long long piece_len;         // elements per piece (a multiple of 8)
@@ -44,23 +53,256 @@ struct GnParams {
   float eps;
 };
 
-// sum of a double over the CTA (kGnThreads threads); valid in thread 0
-__device__ __forceinline__ double cta_sum(double v, double* red) {
-#pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (lane == 0) red[warp] = v;
-  __syncthreads();
-  double t = 0.0;
-  if (threadIdx.x == 0)
-    for (int w = 0; w < kGnThreads / 32; ++w) t += red[w];
-  __syncthreads();
-  return t;
+__device__ __forceinline__ unsigned long long tagged(unsigned tag, float v) {
+  return (static_cast<unsigned long long>(tag) << 32) | __float_as_uint(v);
 }
+
+__device__ __forceinline__ float tagged_value(unsigned long long w) {
+  return __uint_as_float(static_cast<unsigned>(w));
+}
+
+__device__ __forceinline__ unsigned tag_of(unsigned long long w) { return static_cast<unsigned>(w >> 32); }
+
+// 16-byte record store / load at gpu scope, each 8-byte half single-copy atomic
+__device__ __forceinline__ void st_record(unsigned long long* p, unsigned long long a, unsigned long long b) {
+  asm volatile("st.relaxed.gpu.global.v2.b64 [%0], {%1, %2};" ::"l"(p), "l"(a), "l"(b) : "memory");
+}
+
+__device__ __forceinline__ ulonglong2 ld_record(const unsigned long long* p) {
+  unsigned long long a, b;
+  asm volatile("ld.relaxed.gpu.global.v2.b64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
+  return make_ulonglong2(a, b);
+}
+
+// The statistics of one piece from per-thread fp32 pair sums: fp32 xor tree
+// in each warp, warp sums added in order by thread 0.  `red` holds 2 *
+// kGnWarps floats; `sync` is the barrier over the kGnThreads threads.
+// Valid in thread 0.
+template <typename Sync>
+__device__ __forceinline__ void piece_sums(float2 a1, float2 a2, float* red, Sync sync, float* s1, float* s2) {
+  float v1 = __fadd_rn(a1.x, a1.y), v2 = __fadd_rn(a2.x, a2.y);
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    v1 = __fadd_rn(v1, __shfl_xor_sync(0xffffffffu, v1, off));
+    v2 = __fadd_rn(v2, __shfl_xor_sync(0xffffffffu, v2, off));
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) {
+    red[warp] = v1;
+    red[kGnWarps + warp] = v2;
+  }
+  sync();
+  float t1 = 0.0f, t2 = 0.0f;
+  if (threadIdx.x == 0) {
+    for (int w = 0; w < kGnWarps; ++w) t1 = __fadd_rn(t1, red[w]);
+    for (int w = 0; w < kGnWarps; ++w) t2 = __fadd_rn(t2, red[kGnWarps + w]);
+  }
+  *s1 = t1;
+  *s2 = t2;
+}
+
+// Bounded-wait context of the fused path's record polls.
+struct RecordWait {
+  unsigned tag;                      // the call's tag
+  unsigned long long limit_ns;
+  volatile int* abort_cta;           // shared-memory abort flag of the CTA
+  unsigned* abort_grid;              // == tag once any CTA has given up
+  int* status;
+};
+
+// whether this CTA or another has given up (then this CTA's flag is raised)
+__device__ __forceinline__ bool grid_aborted(const RecordWait& w) {
+  if (*w.abort_cta) return true;
+  if (*reinterpret_cast<volatile unsigned*>(w.abort_grid) != w.tag) return false;
+  *w.abort_cta = 1;
+  return true;
+}
+
+__device__ __forceinline__ void give_up(const RecordWait& w) {
+  *w.abort_cta = 1;
+  atomicExch(w.abort_grid, w.tag);
+  if (w.status) atomicCAS(w.status, 0, kStatusTimeout);
+}
+
+// Compensated fp32 sums (Neumaier's variant of Kahan summation): hi + lo
+// carries the sum with about twice fp32's precision.  GB300's fp64 rate is
+// a small fraction of its fp32 rate, so the per-span combine stays in fp32.
+struct Sum2 {
+  float hi = 0.0f, lo = 0.0f;
+  __device__ __forceinline__ void add(float x) {
+    const float t = __fadd_rn(hi, x);
+    lo = __fadd_rn(lo, fabsf(hi) >= fabsf(x) ? __fadd_rn(__fsub_rn(hi, t), x) : __fadd_rn(__fsub_rn(x, t), hi));
+    hi = t;
+  }
+  // hi + lo of two compensated sums: the rounding error of hi + o.hi is
+  // exact (Knuth's TwoSum), so the result does not depend on the order of
+  // the two operands
+  __device__ __forceinline__ void merge(const Sum2& o) {
+    const float s = __fadd_rn(hi, o.hi);
+    const float bb = __fsub_rn(s, hi);
+    const float e = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bb)), __fsub_rn(o.hi, bb));
+    lo = __fadd_rn(__fadd_rn(lo, o.lo), e);
+    hi = s;
+  }
+  __device__ __forceinline__ float value() const { return __fadd_rn(hi, lo); }
+};
+
+__device__ __forceinline__ Sum2 shfl_xor_sum2(const Sum2& v, int off) {
+  Sum2 o;
+  o.hi = __shfl_xor_sync(0xffffffffu, v.hi, off);
+  o.lo = __shfl_xor_sync(0xffffffffu, v.lo, off);
+  return o;
+}
+
+// Mean and 1/sqrt(var + eps) of a span from its records, in one fixed
+// order: lane l adds pieces l, l+32, l+64, ... into compensated fp32 sums
+// (up to eight records in flight; the order of the additions does not
+// change), then an xor tree over the warp that ends with the same sums in
+// every lane; mean = K + S1/L, var = max(S2/L - (S1/L)^2, 0).  Called by
+// one whole warp; lane 0 writes coef[0] = mean, coef[1] = rstd.
+//
+// kWait (fused path): a record counts only once both its words carry
+// w->tag; a lane re-reads from its first record without it, so the records
+// are polled and read in the same loads.  Returns false, in every lane,
+// when a lane gave up (bounded by w->limit_ns, or another CTA gave up).
+template <bool kWait>
+__device__ __forceinline__ bool combine_span(const unsigned long long* rec, int pieces, long long span_len,
+                                             float eps, const RecordWait* w, float* coef) {
+  constexpr int kBatch = 8;
+  const int lane = threadIdx.x & 31;
+  // the shift K (written with piece 0's sums), loaded with the first batch
+  unsigned long long kw = lane == 0 ? ld_record(rec + 2 * pieces).x : 0ull;
+  Sum2 s1, s2;
+  bool ok = true;
+  unsigned long long t0 = 0;
+  unsigned backoff = 32;                             // ns between polls, doubling to 1 us
+  int i = lane;
+  while (i < pieces) {
+    ulonglong2 v[kBatch];
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int k = i + 32 * b;
+      v[b] = k < pieces ? ld_record(rec + 2 * k) : make_ulonglong2(0ull, 0ull);
+    }
+    int took = 0;
+    bool stop = false;
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      if (!stop && i + 32 * b < pieces && (!kWait || (tag_of(v[b].x) == w->tag && tag_of(v[b].y) == w->tag))) {
+        s1.add(tagged_value(v[b].x));
+        s2.add(tagged_value(v[b].y));
+        ++took;
+      } else {
+        stop = true;
+      }
+    }
+    i += 32 * took;
+    if (kWait && took == 0) {
+      if (t0 == 0) t0 = global_timer_ns();
+      if (grid_aborted(*w)) {
+        ok = false;
+        break;
+      }
+      if (global_timer_ns() - t0 > w->limit_ns) {
+        give_up(*w);
+        ok = false;
+        break;
+      }
+      __nanosleep(backoff);
+      backoff = backoff < 1024 ? 2 * backoff : 1024;
+    } else {
+      backoff = 32;
+    }
+  }
+  if (kWait && lane == 0 && ok) {
+    if (t0 == 0) t0 = global_timer_ns();
+    while (tag_of(kw) != w->tag) {
+      if (grid_aborted(*w)) {
+        ok = false;
+        break;
+      }
+      if (global_timer_ns() - t0 > w->limit_ns) {
+        give_up(*w);
+        ok = false;
+        break;
+      }
+      __nanosleep(backoff);
+      backoff = backoff < 1024 ? 2 * backoff : 1024;
+      kw = ld_record(rec + 2 * pieces).x;
+    }
+  }
+  if (!__all_sync(0xffffffffu, ok)) return false;
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    const Sum2 o1 = shfl_xor_sum2(s1, off), o2 = shfl_xor_sum2(s2, off);
+    s1.merge(o1);
+    s2.merge(o2);
+  }
+  if (lane == 0) {
+    const float inv_l = __frcp_rn(static_cast<float>(span_len));
+    const float m1 = __fmul_rn(s1.value(), inv_l);
+    float var = __fmaf_rn(-m1, m1, __fmul_rn(s2.value(), inv_l));
+    var = var > 0.0f ? var : 0.0f;
+    coef[0] = __fadd_rn(tagged_value(kw), m1);
+    coef[1] = rsqrtf(__fadd_rn(var, eps));
+  }
+  return true;
+}
+
+// Folded coefficients of channel c: a = gamma[c] * rstd, b = beta[c] - mean * a
+__device__ __forceinline__ void fold_channel(float g, float be, float mean, float rstd, float2& A, float2& B) {
+  const float a = __fmul_rn(g, rstd);
+  const float bb = __fmaf_rn(-mean, a, be);
+  A = make_float2(a, a);
+  B = make_float2(bb, bb);
+}
+
+// Channel (within the group) of element e of a span: e < L < 2^31
+__device__ __forceinline__ unsigned channel_of(long long e, long long hw) {
+  return static_cast<unsigned>(e) / static_cast<unsigned>(hw);
+}
+
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// silu(x*a + b) of one 16-byte vector (a vector never straddles a channel:
+// H*W is a multiple of 8): y = x*a + b, e^-y = 2^(-y * log2(e)) on the
+// special-function unit, silu(y) = y * (1 / (1 + e^-y)), the fp32 steps on
+// paired instructions.  Saturates correctly: e^-y overflows to +inf for very
+// negative y, giving y * 0.
+constexpr float kNegLog2e = -1.4426950408889634f;    // -log2(e)
+
+template <typename T>
+__device__ __forceinline__ uint4 silu_affine(const uint4& raw, const float2& A, const float2& B) {
+  float2 X[4], O[4];
+  Elem<T>::unpack(raw, X);
+  const float2 nl = make_float2(kNegLog2e, kNegLog2e), one = make_float2(1.0f, 1.0f);
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float2 y = __ffma2_rn(X[j], A, B);
+    const float2 t = __fmul2_rn(y, nl);
+    const float2 d = __fadd2_rn(make_float2(ex2_approx(t.x), ex2_approx(t.y)), one);
+    O[j] = __fmul2_rn(y, make_float2(rcp_approx(d.x), rcp_approx(d.y)));
+  }
+  return Elem<T>::pack(O);
+}
+
+struct CtaSync {
+  __device__ __forceinline__ void operator()() const { __syncthreads(); }
+};
 
 template <typename T>
 __global__ void __launch_bounds__(kGnThreads) gn_stats_kernel(const __grid_constant__ GnParams p) {
-  __shared__ double red[2][kGnThreads / 32];
+  __shared__ float red[2 * kGnWarps];
   const int span = p.span0 + blockIdx.y;
   const int piece = blockIdx.x;
   const char* base = p.x + static_cast<long long>(span) * p.span_len * 2;
@@ -94,17 +336,13 @@ __global__ void __launch_bounds__(kGnThreads) gn_stats_kernel(const __grid_const
       }
     }
   }
-  const double s1 = cta_sum(static_cast<double>(a1.x) + static_cast<double>(a1.y), red[0]);
-  const double s2 = cta_sum(static_cast<double>(a2.x) + static_cast<double>(a2.y), red[1]);
+  float s1, s2;
+  piece_sums(a1, a2, red, CtaSync(), &s1, &s2);
   if (threadIdx.x == 0) {
-    double* rec = p.partial + static_cast<long long>(span) * (p.pieces + 1) * 2;
-    rec[2 * piece] = s1;
-    rec[2 * piece + 1] = s2;
-    if (piece == 0) {
-      // the shift, kept here because an in-place apply overwrites x
-      rec[2 * p.pieces] = static_cast<double>(first[0].x);
-      rec[2 * p.pieces + 1] = 0.0;
-    }
+    unsigned long long* rec = p.rec + static_cast<long long>(span) * (p.pieces + 1) * 2;
+    st_record(rec + 2 * piece, tagged(0u, s1), tagged(0u, s2));
+    // the shift, kept here because an in-place apply overwrites x
+    if (piece == 0) st_record(rec + 2 * p.pieces, tagged(0u, first[0].x), tagged(0u, 0.0f));
   }
 }
 
@@ -115,29 +353,15 @@ __global__ void __launch_bounds__(kGnThreads) gn_apply_kernel(const __grid_const
   const int piece = blockIdx.x;
   const char* base = p.x + static_cast<long long>(span) * p.span_len * 2;
   char* obase = p.out + static_cast<long long>(span) * p.span_len * 2;
-  if (threadIdx.x == 0) {
-    const double* rec = p.partial + static_cast<long long>(span) * (p.pieces + 1) * 2;
-    double s1 = 0.0, s2 = 0.0;
-    for (int i = 0; i < p.pieces; ++i) {
-      s1 += rec[2 * i];
-      s2 += rec[2 * i + 1];
-    }
-    const double inv_l = 1.0 / static_cast<double>(p.span_len);
-    const double m1 = s1 * inv_l;
-    double var = s2 * inv_l - m1 * m1;
-    var = var > 0.0 ? var : 0.0;
-    coef[0] = static_cast<float>(rec[2 * p.pieces] + m1);
-    coef[1] = static_cast<float>(1.0 / sqrt(var + static_cast<double>(p.eps)));
-  }
+  if (threadIdx.x < 32)
+    combine_span<false>(p.rec + static_cast<long long>(span) * (p.pieces + 1) * 2, p.pieces, p.span_len, p.eps,
+                        nullptr, coef);
   __syncthreads();
   const float mean = coef[0], rstd = coef[1];
-  const int g = span % p.groups;
+  const int ch0 = (span % p.groups) * p.group_channels;
   const long long lo = static_cast<long long>(piece) * p.piece_len;
   long long hi = lo + p.piece_len;
   if (hi > p.span_len) hi = p.span_len;
-  // channel of the current chunk (a 16-byte chunk never straddles a
-  // channel: H*W is a multiple of 8), refreshed only when a chunk crosses
-  // into the next channel, with its folded coefficients a and b
   long long ch_end = -1;
   float2 A = make_float2(0.0f, 0.0f), B = make_float2(0.0f, 0.0f);
   constexpr long long kStride = kGnThreads * 8;
@@ -155,22 +379,418 @@ __global__ void __launch_bounds__(kGnThreads) gn_apply_kernel(const __grid_const
       const long long e = e0 + b * kStride;
       if (e >= hi) break;
       if (e >= ch_end) {
-        const long long cl = e / p.hw;
-        ch_end = (cl + 1) * p.hw;
-        const int c = g * p.group_channels + static_cast<int>(cl);
-        const float a = __fmul_rn(__ldg(p.gamma + c), rstd);
-        const float bb = __fmaf_rn(-mean, a, __ldg(p.beta + c));
-        A = make_float2(a, a);
-        B = make_float2(bb, bb);
+        const unsigned cl = channel_of(e, p.hw);
+        ch_end = (static_cast<long long>(cl) + 1) * p.hw;
+        fold_channel(__ldg(p.gamma + ch0 + cl), __ldg(p.beta + ch0 + cl), mean, rstd, A, B);
       }
-      float2 X[4], O[4];
-      Elem<T>::unpack(v[b], X);
+      store16(obase + e * 2, silu_affine<T>(v[b], A, B));
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// One-launch group norm + SiLU: x read once.
+//
+// The N*G spans are cut into chunks of kGnfChunk elements (the last chunk
+// of a span may be short); chunk j = span*P + piece.  A persistent CTA per
+// SM takes chunks blockIdx.x, blockIdx.x + grid, ... in order, with four
+// roles working at once:
+//   producer lane: bulk-copies each chunk, and its span's first 16 bytes
+//       (K), into a ring of kGnfSlots shared-memory slots;
+//   eight stats warps: for each chunk, its sums from shared memory (the
+//       same per-thread order and reduction as gn_stats_kernel with
+//       kGnfChunk-element pieces), stored as the chunk's tagged record (and
+//       K's, for piece 0);
+//   kGnfCombiners combiner warps: the CTA's spans in turn (span k to warp
+//       k % kGnfCombiners); once this CTA's stats warps have recorded their
+//       last chunk of the span (so the other CTAs' records are due too),
+//       poll its records and combine them with combine_span into a ring of
+//       kGnfCoefSlots coefficient pairs;
+//   twelve apply warps: for each chunk, once its span's coefficients are
+//       in, silu(x*a + b) from the staged chunk (gamma and beta staged in
+//       shared memory when C <= kGnfMaxSmemChannels).
+// A slot goes back to the producer when both the stats and the apply warps
+// are done with it.  The results equal the two-pass path's with
+// kGnfChunk-element pieces bit for bit.
+//
+// No CTA can wait forever for another: the grid is co-resident (a
+// cooperative launch) and a CTA holds at most ceil(P / grid) <= kGnfSlots
+// chunks of any span (checked by the host).  Then the lowest unfinished
+// span always has all its chunks loaded and recorded: a CTA whose stats
+// warps wait for a slot has its apply warps at a chunk kGnfSlots earlier,
+// which cannot be in that span.  Every wait is bounded all the same: a wait
+// that runs out writes QKNR_ERR_TIMEOUT to *status and sets the
+// workspace's abort word to the tag, which the other CTAs' waits watch;
+// every warp then leaves its loop, and the producer waits (bounded) for its
+// copies in flight before its CTA exits.
+//
+// In place (out == x) is safe: a chunk is written only after its span's
+// records are all in, i.e. after every chunk of the span, the one whose K
+// the others copied among them, has been loaded.
+
+constexpr int kGnfStatsWarps = kGnWarps;             // 8: the reduction of gn_stats_kernel
+constexpr int kGnfStatsThreads = 32 * kGnfStatsWarps;
+constexpr int kGnfApplyWarps = 12;
+constexpr int kGnfApplyWarp0 = kGnfStatsWarps;
+constexpr int kGnfProducerWarp = kGnfApplyWarp0 + kGnfApplyWarps;
+constexpr int kGnfCombiners = 4;
+constexpr int kGnfCombinerWarp0 = kGnfProducerWarp + 1;
+constexpr int kGnfThreads = 32 * (kGnfCombinerWarp0 + kGnfCombiners);
+constexpr int kGnfChunk = 12288;                     // elements per chunk
+constexpr int kGnfChunkBytes = kGnfChunk * 2;
+constexpr int kGnfStatsVec = kGnfChunk / 8 / kGnfStatsThreads;       // 16-byte vectors per stats thread
+constexpr int kGnfApplyVec = kGnfChunk / 8 / (32 * kGnfApplyWarps);   // ... per apply thread
+static_assert(kGnfChunk / 8 == kGnfStatsVec * kGnfStatsThreads, "stats warps cover a chunk");
+static_assert(kGnfChunk / 8 == kGnfApplyVec * 32 * kGnfApplyWarps, "apply warps cover a chunk");
+static_assert(kGnfStatsVec <= kGnBatch, "one batch of gn_stats_kernel covers a chunk (same order)");
+constexpr int kGnfSlots = 8;
+constexpr int kGnfCoefSlots = 8;
+// dynamic shared memory map (bytes)
+constexpr int kGnfOffFull = 0;                       // full[kGnfSlots]
+constexpr int kGnfOffEmpty = 128;                    // empty[kGnfSlots]
+constexpr int kGnfOffCoefFull = 256;                 // coef_full[kGnfCoefSlots]
+constexpr int kGnfOffCoefEmpty = 320;                // coef_empty[kGnfCoefSlots]
+constexpr int kGnfOffAbort = 384;
+constexpr int kGnfOffStatsDone = 388;                // chunks this CTA's stats warps have recorded
+constexpr int kGnfOffK = 512;                        // [kGnfSlots][16 bytes]: the span's first 16 bytes
+constexpr int kGnfOffRed = 768;                      // [2 * kGnWarps] floats
+constexpr int kGnfOffCoef = 896;                     // [kGnfCoefSlots][mean, rstd]
+constexpr int kGnfOffSlot0 = 1024;
+constexpr int kGnfOffGammaBeta = kGnfOffSlot0 + kGnfSlots * kGnfChunkBytes;   // gamma[C], beta[C]
+constexpr int kGnfMaxSmemChannels = 2048;            // larger C reads gamma / beta from global memory
+constexpr int kGnfSmemBytes = kGnfOffGammaBeta + 8 * kGnfMaxSmemChannels;
+constexpr unsigned kGnfFlagStallLoads = 0x1u;        // test: issue no copies
+constexpr unsigned kGnfFlagStallRecords = 0x2u;      // test: write no record
+static_assert(kGnfOffK + 16 * kGnfSlots <= kGnfOffRed, "shared memory map");
+static_assert(kGnfOffCoef + 8 * kGnfCoefSlots <= kGnfOffSlot0, "shared memory map");
+
+struct GnFusedParams {
+  const char* x;
+  char* out;
+  const float* gamma;
+  const float* beta;
+  unsigned long long* rec;     // [spans][P + 1][2] tagged words
+  unsigned* abort_word;        // == tag once a CTA has given up
+  int* status;                 // optional
+  long long span_len;          // L
+  long long hw;                // H * W (a multiple of 8)
+  unsigned pieces;             // P = ceil(L / kGnfChunk)
+  unsigned total_chunks;       // spans * P
+  int groups;
+  int group_channels;
+  int channels;                // C; gamma and beta are staged in shared memory when <= kGnfMaxSmemChannels
+  unsigned tag;                // this call's record tag (nonzero)
+  unsigned flags;
+  unsigned long long wait_limit_ns;
+  float eps;
+};
+
+// (span, piece) of a CTA's chunks blockIdx.x, blockIdx.x + G, ..., kept as
+// a running quotient and remainder of the chunk index by P
+struct ChunkPos {
+  unsigned span, piece;
+  __device__ __forceinline__ void init(unsigned j, unsigned P) {
+    span = j / P;
+    piece = j - span * P;
+  }
+  __device__ __forceinline__ void advance(unsigned G, unsigned P) {
+    piece += G;
+    if (piece >= P) {
+      const unsigned q = piece / P;
+      span += q;
+      piece -= q * P;
+    }
+  }
+};
+
+__device__ __forceinline__ void gnf_stats_barrier() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kGnfStatsThreads) : "memory");
+}
+
+struct GnfStatsSync {
+  __device__ __forceinline__ void operator()() const { gnf_stats_barrier(); }
+};
+
+// bar.sync over the stats warps that also returns whether `pred` held in all
+__device__ __forceinline__ bool gnf_stats_barrier_and(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, 1, %2, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "n"(kGnfStatsThreads)
+      : "memory");
+  return r != 0;
+}
+
+// one lane's bounded mbarrier wait, its result given to the whole warp
+__device__ __forceinline__ bool gnf_warp_wait(uint32_t bar, uint32_t parity, unsigned long long limit,
+                                              volatile int* abort_cta, int* status) {
+  bool ok = true;
+  if ((threadIdx.x & 31) == 0) ok = mbar_try_wait(bar, parity) || bounded_wait(bar, parity, limit, abort_cta, status);
+  return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+}
+
+// one lane waits (bounded, sleeping) until the shared word reaches `target`;
+// the result goes to the whole warp
+static __device__ __noinline__ bool gnf_wait_local(const volatile unsigned* word, unsigned target,
+                                                   const RecordWait& w) {
+  bool ok = true;
+  if ((threadIdx.x & 31) == 0 && *word < target) {
+    const unsigned long long t0 = global_timer_ns();
+    while (*word < target) {
+      if (grid_aborted(w)) {
+        ok = false;
+        break;
+      }
+      if (global_timer_ns() - t0 > w.limit_ns) {
+        give_up(w);
+        ok = false;
+        break;
+      }
+      __nanosleep(256);
+    }
+  }
+  return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kGnfThreads, 1) gn_fused_kernel(const __grid_constant__ GnFusedParams p) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t base = smem_addr(smem);
+  const uint32_t full0 = base + kGnfOffFull;
+  const uint32_t empty0 = base + kGnfOffEmpty;
+  const uint32_t cfull0 = base + kGnfOffCoefFull;
+  const uint32_t cempty0 = base + kGnfOffCoefEmpty;
+  volatile int* abort_cta = reinterpret_cast<volatile int*>(smem + kGnfOffAbort);
+  volatile unsigned* stats_done = reinterpret_cast<volatile unsigned*>(smem + kGnfOffStatsDone);
+  float* coef = reinterpret_cast<float*>(smem + kGnfOffCoef);
+  const unsigned G = gridDim.x;
+  const unsigned mine = (p.total_chunks - blockIdx.x + G - 1) / G;    // grid <= total_chunks
+  const unsigned P = p.pieces;
+  const unsigned long long limit = p.wait_limit_ns;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kGnfSlots; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, kGnfStatsWarps + kGnfApplyWarps);
+    }
+    for (int s = 0; s < kGnfCoefSlots; ++s) {
+      mbar_init(cfull0 + 8 * s, 1);
+      mbar_init(cempty0 + 8 * s, kGnfApplyWarps);
+    }
+    *abort_cta = 0;
+    *stats_done = 0;
+    fence_barrier_init();
+  }
+  const bool gb_smem = p.channels <= kGnfMaxSmemChannels;
+  float* sgamma = reinterpret_cast<float*>(smem + kGnfOffGammaBeta);
+  float* sbeta = sgamma + kGnfMaxSmemChannels;
+  if (gb_smem) {
+    for (int c = threadIdx.x; c < p.channels; c += blockDim.x) {
+      sgamma[c] = __ldg(p.gamma + c);
+      sbeta[c] = __ldg(p.beta + c);
+    }
+  }
+  __syncthreads();
+
+  ChunkPos pos;
+  pos.init(blockIdx.x, P);
+
+  if (warp == kGnfProducerWarp) {
+    // ---------------- producer: one lane; per chunk a bulk copy of the chunk
+    // and one of its span's first 16 bytes, both counted on the slot's barrier
+    if (lane != 0) return;
+    unsigned issued = 0;
+    bool ok = true;
+    int s = 0;
+    uint32_t ph = 0;
+    for (unsigned t = 0; t < mine; ++t, pos.advance(G, P)) {
+      const uint32_t empty = empty0 + 8 * s;
+      if (!mbar_try_wait(empty, ph ^ 1u) && !bounded_wait(empty, ph ^ 1u, limit, abort_cta, p.status)) {
+        ok = false;
+        break;
+      }
+      if (*abort_cta) {
+        ok = false;
+        break;
+      }
+      if (p.flags & kGnfFlagStallLoads) break;
+      const long long lo = static_cast<long long>(pos.piece) * kGnfChunk;
+      const long long rest = p.span_len - lo;
+      const uint32_t bytes = static_cast<uint32_t>(rest < kGnfChunk ? rest : kGnfChunk) * 2u;
+      const uint32_t full = full0 + 8 * s;
+      const char* span_x = p.x + static_cast<long long>(pos.span) * p.span_len * 2;
+      mbar_arrive_expect_tx(full, bytes + 16u);
+      bulk_load(base + kGnfOffSlot0 + s * kGnfChunkBytes, span_x + lo * 2, bytes, full);
+      bulk_load(base + kGnfOffK + 16 * s, span_x, 16u, full);
+      ++issued;
+      if (++s == kGnfSlots) {
+        s = 0;
+        ph ^= 1u;
+      }
+    }
+    if (!ok || *abort_cta) {
+      // wait (bounded) for the copies of the latest use of every slot
+      const unsigned first = issued > kGnfSlots ? issued - kGnfSlots : 0;
+      for (unsigned it = first; it < issued; ++it) {
+        const uint32_t bar = full0 + 8 * (it % kGnfSlots);
+        const uint32_t phase = (it / kGnfSlots) & 1u;
+        const unsigned long long t0 = global_timer_ns();
+        while (!mbar_try_wait(bar, phase) && global_timer_ns() - t0 < limit) {
+        }
+      }
+    }
+    return;
+  }
+
+  if (warp >= kGnfCombinerWarp0) {
+    // ---------------- combiners: the coefficients of the CTA's spans
+    const int c = warp - kGnfCombinerWarp0;
+    const RecordWait rw{p.tag, limit, abort_cta, p.abort_word, p.status};
+    unsigned k = 0;                                  // the CTA's k-th span
+    for (unsigned t = 0; t < mine;) {
+      // this CTA's chunks of the span: t .. t_end - 1
+      const unsigned span = pos.span;
+      unsigned t_end = t;
+      while (t_end < mine && pos.span == span) {
+        ++t_end;
+        pos.advance(G, P);
+      }
+      t = t_end;
+      const unsigned kk = k++;
+      if (kk % kGnfCombiners != static_cast<unsigned>(c)) continue;
+      const int e = static_cast<int>(kk % kGnfCoefSlots);
+      const uint32_t use_parity = (kk / kGnfCoefSlots) & 1u;
+      if (!gnf_warp_wait(cempty0 + 8 * e, use_parity ^ 1u, limit, abort_cta, p.status)) break;
+      if (!gnf_wait_local(stats_done, t_end, rw)) break;
+      if (!combine_span<true>(p.rec + static_cast<long long>(span) * (P + 1) * 2, static_cast<int>(P), p.span_len,
+                              p.eps, &rw, coef + 2 * e))
+        break;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(cfull0 + 8 * e);    // release: the coefficients are visible
+    }
+    return;
+  }
+
+  if (warp >= kGnfApplyWarp0) {
+    // ---------------- apply warps: each on its own, no barrier among them
+    const int at = (warp - kGnfApplyWarp0) * 32 + lane;
+    unsigned cached_span = 0xffffffffu;
+    unsigned nspans = 0;
+    int ch0 = 0;
+    float mean = 0.0f, rstd = 0.0f;
+    int s = 0;
+    uint32_t ph = 0;
+    for (unsigned u = 0; u < mine; ++u, pos.advance(G, P)) {
+      const unsigned span = pos.span;
+      if (span != cached_span) {
+        // hand back the previous span's coefficients (held in registers),
+        // then take this span's
+        if (nspans > 0) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(cempty0 + 8 * ((nspans - 1) % kGnfCoefSlots));
+        }
+        const int e = static_cast<int>(nspans % kGnfCoefSlots);
+        if (!gnf_warp_wait(cfull0 + 8 * e, (nspans / kGnfCoefSlots) & 1u, limit, abort_cta, p.status)) break;
+        mean = coef[2 * e];
+        rstd = coef[2 * e + 1];
+        ch0 = static_cast<int>(span % static_cast<unsigned>(p.groups)) * p.group_channels;
+        cached_span = span;
+        ++nspans;
+      }
+      if (!gnf_warp_wait(full0 + 8 * s, ph, limit, abort_cta, p.status)) break;
+      const long long lo = static_cast<long long>(pos.piece) * kGnfChunk;
+      const long long rest = p.span_len - lo;
+      const int nvec = static_cast<int>(rest < kGnfChunk ? rest : kGnfChunk) / 8;
+      char* obase = p.out + (static_cast<long long>(span) * p.span_len + lo) * 2;
+      const unsigned char* slot = smem + kGnfOffSlot0 + s * kGnfChunkBytes;
+      long long ch_end = -1;
+      float2 A = make_float2(0.0f, 0.0f), B = make_float2(0.0f, 0.0f);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float2 y = __ffma2_rn(X[j], A, B);
-        O[j] = make_float2(__fdividef(y.x, 1.0f + __expf(-y.x)), __fdividef(y.y, 1.0f + __expf(-y.y)));
+      for (int b = 0; b < kGnfApplyVec; ++b) {
+        const int v = at + b * 32 * kGnfApplyWarps;
+        if (v < nvec) {
+          const uint4 raw = *reinterpret_cast<const uint4*>(slot + v * 16);
+          const long long e = lo + v * 8;
+          if (e >= ch_end) {
+            const unsigned cl = channel_of(e, p.hw);
+            ch_end = (static_cast<long long>(cl) + 1) * p.hw;
+            const int ch = ch0 + static_cast<int>(cl);
+            fold_channel(gb_smem ? sgamma[ch] : __ldg(p.gamma + ch), gb_smem ? sbeta[ch] : __ldg(p.beta + ch), mean,
+                         rstd, A, B);
+          }
+          store16(obase + v * 16, silu_affine<T>(raw, A, B));
+        }
       }
-      store16(obase + e * 2, Elem<T>::pack(O));
+      // the slot has been read for the last time by this warp
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty0 + 8 * s);
+      if (++s == kGnfSlots) {
+        s = 0;
+        ph ^= 1u;
+      }
+    }
+    return;
+  }
+
+  // ---------------- stats warps
+  const int tid = threadIdx.x;                       // 0 .. kGnfStatsThreads - 1
+  float* red = reinterpret_cast<float*>(smem + kGnfOffRed);
+  int s = 0;
+  uint32_t ph = 0;
+  for (unsigned t = 0; t < mine; ++t, pos.advance(G, P)) {
+    const bool got = mbar_try_wait(full0 + 8 * s, ph) || bounded_wait(full0 + 8 * s, ph, limit, abort_cta, p.status);
+    if (!gnf_stats_barrier_and(got)) {
+      if (tid == 0) atomicExch(p.abort_word, p.tag);
+      break;                                         // every stats warp leaves together
+    }
+    const unsigned span = pos.span, piece = pos.piece;
+    const long long lo = static_cast<long long>(piece) * kGnfChunk;
+    const long long rest = p.span_len - lo;
+    const int nvec = static_cast<int>(rest < kGnfChunk ? rest : kGnfChunk) / 8;
+    float2 first[4];
+    Elem<T>::unpack(*reinterpret_cast<const uint4*>(smem + kGnfOffK + 16 * s), first);
+    const float2 nk = make_float2(-first[0].x, -first[0].x);
+    const unsigned char* slot = smem + kGnfOffSlot0 + s * kGnfChunkBytes;
+    float2 a1 = make_float2(0.0f, 0.0f), a2 = make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int b = 0; b < kGnfStatsVec; ++b) {
+      const int v = tid + b * kGnfStatsThreads;
+      if (v < nvec) {
+        float2 X[4];
+        Elem<T>::unpack(*reinterpret_cast<const uint4*>(slot + v * 16), X);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float2 d = __fadd2_rn(X[q], nk);
+          a1 = __fadd2_rn(a1, d);
+          a2 = __ffma2_rn(d, d, a2);
+        }
+      }
+    }
+    // this warp has read the slot for the last time
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty0 + 8 * s);
+    float s1, s2;
+    piece_sums(a1, a2, red, GnfStatsSync(), &s1, &s2);
+    if (tid == 0) {
+      if (!(p.flags & kGnfFlagStallRecords)) {
+        unsigned long long* rec = p.rec + static_cast<long long>(span) * (P + 1) * 2;
+        st_record(rec + 2 * piece, tagged(p.tag, s1), tagged(p.tag, s2));
+        if (piece == 0) st_record(rec + 2 * P, tagged(p.tag, first[0].x), tagged(p.tag, 0.0f));
+      }
+      *stats_done = t + 1;
+    }
+    // red[] is rewritten by the next chunk only after every stats warp has
+    // passed that chunk's first barrier, which thread 0 reaches after
+    // reading it here
+    if (++s == kGnfSlots) {
+      s = 0;
+      ph ^= 1u;
     }
   }
 }

@@ -57,6 +57,8 @@ qknr_status device_info(int dev, DeviceInfo* out) {
   if ((e = cudaDeviceGetAttribute(&d.smem_reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev)) !=
       cudaSuccess)
     return cuda_fail(e, "cudaDeviceGetAttribute(ReservedSharedMemoryPerBlock)");
+  if ((e = cudaDeviceGetAttribute(&d.cooperative, cudaDevAttrCooperativeLaunch, dev)) != cudaSuccess)
+    return cuda_fail(e, "cudaDeviceGetAttribute(CooperativeLaunch)");
   g_dev[dev] = d;
   *out = d;
   return QKNR_OK;

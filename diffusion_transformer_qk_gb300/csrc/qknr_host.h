@@ -21,6 +21,7 @@ struct DeviceInfo {
   int smem_optin = 0;       // max dynamic shared memory per block (opt-in)
   int smem_per_sm = 0;
   int smem_reserved = 0;    // per-block reservation
+  int cooperative = 0;      // cooperative launches supported
 };
 
 // Attributes of device `dev`, queried once and cached.

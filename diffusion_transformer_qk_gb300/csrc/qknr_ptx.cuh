@@ -49,6 +49,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// The same test, but a thread whose phase is not complete is suspended
+// (issuing nothing) until it completes or about `hint_ns` have passed.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 __device__ __forceinline__ unsigned long long global_timer_ns() {
   unsigned long long t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -71,15 +85,15 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 
 // Wait for phase `parity` of `bar` to complete, giving up at the deadline
 // or when another warp of the CTA has aborted.  Returns false on give-up.
+// The waiting thread sleeps in the barrier (20 us at a time) instead of
+// spinning, so waiters leave the issue slots to the warps doing work.
 static __device__ __noinline__ bool bounded_wait(uint32_t bar, uint32_t parity,
                                           unsigned long long limit_ns, volatile int* abort_flag,
                                           int* status) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_timer_ns();
   while (true) {
-#pragma unroll 1
-    for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
     if (*abort_flag) return false;
     if (global_timer_ns() - t0 > limit_ns) {
       *abort_flag = 1;

@@ -31,15 +31,17 @@ STATUS = {
 }
 OK, ERR_TIMEOUT = 0, 6
 FLAG_TEST_STALL = 0x1
-ABI_VERSION = 1
+ABI_VERSION = 2
 
 EXPORTS = (
     "qknr_args_init", "qknr_forward", "qknr_query", "qknr_status_string",
     "qknr_last_error", "qknr_abi_version", "qknr_sizeof_args", "qknr_sizeof_launch_info",
     "qknr_adaln_args_init", "qknr_adaln_forward", "qknr_adaln_query", "qknr_adaln_sizeof_args",
     "qknr_gn_args_init", "qknr_gn_workspace_bytes", "qknr_gn_silu_forward", "qknr_gn_sizeof_args",
-    "qknr_gn_silu_forward_noalloc",
+    "qknr_gn_silu_forward_noalloc", "qknr_gn_query",
 )
+GN_MODE = {"auto": 0, "fused": 1, "two_pass": 2}
+GN_FLAG_TEST_NO_RECORDS = 0x2
 GN_NOALLOC_SCRATCH_BYTES = 1 << 20
 
 
@@ -106,6 +108,7 @@ class QknrGnArgs(ctypes.Structure):
         ("gamma", c_void_p), ("beta", c_void_p), ("eps", c_float),
         ("workspace", c_void_p), ("workspace_bytes", c_size_t),
         ("piece_elems", c_int32), ("l2_batch_bytes", c_int64),
+        ("dev_status", c_void_p), ("mode", c_int32), ("flags", c_uint32), ("wait_limit_ns", c_uint64),
     ]
 
 
@@ -164,6 +167,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         lib.qknr_gn_sizeof_args.restype = c_size_t
         lib.qknr_gn_silu_forward_noalloc.argtypes = [ctypes.POINTER(QknrGnArgs), c_void_p]
         lib.qknr_gn_silu_forward_noalloc.restype = c_int32
+        lib.qknr_gn_query.argtypes = [ctypes.POINTER(QknrGnArgs), ctypes.POINTER(QknrLaunchInfo)]
+        lib.qknr_gn_query.restype = c_int32
         if lib.qknr_abi_version() != ABI_VERSION:
             raise RuntimeError("libqknr.so ABI version mismatch")
         if lib.qknr_sizeof_args() != ctypes.sizeof(QknrArgs) or \
@@ -564,7 +569,7 @@ def adaln_modulate(x, scale, shift, *, rows_per_batch=None, out=None, stream=Non
 # group norm + SiLU (include/qknr_gn.h)
 
 def gn_args(x, groups, gamma, beta, *, out=None, eps=1e-6, workspace=None, piece_elems=0,
-            l2_batch_bytes=0) -> QknrGnArgs:
+            l2_batch_bytes=0, mode="auto", dev_status=None, flags=0, wait_limit_ns=0) -> QknrGnArgs:
     """Arguments for ``silu(group_norm(x))`` on an NCHW tensor ``x``."""
     if x.dim() != 4 or not x.is_contiguous() or not x.is_cuda or x.dtype not in _ACT:
         raise ValueError("x must be a contiguous 4-D (NCHW) bfloat16/float16 CUDA tensor")
@@ -584,9 +589,22 @@ def gn_args(x, groups, gamma, beta, *, out=None, eps=1e-6, workspace=None, piece
     a.gamma, a.beta = gamma.data_ptr(), beta.data_ptr()
     a.eps = eps
     a.piece_elems, a.l2_batch_bytes = piece_elems, l2_batch_bytes
+    a.mode = GN_MODE[mode]
+    a.dev_status = _ptr(dev_status)
+    a.flags, a.wait_limit_ns = flags, wait_limit_ns
     if workspace is not None:
         a.workspace, a.workspace_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
     return a
+
+
+def gn_query(a: QknrGnArgs) -> dict:
+    """qknr_gn_query: the path and launch qknr_gn_silu_forward would take."""
+    lib = load()
+    info = QknrLaunchInfo()
+    st = lib.qknr_gn_query(ctypes.byref(a), ctypes.byref(info))
+    if st != OK:
+        raise QknrError(st, lib.qknr_last_error().decode())
+    return info.as_dict()
 
 
 def gn_workspace_bytes(a: QknrGnArgs) -> int:
@@ -606,10 +624,12 @@ def gn_launch(a: QknrGnArgs, stream: Optional[torch.cuda.Stream] = None) -> None
         raise QknrError(st, lib.qknr_last_error().decode())
 
 
-def group_norm_silu(x, groups, gamma, beta, *, out=None, workspace=None, stream=None, **kw):
+def group_norm_silu(x, groups, gamma, beta, *, out=None, workspace=None, stream=None, status=True, **kw):
     """silu(group_norm(x)) on NCHW ``x``; in place unless ``out`` is given.
     ``workspace`` (a CUDA tensor of at least gn_workspace_bytes) is created
     by this binding when not given."""
+    if status and "dev_status" not in kw:
+        kw["dev_status"] = status_buffer(x.device)
     a = gn_args(x, groups, gamma, beta, out=out, **kw)
     if workspace is None:
         workspace = torch.empty(gn_workspace_bytes(a), dtype=torch.uint8, device=x.device)

@@ -46,7 +46,7 @@ extern "C" {
 struct CUstream_st;
 typedef struct CUstream_st *qknr_stream_t;
 
-#define QKNR_ABI_VERSION 1
+#define QKNR_ABI_VERSION 2
 
 typedef enum {
   QKNR_BF16 = 0, /* activations or cos/sin */

@@ -12,14 +12,27 @@
  *
  * rounded once into the activation dtype.  The statistics are sums around
  * the group's first element K, S1 = sum (x - K), S2 = sum (x - K)^2, taken
- * per piece in fp32 and combined in fp64: mean = K + S1/L, var = S2/L -
- * (S1/L)^2.
+ * per piece in fp32 and combined in compensated fp32 (about twice fp32's
+ * precision): mean = K + S1/L, var = S2/L - (S1/L)^2.
  *
  * A group is large and there are few of them, so each is cut into pieces
- * and the call runs two stream-ordered kernels (piece statistics into a
- * caller-provided device workspace, then the normalise + SiLU pass), once
- * for all groups or once per batch of groups.  No kernel waits for another
- * CTA.
+ * whose statistics go to a caller-provided device workspace.  Two paths:
+ *
+ *   fused (QKNR_GN_FUSED): one persistent cooperative launch, one CTA per
+ *     SM, that reads x once.  Each 12288-element piece is kept in shared
+ *     memory from its statistics to its normalise + SiLU pass; CTAs publish
+ *     piece statistics through the workspace, tagged with a value unique to
+ *     the call (so the workspace needs no clearing), and wait (bounded) for
+ *     the other pieces of a group.  Needs cooperative launch support and
+ *     groups of at most 8 * SMs pieces (14.9 M elements on 152 SMs).
+ *   two-pass (QKNR_GN_TWO_PASS): a statistics kernel and a normalise + SiLU
+ *     kernel, once for all groups or once per batch of groups; x is read
+ *     twice.  No CTA waits for another.
+ *
+ * QKNR_GN_AUTO takes the fused path when this device and shape allow it
+ * and piece_elems and l2_batch_bytes are 0 (they tune the two-pass path),
+ * else the two-pass path.  Both give the same bits when the two-pass
+ * pieces are 12288 elements.
  *
  * Ownership and errors follow qknr.h: the caller owns every buffer
  * (activations, gamma, beta and the workspace); the library allocates
@@ -35,6 +48,16 @@
 extern "C" {
 #endif
 
+typedef enum {
+  QKNR_GN_AUTO = 0,
+  QKNR_GN_FUSED = 1,          /* QKNR_ERR_UNSUPPORTED where the fused path cannot run */
+  QKNR_GN_TWO_PASS = 2
+} qknr_gn_mode;
+
+/* test only: the fused path publishes no piece statistics, so every wait
+   for a group's statistics runs out and the call reports QKNR_ERR_TIMEOUT */
+#define QKNR_GN_FLAG_TEST_NO_RECORDS 0x2u
+
 typedef struct qknr_gn_args {
   uint32_t abi_version;       /* QKNR_ABI_VERSION */
   int32_t dtype;              /* QKNR_BF16 or QKNR_FP16 */
@@ -48,17 +71,30 @@ typedef struct qknr_gn_args {
   size_t workspace_bytes;
   int32_t piece_elems;        /* elements per piece (multiple of 8); 0 = about 1024 pieces in all, >= 65536 each */
   int64_t l2_batch_bytes;     /* activation bytes per batch of groups; 0 or -1 = one batch */
+  int32_t *dev_status;        /* optional device int32: the fused path writes QKNR_ERR_TIMEOUT
+                                 here when one of its waits runs out (see qknr.h) */
+  int32_t mode;               /* QKNR_GN_AUTO, QKNR_GN_FUSED or QKNR_GN_TWO_PASS */
+  uint32_t flags;             /* QKNR_FLAG_TEST_STALL, QKNR_GN_FLAG_TEST_NO_RECORDS (tests only) */
+  uint64_t wait_limit_ns;     /* bound of each wait of the fused path; 0 = 2 s */
 } qknr_gn_args;
 
 /* Defaults: bf16, eps 1e-6, automatic pieces and batches, all else zero. */
 void qknr_gn_args_init(qknr_gn_args *a);
 
-/* Device workspace the call needs for these arguments (16 bytes per piece
-   and one more per group of each sample). */
+/* Device workspace the call needs for these arguments: 16 bytes per piece
+   and one more per group of each sample, plus 16 bytes for the fused path
+   (in QKNR_GN_AUTO the larger of the two paths' needs).  Depends on the
+   arguments only, not on the device. */
 qknr_status qknr_gn_workspace_bytes(const qknr_gn_args *args, size_t *bytes);
 
 /* Validate and launch on `stream` (asynchronous). */
 qknr_status qknr_gn_silu_forward(const qknr_gn_args *args, qknr_stream_t stream);
+
+/* Validate and describe the launch without launching: for the fused path
+   the grid, block, shared memory, ring slots (stages) and piece bytes
+   (stage_bytes); for the two-pass path the apply kernel's grid (pieces x
+   groups of a batch) and block.  Queries the current device. */
+qknr_status qknr_gn_query(const qknr_gn_args *args, qknr_launch_info *info);
 
 /* sizeof(qknr_gn_args) as compiled into the library. */
 size_t qknr_gn_sizeof_args(void);
@@ -78,10 +114,11 @@ size_t qknr_gn_sizeof_args(void);
  *
  * The first call on a device looks up the array's device address (with
  * that device current) and caches it; make that first call before any
- * stream capture.  Every call on a device shares the one array and every
- * call writes all the scratch it reads, so nothing needs clearing, but
- * calls whose kernels overlap on the GPU (different streams, no ordering
- * between them) race on it.
+ * stream capture.  Every call on a device shares the one array, and
+ * nothing in it needs clearing: the two-pass path reads only what the same
+ * call wrote, and the fused path accepts only statistics tagged with its
+ * own call's tag.  Calls whose kernels overlap on the GPU (different
+ * streams, no ordering between them) race on the array.
  */
 #define QKNR_GN_NOALLOC_SCRATCH_BYTES (1 << 20)
 qknr_status qknr_gn_silu_forward_noalloc(const qknr_gn_args *args, qknr_stream_t stream);

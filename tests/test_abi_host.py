@@ -244,16 +244,37 @@ def valid_gn():
     return a
 
 
+def gn_ws(lib, a):
+    n = ctypes.c_size_t(0)
+    assert lib.qknr_gn_workspace_bytes(ctypes.byref(a), ctypes.byref(n)) == 0, lib.qknr_last_error()
+    return n.value
+
+
 def test_gn_workspace_bytes(lib):
     a = valid_gn()
-    n = ctypes.c_size_t(0)
-    assert lib.qknr_gn_workspace_bytes(ctypes.byref(a), ctypes.byref(n)) == 0
-    # 32 spans of 2*16*16 = 512 elements: one piece each (pieces are at least
-    # 65536 elements), plus the shift record
-    assert n.value == 32 * 2 * 16
-    a.piece_elems = 64
-    assert lib.qknr_gn_workspace_bytes(ctypes.byref(a), ctypes.byref(n)) == 0
-    assert n.value == 32 * (8 + 1) * 16
+    # 32 spans of 2*16*16 = 512 elements: one piece each on both paths
+    # (two-pass pieces are at least 65536 elements, fused ones 12288), plus
+    # the shift record; the fused path adds 16 bytes (its abort word)
+    a.mode = Q.GN_MODE["two_pass"]
+    assert gn_ws(lib, a) == 32 * 2 * 16
+    a.mode = Q.GN_MODE["fused"]
+    assert gn_ws(lib, a) == 32 * 2 * 16 + 16
+    a.mode = Q.GN_MODE["auto"]                     # the larger of the two
+    assert gn_ws(lib, a) == 32 * 2 * 16 + 16
+    a.piece_elems = 64                             # two-pass tuning: two-pass only
+    assert gn_ws(lib, a) == 32 * (8 + 1) * 16
+    # a group of 2 x 128 x 128 = 32768 elements: 3 fused pieces of 12288
+    a = valid_gn()
+    a.h = a.w = 128
+    a.mode = Q.GN_MODE["fused"]
+    assert gn_ws(lib, a) == 32 * (3 + 1) * 16 + 16
+
+
+def test_gn_workspace_does_not_depend_on_the_device(lib):
+    # no CUDA call is made: the size comes from the arguments alone
+    a = valid_gn()
+    a.x = a.gamma = a.beta = a.workspace = None
+    assert gn_ws(lib, a) > 0
 
 
 @pytest.mark.parametrize("mutate,expect", [
@@ -273,6 +294,8 @@ def test_gn_workspace_bytes(lib):
     (lambda a: setattr(a, "gamma", FAKE + (1 << 30) + 2), 3),
     (lambda a: setattr(a, "out", FAKE + 1024), 7),          # out inside x
     (lambda a: setattr(a, "workspace", FAKE + 4096), 7),    # workspace inside x
+    (lambda a: setattr(a, "mode", 3), 4),
+    (lambda a: setattr(a, "dev_status", FAKE + 3 * (1 << 30) + 2), 3),
 ])
 def test_gn_validation_rejects(lib, mutate, expect):
     a = valid_gn()

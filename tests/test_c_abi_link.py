@@ -61,12 +61,18 @@ int main(void) {
 
   qknr_gn_args_init(&g);
   g.n = 1; g.c = 64; g.h = 16; g.w = 16; g.groups = 32;
+  g.mode = QKNR_GN_TWO_PASS;
   CHECK(qknr_gn_workspace_bytes(&g, &ws) == QKNR_OK && ws == 32 * 2 * 2 * sizeof(double), 40);
+  g.mode = QKNR_GN_AUTO;
+  CHECK(qknr_gn_workspace_bytes(&g, &ws) == QKNR_OK && ws >= 32 * 2 * 2 * sizeof(double), 44);
   g.groups = 3;                                                 /* does not divide C */
   CHECK(qknr_gn_workspace_bytes(&g, &ws) == QKNR_ERR_SHAPE, 41);
   g.groups = 32;
   CHECK(qknr_gn_silu_forward(&g, NULL) == QKNR_ERR_NULL, 42);   /* no x / gamma / beta */
   CHECK(qknr_gn_silu_forward_noalloc(&g, NULL) == QKNR_ERR_NULL, 43);
+  CHECK(qknr_gn_query(&g, NULL) == QKNR_ERR_NULL, 45);
+  g.mode = 7;
+  CHECK(qknr_gn_workspace_bytes(&g, &ws) == QKNR_ERR_UNSUPPORTED, 46);
   printf("ok\n");
   return 0;
 }

@@ -14,6 +14,9 @@ pytestmark = pytest.mark.gpu
 @pytest.fixture(scope="module", autouse=True)
 def _lib(built_lib, cuda_device):
     Q.load()
+    Q.status_buffer().zero_()
+    yield
+    assert Q.read_status() == 0, "a kernel reported a wait timeout"
 
 
 def run(w, inp, out=False, **kw):
@@ -86,8 +89,113 @@ def test_workspace_checks():
     gm = torch.ones(32, device="cuda")
     a = Q.gn_args(x, 8, gm, gm)
     need = Q.gn_workspace_bytes(a)
-    assert need == 8 * (1 + 1) * 16               # 8 spans, 1 piece each, plus the shift record
+    # 8 spans, 1 piece each, plus the shift record; the fused path adds 16
+    # bytes (its abort word)
+    assert need == 8 * (1 + 1) * 16 + 16
     small = torch.empty(need - 16, dtype=torch.uint8, device="cuda")
     with pytest.raises(Q.QknrError) as e:
         Q.group_norm_silu(x, 8, gm, gm, workspace=small)
     assert e.value.status == 2
+
+
+# ---------------------------------------------------------------------------
+# the fused one-launch path
+
+def gn_call(x, w, inp, **kw):
+    return Q.group_norm_silu(x, w.groups, torch.from_numpy(inp["gamma"]).cuda(),
+                             torch.from_numpy(inp["beta"]).cuda(), eps=w.eps, **kw)
+
+
+def query(w, **kw):
+    x = torch.empty((w.n, w.c, w.h, w.w), dtype=torch.bfloat16 if w.dtype == "bf16" else torch.float16,
+                    device="cuda")
+    g = torch.ones(w.c, device="cuda")
+    return Q.gn_query(Q.gn_args(x, w.groups, g, g, **kw))
+
+
+@pytest.mark.parametrize("name", list(I.GN_WORKLOADS))
+def test_vae_shapes_take_the_fused_path(name):
+    info = query(I.GN_WORKLOADS[name])
+    assert info["kernel"].startswith("gn_fused<bf16>"), info
+    assert info["grid"] == info["num_sms"] and info["block"] == 800 and info["stages"] == 8
+    two = query(I.GN_WORKLOADS[name], mode="two_pass")
+    assert two["kernel"].startswith("gn_stats+gn_apply"), two
+
+
+@pytest.mark.parametrize("shape,groups", [((2, 64, 16, 16), 32), ((1, 32, 8, 8), 8), ((3, 12, 4, 6), 3),
+                                          ((2, 4, 2, 4), 1), ((1, 512, 64, 64), 32), ((2, 96, 40, 72), 32),
+                                          ((1, 8, 100, 104), 2), ((1, 128, 256, 256), 32)])
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_fused_equals_two_pass_with_the_same_pieces(shape, groups, dtype):
+    # same per-thread order, same CTA reduction, same combine: the same bits
+    w = I.GroupNormWorkload("f", *shape, groups=groups, dtype=dtype, scale=1.7, offset=-0.4, seed=sum(shape) + 1)
+    inp = I.make_gn_inputs(w)
+    a = gn_call(to_dev(inp["x"], dtype), w, inp, mode="fused")
+    b = gn_call(to_dev(inp["x"], dtype), w, inp, mode="two_pass", piece_elems=12288)
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    if w.elements <= 1 << 20:
+        ref = G.group_norm_silu(inp["x"], dtype, groups, inp["gamma"], inp["beta"], w.eps)
+        compare(to_bits(a), ref, dtype, "fused")
+
+
+def test_fused_in_place_equals_out_of_place_and_repeats():
+    w = I.GroupNormWorkload("ip", 2, 64, 96, 96, groups=32, scale=2.0, seed=41)
+    inp = I.make_gn_inputs(w)
+    src = to_dev(inp["x"], "bf16")
+    out = torch.empty_like(src)
+    gn_call(src, w, inp, out=out, mode="fused")
+    for _ in range(3):                                  # the counters start at zero on every call
+        x = to_dev(inp["x"], "bf16")
+        gn_call(x, w, inp, mode="fused")
+        torch.cuda.synchronize()
+        assert torch.equal(x.view(torch.int16), out.view(torch.int16))
+    np.testing.assert_array_equal(to_bits(src), inp["x"])
+
+
+@pytest.mark.parametrize("shape,per_cta", [((1, 1, 2880, 2800), 5), ((1, 3, 2048, 2000), 7),
+                                           ((1, 2, 2720, 2700), 8)])
+def test_fused_large_groups(shape, per_cta):
+    # 657, 1000 and 1196 pieces of 12288 elements per group over 152 CTAs;
+    # at most 8 per CTA
+    w = I.GroupNormWorkload("big", *shape, groups=1, scale=1.2, offset=0.7, seed=43)
+    info = query(w)
+    assert info["kernel"].startswith("gn_fused") and info["kernel"].endswith(f" {per_cta} per CTA"), info
+    inp = I.make_gn_inputs(w)
+    res = gn_call(to_dev(inp["x"], "bf16"), w, inp)
+    torch.cuda.synchronize()
+    got = to_bits(res)
+    g = np.random.Generator(np.random.PCG64(8))
+    idx = tuple(g.integers(0, s, 3000) for s in (w.n, w.c, w.h, w.w))
+    ref = G.group_norm_silu_at(inp["x"], w.dtype, w.groups, inp["gamma"], inp["beta"], w.eps, idx)
+    compare(got[idx], ref, w.dtype, "large group")
+
+
+def test_groups_beyond_the_fused_limit_fall_back_to_two_pass():
+    # 1366 pieces per group: 9 per CTA, more than the 8 ring slots
+    w = I.GroupNormWorkload("huge", 1, 1, 4096, 4096, groups=1, seed=44)
+    assert query(w)["kernel"].startswith("gn_stats+gn_apply")
+    x = torch.zeros((1, 1, 4096, 4096), dtype=torch.bfloat16, device="cuda")
+    g = torch.ones(1, device="cuda")
+    with pytest.raises(Q.QknrError) as e:
+        Q.group_norm_silu(x, 1, g, g, mode="fused")
+    assert e.value.status == 4 and "per CTA" in str(e.value)
+
+
+@pytest.mark.parametrize("flag", [Q.FLAG_TEST_STALL, Q.GN_FLAG_TEST_NO_RECORDS])
+def test_fused_bounded_waits_report_timeout(flag):
+    w = I.GroupNormWorkload("s", 1, 64, 64, 64, groups=32, seed=45)
+    inp = I.make_gn_inputs(w)
+    x = to_dev(inp["x"], "bf16")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gn_call(x, w, inp, mode="fused", dev_status=status, flags=flag, wait_limit_ns=2_000_000)
+    torch.cuda.synchronize()
+    assert int(status.item()) == Q.ERR_TIMEOUT
+    np.testing.assert_array_equal(to_bits(x), inp["x"])   # nothing was written
+    # the context stays usable and the next call starts clean
+    status.zero_()
+    res = gn_call(x, w, inp, mode="fused", dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ref = G.group_norm_silu(inp["x"], "bf16", w.groups, inp["gamma"], inp["beta"], w.eps)
+    compare(to_bits(res), ref, "bf16", "after timeout")
