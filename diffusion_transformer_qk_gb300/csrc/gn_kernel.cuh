@@ -452,6 +452,7 @@ constexpr int kGnfOffCoefFull = 256;                 // coef_full[kGnfCoefSlots]
 constexpr int kGnfOffCoefEmpty = 320;                // coef_empty[kGnfCoefSlots]
 constexpr int kGnfOffAbort = 384;
 constexpr int kGnfOffStatsDone = 388;                // chunks this CTA's stats warps have recorded
+constexpr int kGnfOffMeta = 448;                     // [kGnfSlots][2]: first channel, next channel's first element
 constexpr int kGnfOffK = 512;                        // [kGnfSlots][16 bytes]: the span's first 16 bytes
 constexpr int kGnfOffRed = 768;                      // [2 * kGnWarps] floats
 constexpr int kGnfOffCoef = 896;                     // [kGnfCoefSlots][mean, rstd]
@@ -462,6 +463,7 @@ constexpr int kGnfSmemBytes = kGnfOffGammaBeta + 8 * kGnfMaxSmemChannels;
 constexpr unsigned kGnfFlagStallLoads = 0x1u;        // test: issue no copies
 constexpr unsigned kGnfFlagStallRecords = 0x2u;      // test: write no record
 static_assert(kGnfOffK + 16 * kGnfSlots <= kGnfOffRed, "shared memory map");
+static_assert(kGnfOffMeta + 8 * kGnfSlots <= kGnfOffK, "shared memory map");
 static_assert(kGnfOffCoef + 8 * kGnfCoefSlots <= kGnfOffSlot0, "shared memory map");
 
 struct GnFusedParams {
@@ -525,11 +527,16 @@ __device__ __forceinline__ bool gnf_stats_barrier_and(bool pred) {
   return r != 0;
 }
 
+// a wait's first attempt sleeps in the barrier (most complete within it),
+// skipping the out-of-line bounded_wait unless it runs out
+constexpr uint32_t kGnfSleepNs = 20000;
+
 // one lane's bounded mbarrier wait, its result given to the whole warp
 __device__ __forceinline__ bool gnf_warp_wait(uint32_t bar, uint32_t parity, unsigned long long limit,
                                               volatile int* abort_cta, int* status) {
   bool ok = true;
-  if ((threadIdx.x & 31) == 0) ok = mbar_try_wait(bar, parity) || bounded_wait(bar, parity, limit, abort_cta, status);
+  if ((threadIdx.x & 31) == 0)
+    ok = mbar_try_wait_sleep(bar, parity, kGnfSleepNs) || bounded_wait(bar, parity, limit, abort_cta, status);
   return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
 }
 
@@ -611,7 +618,8 @@ __global__ void __launch_bounds__(kGnfThreads, 1) gn_fused_kernel(const __grid_c
     uint32_t ph = 0;
     for (unsigned t = 0; t < mine; ++t, pos.advance(G, P)) {
       const uint32_t empty = empty0 + 8 * s;
-      if (!mbar_try_wait(empty, ph ^ 1u) && !bounded_wait(empty, ph ^ 1u, limit, abort_cta, p.status)) {
+      if (!mbar_try_wait_sleep(empty, ph ^ 1u, kGnfSleepNs) &&
+          !bounded_wait(empty, ph ^ 1u, limit, abort_cta, p.status)) {
         ok = false;
         break;
       }
@@ -625,6 +633,12 @@ __global__ void __launch_bounds__(kGnfThreads, 1) gn_fused_kernel(const __grid_c
       const uint32_t bytes = static_cast<uint32_t>(rest < kGnfChunk ? rest : kGnfChunk) * 2u;
       const uint32_t full = full0 + 8 * s;
       const char* span_x = p.x + static_cast<long long>(pos.span) * p.span_len * 2;
+      // the chunk's first channel (within the group) and where the next one
+      // starts, for the apply warps; published by the arrive below
+      const unsigned cl = channel_of(lo, p.hw);
+      unsigned* meta = reinterpret_cast<unsigned*>(smem + kGnfOffMeta + 8 * s);
+      meta[0] = cl;
+      meta[1] = (cl + 1u) * static_cast<unsigned>(p.hw);
       mbar_arrive_expect_tx(full, bytes + 16u);
       bulk_load(base + kGnfOffSlot0 + s * kGnfChunkBytes, span_x + lo * 2, bytes, full);
       bulk_load(base + kGnfOffK + 16 * s, span_x, 16u, full);
@@ -704,28 +718,39 @@ __global__ void __launch_bounds__(kGnfThreads, 1) gn_fused_kernel(const __grid_c
         ++nspans;
       }
       if (!gnf_warp_wait(full0 + 8 * s, ph, limit, abort_cta, p.status)) break;
-      const long long lo = static_cast<long long>(pos.piece) * kGnfChunk;
-      const long long rest = p.span_len - lo;
+      const unsigned lo = pos.piece * static_cast<unsigned>(kGnfChunk);     // < L < 2^31
+      const unsigned rest = static_cast<unsigned>(p.span_len) - lo;
       const int nvec = static_cast<int>(rest < kGnfChunk ? rest : kGnfChunk) / 8;
       char* obase = p.out + (static_cast<long long>(span) * p.span_len + lo) * 2;
       const unsigned char* slot = smem + kGnfOffSlot0 + s * kGnfChunkBytes;
-      long long ch_end = -1;
-      float2 A = make_float2(0.0f, 0.0f), B = make_float2(0.0f, 0.0f);
-#pragma unroll
-      for (int b = 0; b < kGnfApplyVec; ++b) {
-        const int v = at + b * 32 * kGnfApplyWarps;
-        if (v < nvec) {
-          const uint4 raw = *reinterpret_cast<const uint4*>(slot + v * 16);
-          const long long e = lo + v * 8;
-          if (e >= ch_end) {
-            const unsigned cl = channel_of(e, p.hw);
-            ch_end = (static_cast<long long>(cl) + 1) * p.hw;
-            const int ch = ch0 + static_cast<int>(cl);
-            fold_channel(gb_smem ? sgamma[ch] : __ldg(p.gamma + ch), gb_smem ? sbeta[ch] : __ldg(p.beta + ch), mean,
-                         rstd, A, B);
-          }
-          store16(obase + v * 16, silu_affine<T>(raw, A, B));
+      const unsigned hw = static_cast<unsigned>(p.hw);
+      const uint2 meta = *reinterpret_cast<const uint2*>(smem + kGnfOffMeta + 8 * s);
+      unsigned ch_end = meta.y;
+      float2 A, B;
+      {
+        const int ch = ch0 + static_cast<int>(meta.x);
+        fold_channel(gb_smem ? sgamma[ch] : __ldg(p.gamma + ch), gb_smem ? sbeta[ch] : __ldg(p.beta + ch), mean, rstd,
+                     A, B);
+      }
+      auto one = [&](int v) {
+        const uint4 raw = *reinterpret_cast<const uint4*>(slot + v * 16);
+        const unsigned e = lo + static_cast<unsigned>(v) * 8u;
+        if (e >= ch_end) {
+          const unsigned cl = e / hw;
+          ch_end = (cl + 1u) * hw;
+          const int ch = ch0 + static_cast<int>(cl);
+          fold_channel(gb_smem ? sgamma[ch] : __ldg(p.gamma + ch), gb_smem ? sbeta[ch] : __ldg(p.beta + ch), mean,
+                       rstd, A, B);
         }
+        store16(obase + v * 16, silu_affine<T>(raw, A, B));
+      };
+      if (nvec == kGnfChunk / 8) {
+#pragma unroll
+        for (int b = 0; b < kGnfApplyVec; ++b) one(at + b * 32 * kGnfApplyWarps);
+      } else {
+#pragma unroll
+        for (int b = 0; b < kGnfApplyVec; ++b)
+          if (at + b * 32 * kGnfApplyWarps < nvec) one(at + b * 32 * kGnfApplyWarps);
       }
       // the slot has been read for the last time by this warp
       __syncwarp();
@@ -744,7 +769,8 @@ __global__ void __launch_bounds__(kGnfThreads, 1) gn_fused_kernel(const __grid_c
   int s = 0;
   uint32_t ph = 0;
   for (unsigned t = 0; t < mine; ++t, pos.advance(G, P)) {
-    const bool got = mbar_try_wait(full0 + 8 * s, ph) || bounded_wait(full0 + 8 * s, ph, limit, abort_cta, p.status);
+    const bool got = mbar_try_wait_sleep(full0 + 8 * s, ph, kGnfSleepNs) ||
+                     bounded_wait(full0 + 8 * s, ph, limit, abort_cta, p.status);
     if (!gnf_stats_barrier_and(got)) {
       if (tid == 0) atomicExch(p.abort_word, p.tag);
       break;                                         // every stats warp leaves together
@@ -758,19 +784,23 @@ __global__ void __launch_bounds__(kGnfThreads, 1) gn_fused_kernel(const __grid_c
     const float2 nk = make_float2(-first[0].x, -first[0].x);
     const unsigned char* slot = smem + kGnfOffSlot0 + s * kGnfChunkBytes;
     float2 a1 = make_float2(0.0f, 0.0f), a2 = make_float2(0.0f, 0.0f);
+    auto one = [&](int v) {
+      float2 X[4];
+      Elem<T>::unpack(*reinterpret_cast<const uint4*>(slot + v * 16), X);
 #pragma unroll
-    for (int b = 0; b < kGnfStatsVec; ++b) {
-      const int v = tid + b * kGnfStatsThreads;
-      if (v < nvec) {
-        float2 X[4];
-        Elem<T>::unpack(*reinterpret_cast<const uint4*>(slot + v * 16), X);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float2 d = __fadd2_rn(X[q], nk);
-          a1 = __fadd2_rn(a1, d);
-          a2 = __ffma2_rn(d, d, a2);
-        }
+      for (int q = 0; q < 4; ++q) {
+        const float2 d = __fadd2_rn(X[q], nk);
+        a1 = __fadd2_rn(a1, d);
+        a2 = __ffma2_rn(d, d, a2);
       }
+    };
+    if (nvec == kGnfChunk / 8) {
+#pragma unroll
+      for (int b = 0; b < kGnfStatsVec; ++b) one(tid + b * kGnfStatsThreads);
+    } else {
+#pragma unroll
+      for (int b = 0; b < kGnfStatsVec; ++b)
+        if (tid + b * kGnfStatsThreads < nvec) one(tid + b * kGnfStatsThreads);
     }
     // this warp has read the slot for the last time
     __syncwarp();
