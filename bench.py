@@ -713,6 +713,48 @@ def run_ours(args, w):
     return 0
 
 
+def run_copy_calibration(args):
+    """A device copy (torch ``copy_``) of the same bytes as each workload
+    size, timed the way the kernels are: per-launch CUDA events after an L2
+    flush, and back to back.  The copy rate grows with size well past L2,
+    so a kernel's fraction of a same-size copy separates its own overhead
+    from the ramp-up and tail that any launch of that size pays."""
+    import torch
+
+    dev = torch.device("cuda", 0)
+    l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or 129 * 2 ** 20
+    flush = torch.empty(2 * l2 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for mb in (25, 50, 113, 134, 268, 671, 1024):
+        n = int(mb * 1e6) // 2
+        a = torch.ones(n, dtype=torch.bfloat16, device=dev)
+        b = torch.empty_like(a)
+        for _ in range(5):
+            b.copy_(a)
+        times = []
+        for _ in range(50):
+            flush.fill_(1.0)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            b.copy_(a)
+            e1.record(stream)
+            torch.cuda.synchronize(dev)
+            times.append(e0.elapsed_time(e1) / 1e3)
+        k = 200
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(k):
+            b.copy_(a)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        moved = 2 * a.numel() * a.element_size()
+        t_flush, t_b2b = statistics.median(times), e0.elapsed_time(e1) / 1e3 / k
+        print(json.dumps({"copy_mb": mb, "bytes_moved": moved, "flushed_us": t_flush * 1e6,
+                          "flushed_gbs": moved / t_flush / 1e9, "back_to_back_us": t_b2b * 1e6,
+                          "back_to_back_gbs": moved / t_b2b / 1e9}), flush=True)
+    return 0
+
+
 def main(argv=None):
     p = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     p.add_argument("--gpus", type=int, default=1)
@@ -731,6 +773,8 @@ def main(argv=None):
     p.add_argument("--l2-flush", choices=["auto", "on", "off"], default="auto")
     p.add_argument("--gn-mode", choices=["auto", "fused", "two_pass"], default="auto",
                    help="group-norm workloads: which path to time")
+    p.add_argument("--copy-calibration", action="store_true",
+                   help="print the device copy rate at the workloads' sizes (one JSON line each) and exit")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -739,6 +783,8 @@ def main(argv=None):
     args = p.parse_args(argv)
     if args.warmup < 3:
         p.error("--warmup must be >= 3")
+    if args.copy_calibration:
+        return run_copy_calibration(args)
     w = I.WORKLOADS.get(args.workload) or I.ADALN_WORKLOADS.get(args.workload) or I.GN_WORKLOADS[args.workload]
     if args.impl == "reference":
         if not isinstance(w, I.Workload):
