@@ -221,9 +221,15 @@ qknr_status check_buffers(const qknr_gn_args* a, const GnPlan& pl) {
   return QKNR_OK;
 }
 
+// The tag of calls made while the stream is being captured into a CUDA
+// graph: a replay reuses its launch's parameters, so the captured call
+// clears the records first (a memset node) and uses this fixed tag.
+constexpr unsigned kCaptureTag = 1u;
+
 // A per-call record tag: a bijective 32-bit mix of a process-wide call
 // counter (no tag repeats within 2^32 calls; tags do not look like small
-// integers or zeros left in a reused workspace), never 0 (the two-pass tag).
+// integers or zeros left in a reused workspace), never 0 (the two-pass tag)
+// and never kCaptureTag.
 unsigned next_tag() {
   static std::atomic<unsigned> counter{0};
   while (true) {
@@ -232,12 +238,24 @@ unsigned next_tag() {
     x ^= x >> 16;
     x *= 0x85EBCA6Bu;
     x ^= x >> 13;
-    if (x != 0u) return x;
+    if (x != 0u && x != kCaptureTag) return x;
   }
 }
 
 qknr_status launch_fused(const qknr_gn_args* a, const GnPlan& pl, const FusedLaunch& fl, cudaStream_t s) {
   char* ws = static_cast<char*>(a->workspace);
+  cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(s, &capture);
+  if (e != cudaSuccess) return qknr_host::cuda_fail(e, "cudaStreamIsCapturing");
+  unsigned tag = 0;
+  if (capture == cudaStreamCaptureStatusActive) {
+    // every replay starts from cleared records and abort word
+    e = cudaMemsetAsync(ws, 0, pl.f_records + 16, s);
+    if (e != cudaSuccess) return qknr_host::cuda_fail(e, "cudaMemsetAsync(group norm records)");
+    tag = kCaptureTag;
+  } else {
+    tag = next_tag();
+  }
   qknr::GnFusedParams fp;
   memset(&fp, 0, sizeof(fp));
   fp.x = static_cast<const char*>(a->x);
@@ -254,12 +272,12 @@ qknr_status launch_fused(const qknr_gn_args* a, const GnPlan& pl, const FusedLau
   fp.groups = a->groups;
   fp.group_channels = a->c / a->groups;
   fp.channels = a->c;
-  fp.tag = next_tag();
+  fp.tag = tag;
   fp.flags = a->flags & (qknr::kGnfFlagStallLoads | qknr::kGnfFlagStallRecords);
   fp.wait_limit_ns = a->wait_limit_ns ? a->wait_limit_ns : kDefaultWaitNs;
   fp.eps = a->eps;
   void* kargs[] = {&fp};
-  cudaError_t e = cudaLaunchCooperativeKernel(fl.fn, dim3(fl.grid), dim3(qknr::kGnfThreads), kargs,
+  e = cudaLaunchCooperativeKernel(fl.fn, dim3(fl.grid), dim3(qknr::kGnfThreads), kargs,
                                               static_cast<size_t>(qknr::kGnfSmemBytes), s);
   if (e != cudaSuccess) return qknr_host::cuda_fail(e, "cudaLaunchCooperativeKernel(fused group norm)");
   return QKNR_OK;

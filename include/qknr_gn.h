@@ -23,7 +23,9 @@
  *     memory from its statistics to its normalise + SiLU pass; CTAs publish
  *     piece statistics through the workspace, tagged with a value unique to
  *     the call (so the workspace needs no clearing), and wait (bounded) for
- *     the other pieces of a group.  Needs cooperative launch support and
+ *     the other pieces of a group.  A call made while its stream is being
+ *     captured into a CUDA graph adds a memset of the records before the
+ *     launch, so every replay starts clean.  Needs cooperative launch support and
  *     groups of at most 8 * SMs pieces (14.9 M elements on 152 SMs).
  *   two-pass (QKNR_GN_TWO_PASS): a statistics kernel and a normalise + SiLU
  *     kernel, once for all groups or once per batch of groups; x is read
