@@ -242,7 +242,12 @@ unsigned next_tag() {
   }
 }
 
-qknr_status launch_fused(const qknr_gn_args* a, const GnPlan& pl, const FusedLaunch& fl, cudaStream_t s) {
+// *too_large: the cooperative launch did not fit the SMs this context may
+// use (e.g. under MPS); in QKNR_GN_AUTO the caller then takes the two-pass
+// path, whose workspace the auto size already covers.
+qknr_status launch_fused(const qknr_gn_args* a, const GnPlan& pl, const FusedLaunch& fl, cudaStream_t s,
+                         bool* too_large) {
+  *too_large = false;
   char* ws = static_cast<char*>(a->workspace);
   cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
   cudaError_t e = cudaStreamIsCapturing(s, &capture);
@@ -279,6 +284,11 @@ qknr_status launch_fused(const qknr_gn_args* a, const GnPlan& pl, const FusedLau
   void* kargs[] = {&fp};
   e = cudaLaunchCooperativeKernel(fl.fn, dim3(fl.grid), dim3(qknr::kGnfThreads), kargs,
                                               static_cast<size_t>(qknr::kGnfSmemBytes), s);
+  if (e == cudaErrorCooperativeLaunchTooLarge && a->mode == QKNR_GN_AUTO && pl.pieces > 0) {
+    (void)cudaGetLastError();                  // a launch-configuration error: not sticky
+    *too_large = true;
+    return QKNR_OK;
+  }
   if (e != cudaSuccess) return qknr_host::cuda_fail(e, "cudaLaunchCooperativeKernel(fused group norm)");
   return QKNR_OK;
 }
@@ -336,7 +346,12 @@ qknr_status qknr_gn_silu_forward(const qknr_gn_args* args, qknr_stream_t stream)
   st = choose(args, pl, &fl, &fused);
   if (st != QKNR_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  return fused ? launch_fused(args, pl, fl, s) : launch_two_pass(args, pl, s);
+  if (fused) {
+    bool too_large = false;
+    st = launch_fused(args, pl, fl, s, &too_large);
+    if (st != QKNR_OK || !too_large) return st;
+  }
+  return launch_two_pass(args, pl, s);
 }
 
 qknr_status qknr_gn_query(const qknr_gn_args* args, qknr_launch_info* info) {

@@ -33,7 +33,8 @@
  *
  * QKNR_GN_AUTO takes the fused path when this device and shape allow it
  * and piece_elems and l2_batch_bytes are 0 (they tune the two-pass path),
- * else the two-pass path.  Both give the same bits when the two-pass
+ * else the two-pass path; it also falls back to the two-pass path when the
+ * cooperative launch does not fit the SMs the context may use.  Both give the same bits when the two-pass
  * pieces are 12288 elements.
  *
  * Ownership and errors follow qknr.h: the caller owns every buffer
