@@ -682,7 +682,9 @@ def run_ours(args, w):
         "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
         "config": dict(workload_config(w, world, run.tokens),
                        l2=("L2 flushed between steps (write of 2x L2); launches timed by per-launch events"
-                           if flush is not None else "inputs larger than L2 (no flush)")),
+                           if flush is not None else
+                           ("inputs larger than L2 (no flush)" if run.bytes_per_launch * L >= 2 * l2 else
+                            "not flushed (--l2-flush off): a hot number, inputs partly served from L2"))),
         "gbs": run.bytes_per_launch * L * K * world / max_elapsed / 1e9,
         "pct_of_hbm_peak": 100.0 * achieved / peak,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
@@ -771,6 +773,8 @@ def main(argv=None):
     p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--e2e-chunk-rows", type=int, default=4096)
     p.add_argument("--l2-flush", choices=["auto", "on", "off"], default="auto")
+    p.add_argument("--dtype", choices=["bf16", "fp16"], default=None,
+                   help="activation dtype of the workload (default: the workload's own, bf16)")
     p.add_argument("--gn-mode", choices=["auto", "fused", "two_pass"], default="auto",
                    help="group-norm workloads: which path to time")
     p.add_argument("--copy-calibration", action="store_true",
@@ -786,6 +790,11 @@ def main(argv=None):
     if args.copy_calibration:
         return run_copy_calibration(args)
     w = I.WORKLOADS.get(args.workload) or I.ADALN_WORKLOADS.get(args.workload) or I.GN_WORKLOADS[args.workload]
+    if args.dtype and args.dtype != w.dtype:
+        kw = {"dtype": args.dtype}
+        if isinstance(w, I.AdaLNWorkload) and w.mod_dtype != "fp32":
+            kw["mod_dtype"] = args.dtype                  # modulation rows in the activation dtype
+        w = w.with_(**kw)
     if args.impl == "reference":
         if not isinstance(w, I.Workload):
             p.error("--impl reference times the QK-norm + RoPE oracle; pick a QK workload")
