@@ -145,7 +145,7 @@ def test_fused_in_place_equals_out_of_place_and_repeats():
     src = to_dev(inp["x"], "bf16")
     out = torch.empty_like(src)
     gn_call(src, w, inp, out=out, mode="fused")
-    for _ in range(3):                                  # the counters start at zero on every call
+    for _ in range(3):                                  # earlier calls' records carry other tags
         x = to_dev(inp["x"], "bf16")
         gn_call(x, w, inp, mode="fused")
         torch.cuda.synchronize()
