@@ -199,3 +199,14 @@ def test_fused_bounded_waits_report_timeout(flag):
     assert int(status.item()) == 0
     ref = G.group_norm_silu(inp["x"], "bf16", w.groups, inp["gamma"], inp["beta"], w.eps)
     compare(to_bits(res), ref, "bf16", "after timeout")
+
+
+@pytest.mark.parametrize("name", list(I.GN_WORKLOADS))
+def test_vae_shapes_fused_equals_two_pass(name):
+    # the full VAE shapes: hundreds of pieces per group over all CTAs
+    w = I.GN_WORKLOADS[name]
+    inp = I.make_gn_inputs(w)
+    a = gn_call(to_dev(inp["x"], w.dtype), w, inp, mode="fused")
+    b = gn_call(to_dev(inp["x"], w.dtype), w, inp, mode="two_pass", piece_elems=12288)
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
