@@ -423,16 +423,27 @@ class Runner:
         d2h = sum(t.numel() * t.element_size() for t in self.pinned_out.values())
         self.pipe = None
         if self.w.packed and not self.w.out_of_place:
+            # in place on the pinned host activation: the Q|K columns of each
+            # row go to the device and back; V is never read or written
             qkv = self.pinned["qkv"]
             self.pipe = self.Q.HostPipeline(qkv.shape[1], qkv.dtype, chunk_rows=chunk_rows, device=self.dev)
+            es = qkv.element_size()
+            qk = (self.w.n_heads_q + self.w.n_heads_k) * self.w.head_dim
+            tables = sum(self.pinned[k].numel() * self.pinned[k].element_size()
+                         for k in ("gamma_q", "gamma_k", "cos", "sin") if k in self.pinned)
+            h2d = qkv.shape[0] * qk * es + tables
+            d2h = qkv.shape[0] * qk * es
         return h2d, d2h
+
+    def e2e_result(self):
+        """The pinned host tensor holding the e2e result."""
+        return self.pinned["qkv"] if self.pipe is not None else self.pinned_out[self.outputs[0]]
 
     def e2e_step(self, stream):
         if self.pipe is not None:
             w, p = self.w, self.pinned
             self.pipe(p["qkv"], w.n_heads_q, w.n_heads_k, w.n_heads_v, w.head_dim, p["gamma_q"], p["gamma_k"],
-                      p["cos"], p["sin"], out_host=self.pinned_out["qkv"], rope_style=w.rope_style,
-                      cos_layout=w.cos_layout, eps=w.eps, **self.tune)
+                      p["cos"], p["sin"], rope_style=w.rope_style, cos_layout=w.cos_layout, eps=w.eps, **self.tune)
             return
         for k, t in self.pinned.items():
             self.d[k].copy_(t, non_blocking=True)
@@ -655,14 +666,16 @@ def run_ours(args, w):
         e2e_s = max_over_ranks(s0.elapsed_time(s1) / 1e3, dev)
         e2e = {"value": whole_job_us_per_call(e2e_s, n_e2e, world), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": n_e2e,
-               "path": ("HostPipeline: pinned host rows in chunks of %d, host->device copy, qknr_forward and "
-                        "device->host copy overlapped on three streams" % args.e2e_chunk_rows) if run.pipe else
+               "path": ("HostPipeline, in place on the pinned host activation: the Q|K columns of rows in chunks "
+                        "of %d copied host->device, qknr_forward, and copied back, overlapped on three streams "
+                        "(V is neither read nor written by the operation, so it never leaves the host)"
+                        % args.e2e_chunk_rows) if run.pipe else
                        "pinned host -> device copies, qknr_forward via the Python binding, device -> pinned host, "
                        "one stream"}
         if getattr(w, "packed", False):
             # each e2e step starts from the host input, so V comes back unchanged
             D3 = (w.n_heads_q + w.n_heads_k) * w.head_dim
-            back = run.pinned_out[run.outputs[0]].view(torch.int16).numpy().view(np.uint16)
+            back = run.e2e_result().view(torch.int16).numpy().view(np.uint16)
             if not np.array_equal(back[:, D3:], run.inp["qkv"][:, D3:]):
                 raise RuntimeError("e2e: V slice changed")
         if int(status.item()) != 0 or (run.pipe is not None and run.pipe.read_status() != 0):

@@ -11,6 +11,7 @@ through) is described in ``include/qknr.h``.
 from __future__ import annotations
 
 import ctypes
+import glob
 import os
 import threading
 from ctypes import c_char, c_float, c_int32, c_int64, c_size_t, c_uint32, c_uint64, c_void_p
@@ -406,6 +407,39 @@ def qk_norm_rope_separate(q, k, n_heads, head_dim, gamma_q, gamma_k, cos, sin, *
 # ---------------------------------------------------------------------------
 # host-resident activations: chunked, overlapped copies around the kernel
 
+_cudart = None
+
+
+def _cudart_lib() -> ctypes.CDLL:
+    """The CUDA runtime libqknr.so links (already loaded with it)."""
+    global _cudart
+    if _cudart is None:
+        load()
+        cands = sorted(glob.glob(os.path.join(_build.cuda_lib_dir(), "libcudart.so*")))
+        if not cands:
+            raise RuntimeError("libcudart.so not found next to the CUDA toolkit")
+        lib = ctypes.CDLL(cands[-1])
+        lib.cudaMemcpy2DAsync.argtypes = [c_void_p, c_size_t, c_void_p, c_size_t, c_size_t, c_size_t, c_int32,
+                                          c_void_p]
+        lib.cudaMemcpy2DAsync.restype = c_int32
+        _cudart = lib
+    return _cudart
+
+
+def copy_rows_async(dst: int, dst_pitch: int, src: int, src_pitch: int, width: int, rows: int,
+                    stream: torch.cuda.Stream) -> None:
+    """``rows`` rows of ``width`` bytes between pitched buffers (host or
+    device, either way; host memory pinned for the copy to be asynchronous),
+    on ``stream``: one cudaMemcpy2DAsync."""
+    if rows == 0 or width == 0:
+        return
+    err = _cudart_lib().cudaMemcpy2DAsync(c_void_p(dst), dst_pitch, c_void_p(src), src_pitch, width, rows,
+                                          4,  # cudaMemcpyDefault: direction from the addresses
+                                          c_void_p(stream.cuda_stream))
+    if err != 0:
+        raise RuntimeError(f"cudaMemcpy2DAsync failed with error {err}")
+
+
 class HostPipeline:
     """Runs the fused QK-RMSNorm + RoPE on a packed QKV activation that lives
     in (pinned) host memory.  Token rows go through the device in chunks:
@@ -414,9 +448,15 @@ class HostPipeline:
     call costs about one direction of copy traffic instead of both plus the
     kernel.
 
+    In place on the host (``out_host`` None or the input) only the Q and K
+    columns of each row cross the host link, as pitched 2-D copies: V is
+    neither read nor written by the operation, so it stays where it is.
+    With a separate ``out_host`` whole rows go both ways and V is copied
+    through unchanged.
+
     The device staging ring (``n_buffers`` chunks) and the device copies of
-    gamma and the cos/sin table are allocated once, here, by torch; the
-    library itself still allocates nothing.  Results are bitwise those of
+    gamma and the cos/sin table are allocated by torch here; the library
+    itself still allocates nothing.  Results are bitwise those of
     ``qk_norm_rope_packed`` on the whole activation: every row is processed
     by the same kernel with the same table row.
     """
@@ -427,12 +467,13 @@ class HostPipeline:
                                    else torch.device(device).index)
         self.chunk_rows = int(chunk_rows)
         self.width = int(width)
-        self.bufs = [torch.empty((self.chunk_rows, self.width), dtype=dtype, device=self.device)
+        self.bufs = [torch.empty(self.chunk_rows * self.width, dtype=dtype, device=self.device)
                      for _ in range(n_buffers)]
         self.h2d = torch.cuda.Stream(self.device)
         self.d2h = torch.cuda.Stream(self.device)
         self.freed = [None] * n_buffers          # event: the buffer's last D2H finished
         self.status = torch.zeros(1, dtype=torch.int32, device=self.device)
+        self.last_h2d_bytes = self.last_d2h_bytes = 0
 
     def _stage_tables(self, gamma_q, gamma_k, cos, sin, stream, user):
         """Device copies of the gains and tables (copied every call, on
@@ -454,10 +495,19 @@ class HostPipeline:
 
     def __call__(self, qkv_host, n_heads_q, n_heads_k, n_heads_v, head_dim, gamma_q, gamma_k, cos, sin, *,
                  out_host=None, rope_style="interleaved", cos_layout="shared_row", eps=1e-6, **tune):
-        if qkv_host.is_cuda or qkv_host.dim() != 2 or qkv_host.shape[1] != self.width:
-            raise ValueError("qkv_host must be a 2-D host tensor of the pipeline's width")
+        if qkv_host.is_cuda or qkv_host.dim() != 2 or qkv_host.shape[1] != self.width or qkv_host.stride(1) != 1:
+            raise ValueError("qkv_host must be a 2-D host tensor of the pipeline's width with contiguous rows")
+        if (n_heads_q + n_heads_k + n_heads_v) * head_dim != self.width:
+            raise ValueError("head counts do not match the pipeline's width")
+        in_place = out_host is None or out_host.data_ptr() == qkv_host.data_ptr()
         out_host = qkv_host if out_host is None else out_host
+        if out_host.shape != qkv_host.shape or out_host.dtype != qkv_host.dtype or out_host.stride(1) != 1:
+            raise ValueError("out_host must match qkv_host")
         T = qkv_host.shape[0]
+        es = qkv_host.element_size()
+        # in place: the Q|K columns only; else whole rows
+        cols = (n_heads_q + n_heads_k) * head_dim if in_place else self.width
+        hv = 0 if in_place else n_heads_v
         compute = torch.cuda.current_stream(self.device)
         gq, gk, cos_d, sin_d = self._stage_tables(gamma_q, gamma_k, cos, sin, self.h2d, compute)
         tables_ready = torch.cuda.Event()
@@ -470,11 +520,12 @@ class HostPipeline:
         for i, r0 in enumerate(range(0, T, self.chunk_rows)):
             r1 = min(T, r0 + self.chunk_rows)
             b = i % n
-            buf = self.bufs[b][: r1 - r0]
+            buf = self.bufs[b][: (r1 - r0) * cols].view(r1 - r0, cols)
             with torch.cuda.stream(self.h2d):
                 if self.freed[b] is not None:
                     self.h2d.wait_event(self.freed[b])
-                buf.copy_(qkv_host[r0:r1], non_blocking=True)
+                copy_rows_async(buf.data_ptr(), cols * es, qkv_host[r0].data_ptr(), qkv_host.stride(0) * es,
+                                cols * es, r1 - r0, self.h2d)
                 loaded = torch.cuda.Event()
                 loaded.record(self.h2d)
             compute.wait_event(loaded)
@@ -483,20 +534,24 @@ class HostPipeline:
             # the chunk's table rows: its own slice of a per-token table, or
             # the whole batch-broadcast table (chunks start on a multiple of it)
             c, s = (cos_d[r0:r1], sin_d[r0:r1]) if rows >= T else (cos_d, sin_d)
-            launch(packed_args(buf, n_heads_q, n_heads_k, n_heads_v, head_dim, gq, gk, c, s,
+            launch(packed_args(buf, n_heads_q, n_heads_k, hv, head_dim, gq, gk, c, s,
                                rope_style=rope_style, cos_layout=cos_layout, eps=eps, dev_status=self.status,
                                **tune), compute)
             computed = torch.cuda.Event()
             computed.record(compute)
             with torch.cuda.stream(self.d2h):
                 self.d2h.wait_event(computed)
-                out_host[r0:r1].copy_(buf, non_blocking=True)
+                copy_rows_async(out_host[r0].data_ptr(), out_host.stride(0) * es, buf.data_ptr(), cols * es,
+                                cols * es, r1 - r0, self.d2h)
                 freed = torch.cuda.Event()
                 freed.record(self.d2h)
                 self.freed[b] = freed
         # the caller's stream sees the results once every D2H copy is done
         done.record(self.d2h)
         compute.wait_event(done)
+        tables = sum(t.numel() * t.element_size() for t in (gamma_q, gamma_k, cos, sin) if t is not None)
+        self.last_h2d_bytes = T * cols * es + tables
+        self.last_d2h_bytes = T * cols * es
         return out_host
 
 

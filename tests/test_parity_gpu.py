@@ -220,6 +220,29 @@ def test_host_pipeline_matches_device_path(T, chunk):
         assert torch.equal(h2.view(torch.int16), out.view(torch.int16))
 
 
+def test_host_pipeline_in_place_moves_only_q_and_k():
+    # a host activation with padded rows: in place, only the Q|K columns
+    # travel; V and the padding are never written
+    w = I.WORKLOADS["wan_32760x40x128"].with_(n_heads_q=4, n_heads_k=4, n_heads_v=4)
+    T = 3000
+    inp = I.make_inputs(w, tokens=T)
+    ref, _ = run_packed(w, inp)
+    width = 12 * 128
+    padded = np.full((T, width + 64), 0x7F7F, dtype=np.uint16)
+    padded[:, :width] = inp["qkv"]
+    host_full = torch.from_numpy(padded.view(np.int16)).view(torch.bfloat16).pin_memory()
+    host = host_full[:, :width]
+    pipe = Q.HostPipeline(width, torch.bfloat16, chunk_rows=1024)
+    pipe(host, 4, 4, 4, 128, torch.from_numpy(inp["gamma_q"]), torch.from_numpy(inp["gamma_k"]),
+         torch.from_numpy(inp["cos"]), torch.from_numpy(inp["sin"]), rope_style=w.rope_style)
+    torch.cuda.synchronize()
+    assert pipe.read_status() == 0
+    got = host_full.view(torch.int16).numpy().view(np.uint16)
+    np.testing.assert_array_equal(got[:, :width], ref.cpu().view(torch.int16).numpy().view(np.uint16))
+    assert np.all(got[:, width:] == 0x7F7F)
+    assert pipe.last_d2h_bytes == T * 8 * 128 * 2
+
+
 def test_host_pipeline_batch_broadcast_table():
     w = I.WORKLOADS["dense_4096x24x128"].with_(seq=500, batch=4, positions="1d")
     T = w.tokens
