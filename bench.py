@@ -576,7 +576,8 @@ def run_ours(args, w):
     if isinstance(w, I.GroupNormWorkload):
         tune = dict(gn_mode=args.gn_mode)
     else:
-        tune = dict(ctas_per_sm=args.ctas_per_sm, stages=args.stages, consumer_warps=args.consumer_warps)
+        tune = dict(ctas_per_sm=args.ctas_per_sm, stages=args.stages, consumer_warps=args.consumer_warps,
+                    group_warps=args.group_warps)
     runner = {I.AdaLNWorkload: AdaLNRunner, I.GroupNormWorkload: GroupNormRunner}.get(type(w), Runner)
     run = runner(w, dev, tune, status, args.tokens)
     stream = torch.cuda.current_stream(dev)
@@ -783,6 +784,7 @@ def main(argv=None):
     p.add_argument("--ctas-per-sm", type=int, default=0)
     p.add_argument("--stages", type=int, default=0)
     p.add_argument("--consumer-warps", type=int, default=0)
+    p.add_argument("--group-warps", type=int, default=0)
     p.add_argument("--e2e-steps", type=int, default=20)
     p.add_argument("--e2e-chunk-rows", type=int, default=4096)
     p.add_argument("--l2-flush", choices=["auto", "on", "off"], default="auto")

@@ -312,11 +312,15 @@ qknr_status size_launch(const qknr_args* a, Plan* pl) {
   const long long grid0 = (long long)di.num_sms * cps;
   const long long rows_per_cta = (a->tokens + grid0 - 1) / grid0;
 
-  // Wide rows that carry a V copy, or that a CTA sees few of, do better as
-  // two groups of two stages (sweeps: Wan out of place 329 vs 350 us,
-  // FLUX.2 Q+K in one launch 73.8 vs 76.1 us); a deeper ring than four
-  // stages in all only queues more reads (Wan 231 vs 211 us with six).
-  const bool two_groups = wide_rows && passes > 0 && (pl->kp.hv > 0 || rows_per_cta_1 < 128);
+  // Wide rows that carry a V copy, a per-head expanded table, or that a CTA
+  // sees few of, do better as two groups of two stages (sweeps: Wan out of
+  // place 329 vs 350 us, Wan with a bf16 expanded table 326 vs 343 us,
+  // FLUX.2 Q+K in one launch 73.8 vs 76.1 us) where two such rings fit (an
+  // fp32 expanded table's stages do not: one group of three); a deeper ring
+  // than four stages in all only queues more reads (Wan 231 vs 211 us with
+  // six).
+  const bool expanded = a->cos_layout == QKNR_COS_PER_HEAD_EXPANDED;
+  const bool two_groups = wide_rows && passes > 0 && (pl->kp.hv > 0 || expanded || rows_per_cta_1 < 128);
   int gw = a->group_warps;
   if (gw == 0) {
     int want = two_groups ? warps / 2 : (wide_rows ? warps : (passes + 5) / 6);   // narrow: ~6 passes per warp
