@@ -321,9 +321,14 @@ qknr_status size_launch(const qknr_args* a, Plan* pl) {
   // six).
   const bool expanded = a->cos_layout == QKNR_COS_PER_HEAD_EXPANDED;
   const bool two_groups = wide_rows && passes > 0 && (pl->kp.hv > 0 || expanded || rows_per_cta_1 < 128);
+  // rows with a V copy that a CTA sees many of: three groups of two stages
+  // (Wan out of place 321 vs 329 us; with few rows per CTA, FLUX.2, two)
+  const bool three_groups = two_groups && pl->kp.hv > 0 && rows_per_cta_1 >= 128;
   int gw = a->group_warps;
   if (gw == 0) {
-    int want = two_groups ? warps / 2 : (wide_rows ? warps : (passes + 5) / 6);   // narrow: ~6 passes per warp
+    int want = three_groups ? warps / 3
+               : two_groups ? warps / 2
+                            : (wide_rows ? warps : (passes + 5) / 6);   // narrow: ~6 passes per warp
     if (want < 1) want = 1;
     gw = warps;
     for (int g = want; g <= warps; ++g)
