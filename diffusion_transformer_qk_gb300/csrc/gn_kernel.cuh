@@ -443,7 +443,7 @@ constexpr int kGnfApplyVec = kGnfChunk / 8 / (32 * kGnfApplyWarps);   // ... per
 static_assert(kGnfChunk / 8 == kGnfStatsVec * kGnfStatsThreads, "stats warps cover a chunk");
 static_assert(kGnfChunk / 8 == kGnfApplyVec * 32 * kGnfApplyWarps, "apply warps cover a chunk");
 static_assert(kGnfStatsVec <= kGnBatch, "one batch of gn_stats_kernel covers a chunk (same order)");
-constexpr int kGnfSlots = 8;
+constexpr int kGnfSlots = 9;
 constexpr int kGnfCoefSlots = 8;
 // dynamic shared memory map (bytes)
 constexpr int kGnfOffFull = 0;                       // full[kGnfSlots]
@@ -452,19 +452,23 @@ constexpr int kGnfOffCoefFull = 256;                 // coef_full[kGnfCoefSlots]
 constexpr int kGnfOffCoefEmpty = 320;                // coef_empty[kGnfCoefSlots]
 constexpr int kGnfOffAbort = 384;
 constexpr int kGnfOffStatsDone = 388;                // chunks this CTA's stats warps have recorded
-constexpr int kGnfOffMeta = 448;                     // [kGnfSlots][2]: first channel, next channel's first element
+constexpr int kGnfOffMeta = 400;                     // [kGnfSlots][2]: first channel, next channel's first element
 constexpr int kGnfOffK = 512;                        // [kGnfSlots][16 bytes]: the span's first 16 bytes
 constexpr int kGnfOffRed = 768;                      // [2 * kGnWarps] floats
 constexpr int kGnfOffCoef = 896;                     // [kGnfCoefSlots][mean, rstd]
 constexpr int kGnfOffSlot0 = 1024;
 constexpr int kGnfOffGammaBeta = kGnfOffSlot0 + kGnfSlots * kGnfChunkBytes;   // gamma[C], beta[C]
-constexpr int kGnfMaxSmemChannels = 2048;            // larger C reads gamma / beta from global memory
+constexpr int kGnfMaxSmemChannels = 1280;            // larger C reads gamma / beta from global memory
 constexpr int kGnfSmemBytes = kGnfOffGammaBeta + 8 * kGnfMaxSmemChannels;
 constexpr unsigned kGnfFlagStallLoads = 0x1u;        // test: issue no copies
 constexpr unsigned kGnfFlagStallRecords = 0x2u;      // test: write no record
+static_assert(kGnfOffFull + 8 * kGnfSlots <= kGnfOffEmpty, "shared memory map");
+static_assert(kGnfOffEmpty + 8 * kGnfSlots <= kGnfOffCoefFull, "shared memory map");
+static_assert(kGnfOffStatsDone + 4 <= kGnfOffMeta, "shared memory map");
 static_assert(kGnfOffK + 16 * kGnfSlots <= kGnfOffRed, "shared memory map");
 static_assert(kGnfOffMeta + 8 * kGnfSlots <= kGnfOffK, "shared memory map");
 static_assert(kGnfOffCoef + 8 * kGnfCoefSlots <= kGnfOffSlot0, "shared memory map");
+static_assert(kGnfSmemBytes <= 227 * 1024, "shared memory map");
 
 struct GnFusedParams {
   const char* x;

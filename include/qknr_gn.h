@@ -26,7 +26,7 @@
  *     the other pieces of a group.  A call made while its stream is being
  *     captured into a CUDA graph adds a memset of the records before the
  *     launch, so every replay starts clean.  Needs cooperative launch support and
- *     groups of at most 8 * SMs pieces (14.9 M elements on 152 SMs).
+ *     groups of at most 9 * SMs pieces (16.8 M elements on 152 SMs).
  *   two-pass (QKNR_GN_TWO_PASS): a statistics kernel and a normalise + SiLU
  *     kernel, once for all groups or once per batch of groups; x is read
  *     twice.  No CTA waits for another.

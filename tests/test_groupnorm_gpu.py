@@ -117,7 +117,7 @@ def query(w, **kw):
 def test_vae_shapes_take_the_fused_path(name):
     info = query(I.GN_WORKLOADS[name])
     assert info["kernel"].startswith("gn_fused<bf16>"), info
-    assert info["grid"] == info["num_sms"] and info["block"] == 800 and info["stages"] == 8
+    assert info["grid"] == info["num_sms"] and info["block"] == 800 and info["stages"] == 9
     two = query(I.GN_WORKLOADS[name], mode="two_pass")
     assert two["kernel"].startswith("gn_stats+gn_apply"), two
 
@@ -154,10 +154,10 @@ def test_fused_in_place_equals_out_of_place_and_repeats():
 
 
 @pytest.mark.parametrize("shape,per_cta", [((1, 1, 2880, 2800), 5), ((1, 3, 2048, 2000), 7),
-                                           ((1, 2, 2720, 2700), 8)])
+                                           ((1, 2, 2720, 2700), 8), ((1, 1, 4096, 4096), 9)])
 def test_fused_large_groups(shape, per_cta):
-    # 657, 1000 and 1196 pieces of 12288 elements per group over 152 CTAs;
-    # at most 8 per CTA
+    # 657, 1000, 1196 and 1366 pieces of 12288 elements per group over 152
+    # CTAs; at most 9 per CTA
     w = I.GroupNormWorkload("big", *shape, groups=1, scale=1.2, offset=0.7, seed=43)
     info = query(w)
     assert info["kernel"].startswith("gn_fused") and info["kernel"].endswith(f" {per_cta} per CTA"), info
@@ -172,10 +172,10 @@ def test_fused_large_groups(shape, per_cta):
 
 
 def test_groups_beyond_the_fused_limit_fall_back_to_two_pass():
-    # 1366 pieces per group: 9 per CTA, more than the 8 ring slots
-    w = I.GroupNormWorkload("huge", 1, 1, 4096, 4096, groups=1, seed=44)
+    # 1400 pieces per group: 10 per CTA, more than the 9 ring slots
+    w = I.GroupNormWorkload("huge", 1, 1, 4200, 4096, groups=1, seed=44)
     assert query(w)["kernel"].startswith("gn_stats+gn_apply")
-    x = torch.zeros((1, 1, 4096, 4096), dtype=torch.bfloat16, device="cuda")
+    x = torch.zeros((1, 1, 4200, 4096), dtype=torch.bfloat16, device="cuda")
     g = torch.ones(1, device="cuda")
     with pytest.raises(Q.QknrError) as e:
         Q.group_norm_silu(x, 1, g, g, mode="fused")

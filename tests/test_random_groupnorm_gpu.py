@@ -1,5 +1,5 @@
 """Seeded random configurations of the group-norm + SiLU call vs the fp64
-oracle: batch, groups, channels per group (past the 2048 channels that the
+oracle: batch, groups, channels per group (past the 1280 channels that the
 fused kernel stages in shared memory), ragged H*W, dtypes, value scale and
 offset, in place / out of place; the fused path is also checked bit for bit
 against the two-pass path with pieces of the same size."""
@@ -30,7 +30,7 @@ def random_case(seed):
     groups = int(g.choice([1, 2, 4, 8, 16, 32]))
     cpg = int(g.integers(1, 25))
     if seed % 6 == 0:
-        groups, cpg = 32, int(g.integers(65, 90))          # C > 2048: gamma / beta from global memory
+        groups, cpg = 32, int(g.integers(65, 90))          # C > 1280: gamma / beta from global memory
     n = int(g.integers(1, 4))
     c = groups * cpg
     # H*W a multiple of 8, sized so a case holds at most about 2 M elements
