@@ -18,8 +18,9 @@
 // subtraction well conditioned (it cancels only the spread of the row
 // around one of its own values).  The sums are reduced by shuffles inside
 // a warp and through shared memory and one named barrier across the group;
-// a second pass over the staged row writes the output, and the stage goes
-// back to the producer after that pass.
+// a second pass over the staged row writes ((x - K) * r - m1 * r) *
+// (1 + scale) + shift with m1 = S1/C and r = rsqrt(var + eps), and the
+// stage goes back to the producer after that pass.
 //
 // Every mbarrier wait is bounded.  The decision to continue is collective:
 // each warp posts whether its wait succeeded with its partial sums, and
@@ -244,8 +245,12 @@ __global__ void __launch_bounds__(kAdaMaxThreads, 1) adaln_kernel(const __grid_c
     const float2 R = make_float2(r, r);
     float2 first[4];
     Elem<T>::unpack(*reinterpret_cast<const uint4*>(st), first);
-    const float mu = __fadd_rn(first[0].x, m1);
-    const float2 nmu = make_float2(-mu, -mu);
+    // normalise as (x - K) * r - m1 * r: x - K is exact for nearby values
+    // and m1 is small, where x - (K + m1) would carry the rounding of the
+    // mean, ulps of a small result when |mean| is large against the spread
+    const float2 nk = make_float2(-first[0].x, -first[0].x);
+    const float c0 = __fmul_rn(-m1, r);
+    const float2 C0 = make_float2(c0, c0);
     // second pass over the staged row: normalise, modulate, store
     char* orow = p.out + row * p.out_stride;
 #pragma unroll UNROLL
@@ -257,7 +262,7 @@ __global__ void __launch_bounds__(kAdaMaxThreads, 1) adaln_kernel(const __grid_c
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const float2 sc1 = __fadd2_rn(sc[j], make_float2(1.0f, 1.0f));
-        o[j] = __ffma2_rn(__fmul2_rn(__fadd2_rn(X[j], nmu), R), sc1, sh[j]);
+        o[j] = __ffma2_rn(__ffma2_rn(__fadd2_rn(X[j], nk), R, C0), sc1, sh[j]);
       }
       store16(orow + k * 16, Elem<T>::pack(o));
     }

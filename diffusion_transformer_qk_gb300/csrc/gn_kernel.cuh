@@ -8,8 +8,9 @@
 // span's first element K (per-thread sums over 16-byte vectors, an fp32
 // xor tree in each warp, the warps' sums added in order).  Per span: the P
 // pieces' sums added in compensated fp32 in one fixed order (combine_span),
-// mean = K + S1/L, var = S2/L - (S1/L)^2, then per channel a = gamma[c] * rstd,
-// b = beta[c] - mean * a, and out = silu(x*a + b) = y / (1 + exp(-y)).
+// m1 = S1/L (the mean is K + m1), var = S2/L - m1^2, then per channel
+// a = gamma[c] * rstd, b = beta[c] - m1 * a, y = (x - K)*a + b and
+// out = silu(y) = y / (1 + exp(-y)).
 // (exp and the reciprocal on the special-function unit: ex2.approx and
 // rcp.approx, about 2 ulp.)
 //
@@ -35,6 +36,7 @@ namespace qknr {
 constexpr int kGnThreads = 256;
 constexpr int kGnWarps = kGnThreads / 32;
 constexpr int kGnBatch = 8;          // 16-byte loads a thread keeps in flight
+constexpr int kGnCoefFloats = 4;     // per span: m1, rstd, K (and one float of padding)
 
 struct GnParams {
   const char* x;
@@ -158,8 +160,9 @@ __device__ __forceinline__ Sum2 shfl_xor_sum2(const Sum2& v, int off) {
 // order: lane l adds pieces l, l+32, l+64, ... into compensated fp32 sums
 // (up to eight records in flight; the order of the additions does not
 // change), then an xor tree over the warp that ends with the same sums in
-// every lane; mean = K + S1/L, var = max(S2/L - (S1/L)^2, 0).  Called by
-// one whole warp; lane 0 writes coef[0] = mean, coef[1] = rstd.
+// every lane; the mean is K + m1 with m1 = S1/L, var = max(S2/L - m1^2, 0).
+// Called by one whole warp; lane 0 writes coef[0] = m1, coef[1] = rstd and
+// coef[2] = K (kGnCoefFloats floats).
 //
 // kWait (fused path): a record counts only once both its words carry
 // w->tag; a lane re-reads from its first record without it, so the records
@@ -243,16 +246,22 @@ __device__ __forceinline__ bool combine_span(const unsigned long long* rec, int 
     const float m1 = __fmul_rn(s1.value(), inv_l);
     float var = __fmaf_rn(-m1, m1, __fmul_rn(s2.value(), inv_l));
     var = var > 0.0f ? var : 0.0f;
-    coef[0] = __fadd_rn(tagged_value(kw), m1);
+    coef[0] = m1;
     coef[1] = rsqrtf(__fadd_rn(var, eps));
+    coef[2] = tagged_value(kw);
   }
   return true;
 }
 
-// Folded coefficients of channel c: a = gamma[c] * rstd, b = beta[c] - mean * a
-__device__ __forceinline__ void fold_channel(float g, float be, float mean, float rstd, float2& A, float2& B) {
+// Folded coefficients of channel c for x - K: a = gamma[c] * rstd and
+// b = beta[c] - m1 * a, so y = (x - K) * a + b.  Folding the whole mean
+// into b instead (y = x * a + b) would make y the difference of two fp32
+// terms of size |mean| * a, whose rounding costs several ulps of a small y
+// when |mean| is large against the spread; x - K is exact for nearby
+// values and m1 is small.
+__device__ __forceinline__ void fold_channel(float g, float be, float m1, float rstd, float2& A, float2& B) {
   const float a = __fmul_rn(g, rstd);
-  const float bb = __fmaf_rn(-mean, a, be);
+  const float bb = __fmaf_rn(-m1, a, be);
   A = make_float2(a, a);
   B = make_float2(bb, bb);
 }
@@ -274,21 +283,21 @@ __device__ __forceinline__ float rcp_approx(float x) {
   return y;
 }
 
-// silu(x*a + b) of one 16-byte vector (a vector never straddles a channel:
-// H*W is a multiple of 8): y = x*a + b, e^-y = 2^(-y * log2(e)) on the
+// silu((x - K)*a + b) of one 16-byte vector (a vector never straddles a
+// channel: H*W is a multiple of 8), NK = (-K, -K): y = (x - K)*a + b, e^-y = 2^(-y * log2(e)) on the
 // special-function unit, silu(y) = y * (1 / (1 + e^-y)), the fp32 steps on
 // paired instructions.  Saturates correctly: e^-y overflows to +inf for very
 // negative y, giving y * 0.
 constexpr float kNegLog2e = -1.4426950408889634f;    // -log2(e)
 
 template <typename T>
-__device__ __forceinline__ uint4 silu_affine(const uint4& raw, const float2& A, const float2& B) {
+__device__ __forceinline__ uint4 silu_affine(const uint4& raw, const float2& NK, const float2& A, const float2& B) {
   float2 X[4], O[4];
   Elem<T>::unpack(raw, X);
   const float2 nl = make_float2(kNegLog2e, kNegLog2e), one = make_float2(1.0f, 1.0f);
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    const float2 y = __ffma2_rn(X[j], A, B);
+    const float2 y = __ffma2_rn(__fadd2_rn(X[j], NK), A, B);
     const float2 t = __fmul2_rn(y, nl);
     const float2 d = __fadd2_rn(make_float2(ex2_approx(t.x), ex2_approx(t.y)), one);
     O[j] = __fmul2_rn(y, make_float2(rcp_approx(d.x), rcp_approx(d.y)));
@@ -348,7 +357,7 @@ __global__ void __launch_bounds__(kGnThreads) gn_stats_kernel(const __grid_const
 
 template <typename T>
 __global__ void __launch_bounds__(kGnThreads) gn_apply_kernel(const __grid_constant__ GnParams p) {
-  __shared__ float coef[2];                  // mean and 1/sqrt(var + eps) of the span
+  __shared__ float coef[kGnCoefFloats];      // m1, 1/sqrt(var + eps) and K of the span
   const int span = p.span0 + blockIdx.y;
   const int piece = blockIdx.x;
   const char* base = p.x + static_cast<long long>(span) * p.span_len * 2;
@@ -357,7 +366,8 @@ __global__ void __launch_bounds__(kGnThreads) gn_apply_kernel(const __grid_const
     combine_span<false>(p.rec + static_cast<long long>(span) * (p.pieces + 1) * 2, p.pieces, p.span_len, p.eps,
                         nullptr, coef);
   __syncthreads();
-  const float mean = coef[0], rstd = coef[1];
+  const float m1 = coef[0], rstd = coef[1];
+  const float2 nk = make_float2(-coef[2], -coef[2]);
   const int ch0 = (span % p.groups) * p.group_channels;
   const long long lo = static_cast<long long>(piece) * p.piece_len;
   long long hi = lo + p.piece_len;
@@ -381,9 +391,9 @@ __global__ void __launch_bounds__(kGnThreads) gn_apply_kernel(const __grid_const
       if (e >= ch_end) {
         const unsigned cl = channel_of(e, p.hw);
         ch_end = (static_cast<long long>(cl) + 1) * p.hw;
-        fold_channel(__ldg(p.gamma + ch0 + cl), __ldg(p.beta + ch0 + cl), mean, rstd, A, B);
+        fold_channel(__ldg(p.gamma + ch0 + cl), __ldg(p.beta + ch0 + cl), m1, rstd, A, B);
       }
-      store16(obase + e * 2, silu_affine<T>(v[b], A, B));
+      store16(obase + e * 2, silu_affine<T>(v[b], nk, A, B));
     }
   }
 }
@@ -455,7 +465,7 @@ constexpr int kGnfOffStatsDone = 388;                // chunks this CTA's stats 
 constexpr int kGnfOffMeta = 400;                     // [kGnfSlots][2]: first channel, next channel's first element
 constexpr int kGnfOffK = 512;                        // [kGnfSlots][16 bytes]: the span's first 16 bytes
 constexpr int kGnfOffRed = 768;                      // [2 * kGnWarps] floats
-constexpr int kGnfOffCoef = 896;                     // [kGnfCoefSlots][mean, rstd]
+constexpr int kGnfOffCoef = 896;                     // [kGnfCoefSlots][kGnCoefFloats]: m1, rstd, K
 constexpr int kGnfOffSlot0 = 1024;
 constexpr int kGnfOffGammaBeta = kGnfOffSlot0 + kGnfSlots * kGnfChunkBytes;   // gamma[C], beta[C]
 constexpr int kGnfMaxSmemChannels = 1280;            // larger C reads gamma / beta from global memory
@@ -467,7 +477,7 @@ static_assert(kGnfOffEmpty + 8 * kGnfSlots <= kGnfOffCoefFull, "shared memory ma
 static_assert(kGnfOffStatsDone + 4 <= kGnfOffMeta, "shared memory map");
 static_assert(kGnfOffK + 16 * kGnfSlots <= kGnfOffRed, "shared memory map");
 static_assert(kGnfOffMeta + 8 * kGnfSlots <= kGnfOffK, "shared memory map");
-static_assert(kGnfOffCoef + 8 * kGnfCoefSlots <= kGnfOffSlot0, "shared memory map");
+static_assert(kGnfOffCoef + 4 * kGnCoefFloats * kGnfCoefSlots <= kGnfOffSlot0, "shared memory map");
 static_assert(kGnfSmemBytes <= 227 * 1024, "shared memory map");
 
 struct GnFusedParams {
@@ -687,7 +697,7 @@ __global__ void __launch_bounds__(kGnfThreads, 1) gn_fused_kernel(const __grid_c
       if (!gnf_warp_wait(cempty0 + 8 * e, use_parity ^ 1u, limit, abort_cta, p.status)) break;
       if (!gnf_wait_local(stats_done, t_end, rw)) break;
       if (!combine_span<true>(p.rec + static_cast<long long>(span) * (P + 1) * 2, static_cast<int>(P), p.span_len,
-                              p.eps, &rw, coef + 2 * e))
+                              p.eps, &rw, coef + kGnCoefFloats * e))
         break;
       __syncwarp();
       if (lane == 0) mbar_arrive(cfull0 + 8 * e);    // release: the coefficients are visible
@@ -701,7 +711,8 @@ __global__ void __launch_bounds__(kGnfThreads, 1) gn_fused_kernel(const __grid_c
     unsigned cached_span = 0xffffffffu;
     unsigned nspans = 0;
     int ch0 = 0;
-    float mean = 0.0f, rstd = 0.0f;
+    float m1 = 0.0f, rstd = 0.0f;
+    float2 nk = make_float2(0.0f, 0.0f);
     int s = 0;
     uint32_t ph = 0;
     for (unsigned u = 0; u < mine; ++u, pos.advance(G, P)) {
@@ -715,8 +726,9 @@ __global__ void __launch_bounds__(kGnfThreads, 1) gn_fused_kernel(const __grid_c
         }
         const int e = static_cast<int>(nspans % kGnfCoefSlots);
         if (!gnf_warp_wait(cfull0 + 8 * e, (nspans / kGnfCoefSlots) & 1u, limit, abort_cta, p.status)) break;
-        mean = coef[2 * e];
-        rstd = coef[2 * e + 1];
+        m1 = coef[kGnCoefFloats * e];
+        rstd = coef[kGnCoefFloats * e + 1];
+        nk = make_float2(-coef[kGnCoefFloats * e + 2], -coef[kGnCoefFloats * e + 2]);
         ch0 = static_cast<int>(span % static_cast<unsigned>(p.groups)) * p.group_channels;
         cached_span = span;
         ++nspans;
@@ -733,7 +745,7 @@ __global__ void __launch_bounds__(kGnfThreads, 1) gn_fused_kernel(const __grid_c
       float2 A, B;
       {
         const int ch = ch0 + static_cast<int>(meta.x);
-        fold_channel(gb_smem ? sgamma[ch] : __ldg(p.gamma + ch), gb_smem ? sbeta[ch] : __ldg(p.beta + ch), mean, rstd,
+        fold_channel(gb_smem ? sgamma[ch] : __ldg(p.gamma + ch), gb_smem ? sbeta[ch] : __ldg(p.beta + ch), m1, rstd,
                      A, B);
       }
       auto one = [&](int v) {
@@ -743,10 +755,10 @@ __global__ void __launch_bounds__(kGnfThreads, 1) gn_fused_kernel(const __grid_c
           const unsigned cl = e / hw;
           ch_end = (cl + 1u) * hw;
           const int ch = ch0 + static_cast<int>(cl);
-          fold_channel(gb_smem ? sgamma[ch] : __ldg(p.gamma + ch), gb_smem ? sbeta[ch] : __ldg(p.beta + ch), mean,
+          fold_channel(gb_smem ? sgamma[ch] : __ldg(p.gamma + ch), gb_smem ? sbeta[ch] : __ldg(p.beta + ch), m1,
                        rstd, A, B);
         }
-        store16(obase + v * 16, silu_affine<T>(raw, A, B));
+        store16(obase + v * 16, silu_affine<T>(raw, nk, A, B));
       };
       if (nvec == kGnfChunk / 8) {
 #pragma unroll

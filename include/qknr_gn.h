@@ -13,7 +13,10 @@
  * rounded once into the activation dtype.  The statistics are sums around
  * the group's first element K, S1 = sum (x - K), S2 = sum (x - K)^2, taken
  * per piece in fp32 and combined in compensated fp32 (about twice fp32's
- * precision): mean = K + S1/L, var = S2/L - (S1/L)^2.
+ * precision): mean = K + S1/L, var = S2/L - (S1/L)^2; the output is
+ * formed from x - K, as (x - K) * a + (beta - (S1/L) * a) with a = gamma *
+ * rsqrt(var + eps), so a group whose mean is large against its spread keeps
+ * its small differences (x - K is exact for nearby values).
  *
  * A group is large and there are few of them, so each is cut into pieces
  * whose statistics go to a caller-provided device workspace.  Two paths:

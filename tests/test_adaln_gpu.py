@@ -80,6 +80,24 @@ def test_hidden_sizes_full(C, dtype):
     check(w, to_bits(res), inp)
 
 
+@pytest.mark.parametrize("dtype,spread,mean", [("fp16", 0.05, -30.0), ("fp16", 0.01, -8.0), ("bf16", 0.05, -30.0),
+                                               ("fp16", 1.0, -200.0), ("bf16", 0.02, 60.0)])
+def test_large_mean_small_spread(dtype, spread, mean):
+    # rows whose mean is hundreds of times their spread: the small
+    # differences must not be lost to the rounding of the mean (every output
+    # of magnitude >= 2^-6 within 1 ulp of the rounded oracle)
+    g = np.random.Generator(np.random.PCG64(64))
+    T, C, rpb = 300, 3072, 150
+    xb = I.to_storage_bits((g.standard_normal((T, C)) * spread + mean).astype(np.float32), dtype)
+    sc = (0.1 * g.standard_normal((2, C))).astype(np.float32)
+    sh = (0.1 * g.standard_normal((2, C))).astype(np.float32)
+    res = Q.adaln_modulate(to_dev(xb, dtype), torch.from_numpy(sc).cuda(), torch.from_numpy(sh).cuda(),
+                           rows_per_batch=rpb, eps=1e-6)
+    torch.cuda.synchronize()
+    ref = A.adaln_modulate(xb, dtype, sc, sh, "fp32", 1e-6, rpb)
+    compare(to_bits(res), ref, dtype, f"mean {mean}, spread {spread}")
+
+
 @pytest.mark.parametrize("T,rpb", [(1, 1), (2, 1), (151, 7), (152, 152), (1000, 1), (4099, 4099), (4099, 100)])
 def test_ragged_rows_and_batches(T, rpb):
     w = I.AdaLNWorkload("r", 1, rpb, 512, mod_dtype="bf16", seed=T)

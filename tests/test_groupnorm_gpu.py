@@ -139,6 +139,21 @@ def test_fused_equals_two_pass_with_the_same_pieces(shape, groups, dtype):
         compare(to_bits(a), ref, dtype, "fused")
 
 
+@pytest.mark.parametrize("dtype,spread,mean", [("fp16", 0.05, -30.0), ("fp16", 0.01, -8.0), ("bf16", 0.05, -30.0),
+                                               ("bf16", 0.02, 60.0)])
+@pytest.mark.parametrize("mode", ["fused", "two_pass"])
+def test_large_mean_small_spread(dtype, spread, mean, mode):
+    # groups whose mean is hundreds of times their spread: the small
+    # differences must not be lost to the rounding of the mean (every output
+    # of magnitude >= 2^-6 within 1 ulp of the rounded oracle)
+    w = I.GroupNormWorkload("m", 2, 64, 48, 40, groups=32, dtype=dtype, scale=spread, offset=mean, seed=65)
+    inp = I.make_gn_inputs(w)
+    res = gn_call(to_dev(inp["x"], dtype), w, inp, mode=mode)
+    torch.cuda.synchronize()
+    ref = G.group_norm_silu(inp["x"], dtype, w.groups, inp["gamma"], inp["beta"], w.eps)
+    compare(to_bits(res), ref, dtype, f"mean {mean}, spread {spread}")
+
+
 def test_fused_in_place_equals_out_of_place_and_repeats():
     w = I.GroupNormWorkload("ip", 2, 64, 96, 96, groups=32, scale=2.0, seed=41)
     inp = I.make_gn_inputs(w)
