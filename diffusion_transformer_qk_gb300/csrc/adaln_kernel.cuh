@@ -12,15 +12,15 @@
 // in flight.  Lane l of warp w of a group of GW warps handles the 16-byte
 // chunks k = (w*32 + l) + i*32*GW of the staged row.
 //
-// Statistics in one pass over the staged row, around a shift K = x[0] of
-// the row: S1 = sum (x - K), S2 = sum (x - K)^2, so mean = K + S1/C and
-// var = S2/C - (S1/C)^2.  Shifting by an element of the row keeps the
-// subtraction well conditioned (it cancels only the spread of the row
-// around one of its own values).  The sums are reduced by shuffles inside
-// a warp and through shared memory and one named barrier across the group;
-// a second pass over the staged row writes ((x - K) * r - m1 * r) *
-// (1 + scale) + shift with m1 = S1/C and r = rsqrt(var + eps), and the
-// stage goes back to the producer after that pass.
+// Statistics in one pass over the staged row (moments.cuh): each thread
+// sums x - k and (x - k)^2 over its values around its own first value k,
+// which gives its count, its mean relative to the row's first element K
+// and its sum of squared deviations; these parts are merged by shuffles
+// inside a warp and, through shared memory and one named barrier, across
+// the group's warps, into m1 = mean - K and var.  A second pass over
+// the staged row writes ((x - K) * r - m1 * r) * (1 + scale) + shift with
+// r = rsqrt(var + eps), and the stage goes back to the producer after that
+// pass.
 //
 // Every mbarrier wait is bounded.  The decision to continue is collective:
 // each warp posts whether its wait succeeded with its partial sums, and
@@ -28,6 +28,7 @@
 // can be left waiting at a named barrier for one that gave up.
 #pragma once
 
+#include "moments.cuh"
 #include "qknr_ptx.cuh"
 
 namespace qknr {
@@ -174,6 +175,8 @@ __global__ void __launch_bounds__(kAdaMaxThreads, 1) adaln_kernel(const __grid_c
   const int n_chunks = p.hidden / 8;
   const int lane_g = gw * 32 + lane;
   const float eps = p.eps, inv_c = p.inv_c;
+  // values this thread sums per row: chunks lane_g, lane_g + gthreads, ...
+  const float my_n = lane_g < n_chunks ? 8.0f * static_cast<float>((n_chunks - 1 - lane_g) / gthreads + 1) : 0.0f;
   const int ring0 = grp * S;
 
   int s = 0;
@@ -191,11 +194,19 @@ __global__ void __launch_bounds__(kAdaMaxThreads, 1) adaln_kernel(const __grid_c
     const unsigned char* st = smem + kAdaOffStage0 + (ring0 + s) * p.stage_bytes;
 
     float2 a1 = make_float2(0.0f, 0.0f), a2 = make_float2(0.0f, 0.0f);
+    float k_minus_k0 = 0.0f;
     if (ok) {
-      // one pass: sums of (x - K) and (x - K)^2, K = the row's first element
-      float2 first[4];
+      // one pass: sums of (x - k) and (x - k)^2, k = the first value of this
+      // thread's first chunk
+      float2 first[4], mine[4];
       Elem<T>::unpack(*reinterpret_cast<const uint4*>(st), first);
-      const float2 nk = make_float2(-first[0].x, -first[0].x);
+      float kt = 0.0f;
+      if (lane_g < n_chunks) {
+        Elem<T>::unpack(*reinterpret_cast<const uint4*>(st + lane_g * 16), mine);
+        kt = mine[0].x;
+      }
+      k_minus_k0 = __fsub_rn(kt, first[0].x);
+      const float2 nk = make_float2(-kt, -kt);
 #pragma unroll UNROLL
       for (int k = lane_g; k < n_chunks; k += gthreads) {
         float2 X[4];
@@ -208,21 +219,17 @@ __global__ void __launch_bounds__(kAdaMaxThreads, 1) adaln_kernel(const __grid_c
         }
       }
     }
-    float s1 = __fadd_rn(a1.x, a1.y), s2 = __fadd_rn(a2.x, a2.y);
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1) {
-      s1 = __fadd_rn(s1, __shfl_xor_sync(0xffffffffu, s1, off));
-      s2 = __fadd_rn(s2, __shfl_xor_sync(0xffffffffu, s2, off));
-    }
-    // post the warp's sums and whether its wait succeeded.  Rows alternate
+    const Moments wm = warp_moments(moments_of(my_n, k_minus_k0, __fadd_rn(a1.x, a1.y), __fadd_rn(a2.x, a2.y)),
+                                    warp_count(gw, n_chunks, gthreads, 8));
+    // post the warp's part and whether its wait succeeded.  Rows alternate
     // between two buffers: a warp can start the next row's posting while a
-    // slower one still reads this row's sums, but cannot get two rows ahead
+    // slower one still reads this row's parts, but cannot get two rows ahead
     // without passing the next row's barrier.
     float* part = part_base + parity * 3 * kAdaMaxWarps;
     parity ^= 1;
     if (lane == 0) {
-      part[gw] = s1;
-      part[kAdaMaxWarps + gw] = s2;
+      part[gw] = wm.u;
+      part[kAdaMaxWarps + gw] = wm.m;
       part[2 * kAdaMaxWarps + gw] = ok ? 1.0f : 0.0f;
     }
     // this row's sample's modulation rows (the same for every row of the
@@ -231,23 +238,24 @@ __global__ void __launch_bounds__(kAdaMaxThreads, 1) adaln_kernel(const __grid_c
     const char* hrow = p.shift + batch * p.mod_stride;
     named_barrier(bar_id, gthreads);
     bool all_ok = true;
-    float t1 = 0.0f, t2 = 0.0f;
+    const float ref = part[0];                    // warp 0 holds values whenever the row does
+    RefSums sums;
     for (int w = 0; w < GW; ++w) {
-      t1 = __fadd_rn(t1, part[w]);
-      t2 = __fadd_rn(t2, part[kAdaMaxWarps + w]);
+      sums.add(Moments{warp_count(w, n_chunks, gthreads, 8), part[w], part[kAdaMaxWarps + w]}, ref);
       all_ok = all_ok && part[2 * kAdaMaxWarps + w] != 0.0f;
     }
     if (!all_ok) break;                           // every warp of the group leaves together
-    const float m1 = __fmul_rn(t1, inv_c);        // mean of (x - K)
-    float var = __fmaf_rn(-m1, m1, __fmul_rn(t2, inv_c));
-    var = var > 0.0f ? var : 0.0f;
+    const Moments row_m = merged(static_cast<float>(p.hidden), ref, sums);
+    const float m1 = row_m.u;                     // mean - K
+    const float var = __fmul_rn(row_m.m, inv_c);
     const float r = rsqrtf(__fadd_rn(var, eps));
     const float2 R = make_float2(r, r);
     float2 first[4];
     Elem<T>::unpack(*reinterpret_cast<const uint4*>(st), first);
     // normalise as (x - K) * r - m1 * r: x - K is exact for nearby values
-    // and m1 is small, where x - (K + m1) would carry the rounding of the
-    // mean, ulps of a small result when |mean| is large against the spread
+    // and m1 = mean - K is rounded only to its own size, where x - (K + m1)
+    // would carry the rounding of the mean itself, ulps of a small result
+    // when |mean| is large against the spread
     const float2 nk = make_float2(-first[0].x, -first[0].x);
     const float c0 = __fmul_rn(-m1, r);
     const float2 C0 = make_float2(c0, c0);

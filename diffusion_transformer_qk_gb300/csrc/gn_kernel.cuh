@@ -4,13 +4,13 @@
 // Activations are NCHW, so the (C/G)*H*W elements of sample n, group g are
 // one contiguous span.  A group has few and large spans (32 groups of up to
 // millions of elements in a VAE decoder), so each span is cut into P pieces.
-// Per piece: fp32 sums S1 = sum (x - K) and S2 = sum (x - K)^2 around the
-// span's first element K (per-thread sums over 16-byte vectors, an fp32
-// xor tree in each warp, the warps' sums added in order).  Per span: the P
-// pieces' sums added in compensated fp32 in one fixed order (combine_span),
-// m1 = S1/L (the mean is K + m1), var = S2/L - m1^2, then per channel
-// a = gamma[c] * rstd, b = beta[c] - m1 * a, y = (x - K)*a + b and
-// out = silu(y) = y / (1 + exp(-y)).
+// Per piece: its count, mean relative to the span's first element K and
+// sum of squared deviations (moments.cuh: each thread's part from fp32 sums
+// around its own first element, merged pairwise in an xor tree in each
+// warp, the warps' parts merged in order).  Per span: the P pieces' parts
+// merged pairwise in one fixed order (combine_span) into m1 (the mean is
+// K + m1) and var, then per channel a = gamma[c] * rstd, b = beta[c] -
+// m1 * a, y = (x - K)*a + b and out = silu(y) = y / (1 + exp(-y)).
 // (exp and the reciprocal on the special-function unit: ex2.approx and
 // rcp.approx, about 2 ulp.)
 //
@@ -22,13 +22,14 @@
 //     the comment above it).
 //
 // Workspace records, 16 bytes per piece and one more per span: two 8-byte
-// words, each (tag << 32) | the bits of an fp32 value: (S1, S2) for piece
-// i < P, (K, 0) at index P.  An 8-byte store is single-copy atomic, so a
+// words, each (tag << 32) | the bits of an fp32 value: (mean - K, sum of
+// squared deviations) for piece i < P, (K, 0) at index P.  An 8-byte store is single-copy atomic, so a
 // word that carries the expected tag also carries its value: the fused
 // path's waits look for its per-call tag, with no counter and no fence.
 // The two-pass path writes tag 0 and does not look at tags.
 #pragma once
 
+#include "moments.cuh"
 #include "qknr_ptx.cuh"
 
 namespace qknr {
@@ -76,31 +77,31 @@ __device__ __forceinline__ ulonglong2 ld_record(const unsigned long long* p) {
   return make_ulonglong2(a, b);
 }
 
-// The statistics of one piece from per-thread fp32 pair sums: fp32 xor tree
-// in each warp, warp sums added in order by thread 0.  `red` holds 2 *
-// kGnWarps floats; `sync` is the barrier over the kGnThreads threads.
-// Valid in thread 0.
+// The part of one piece (moments.cuh) from per-thread fp32 pair sums a1, a2
+// of x - k over the thread's n values, k its first value (k_minus_k0 = k -
+// K): an xor tree in each warp, then thread 0 merges the warps' parts in
+// order (warp w covers vectors tid, tid + kGnThreads, ... of the piece's
+// nvec 16-byte vectors for its lanes tid).  `red` holds 2 * kGnWarps floats;
+// `sync` is the barrier over the kGnThreads threads.  Valid in thread 0.
 template <typename Sync>
-__device__ __forceinline__ void piece_sums(float2 a1, float2 a2, float* red, Sync sync, float* s1, float* s2) {
-  float v1 = __fadd_rn(a1.x, a1.y), v2 = __fadd_rn(a2.x, a2.y);
-#pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) {
-    v1 = __fadd_rn(v1, __shfl_xor_sync(0xffffffffu, v1, off));
-    v2 = __fadd_rn(v2, __shfl_xor_sync(0xffffffffu, v2, off));
-  }
+__device__ __forceinline__ Moments piece_moments(float2 a1, float2 a2, float n, float k_minus_k0, int nvec,
+                                                 float* red, Sync sync) {
+  const Moments mine = moments_of(n, k_minus_k0, __fadd_rn(a1.x, a1.y), __fadd_rn(a2.x, a2.y));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const Moments wp = warp_moments(mine, warp_count(warp, nvec, kGnThreads, 8));
   if (lane == 0) {
-    red[warp] = v1;
-    red[kGnWarps + warp] = v2;
+    red[warp] = wp.u;
+    red[kGnWarps + warp] = wp.m;
   }
   sync();
-  float t1 = 0.0f, t2 = 0.0f;
+  Moments t{0.0f, 0.0f, 0.0f};
   if (threadIdx.x == 0) {
-    for (int w = 0; w < kGnWarps; ++w) t1 = __fadd_rn(t1, red[w]);
-    for (int w = 0; w < kGnWarps; ++w) t2 = __fadd_rn(t2, red[kGnWarps + w]);
+    const float r = red[0];                      // warp 0 holds values whenever the piece does
+    RefSums sums;
+    for (int w = 0; w < kGnWarps; ++w) sums.add(Moments{warp_count(w, nvec, kGnThreads, 8), red[w], red[kGnWarps + w]}, r);
+    t = merged(8.0f * static_cast<float>(nvec), r, sums);
   }
-  *s1 = t1;
-  *s2 = t2;
+  return t;
 }
 
 // Bounded-wait context of the fused path's record polls.
@@ -126,43 +127,14 @@ __device__ __forceinline__ void give_up(const RecordWait& w) {
   if (w.status) atomicCAS(w.status, 0, kStatusTimeout);
 }
 
-// Compensated fp32 sums (Neumaier's variant of Kahan summation): hi + lo
-// carries the sum with about twice fp32's precision.  GB300's fp64 rate is
-// a small fraction of its fp32 rate, so the per-span combine stays in fp32.
-struct Sum2 {
-  float hi = 0.0f, lo = 0.0f;
-  __device__ __forceinline__ void add(float x) {
-    const float t = __fadd_rn(hi, x);
-    lo = __fadd_rn(lo, fabsf(hi) >= fabsf(x) ? __fadd_rn(__fsub_rn(hi, t), x) : __fadd_rn(__fsub_rn(x, t), hi));
-    hi = t;
-  }
-  // hi + lo of two compensated sums: the rounding error of hi + o.hi is
-  // exact (Knuth's TwoSum), so the result does not depend on the order of
-  // the two operands
-  __device__ __forceinline__ void merge(const Sum2& o) {
-    const float s = __fadd_rn(hi, o.hi);
-    const float bb = __fsub_rn(s, hi);
-    const float e = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bb)), __fsub_rn(o.hi, bb));
-    lo = __fadd_rn(__fadd_rn(lo, o.lo), e);
-    hi = s;
-  }
-  __device__ __forceinline__ float value() const { return __fadd_rn(hi, lo); }
-};
-
-__device__ __forceinline__ Sum2 shfl_xor_sum2(const Sum2& v, int off) {
-  Sum2 o;
-  o.hi = __shfl_xor_sync(0xffffffffu, v.hi, off);
-  o.lo = __shfl_xor_sync(0xffffffffu, v.lo, off);
-  return o;
-}
-
 // Mean and 1/sqrt(var + eps) of a span from its records, in one fixed
-// order: lane l adds pieces l, l+32, l+64, ... into compensated fp32 sums
-// (up to eight records in flight; the order of the additions does not
-// change), then an xor tree over the warp that ends with the same sums in
-// every lane; the mean is K + m1 with m1 = S1/L, var = max(S2/L - m1^2, 0).
-// Called by one whole warp; lane 0 writes coef[0] = m1, coef[1] = rstd and
-// coef[2] = K (kGnCoefFloats floats).
+// order: lane l sums pieces l, l+32, l+64, ... around the mean of its first
+// one (up to eight records in flight; the order of the additions does not
+// change), then the lanes' parts are merged by an xor tree (moments.cuh);
+// with m1 the mean relative to K, var = m / L.  Pieces hold
+// piece_len elements, the last one the rest of the span.  Called by one
+// whole warp; lane 0 writes coef[0] = m1, coef[1] = rstd and coef[2] = K
+// (kGnCoefFloats floats).
 //
 // kWait (fused path): a record counts only once both its words carry
 // w->tag; a lane re-reads from its first record without it, so the records
@@ -170,12 +142,15 @@ __device__ __forceinline__ Sum2 shfl_xor_sum2(const Sum2& v, int off) {
 // when a lane gave up (bounded by w->limit_ns, or another CTA gave up).
 template <bool kWait>
 __device__ __forceinline__ bool combine_span(const unsigned long long* rec, int pieces, long long span_len,
-                                             float eps, const RecordWait* w, float* coef) {
+                                             long long piece_len, float eps, const RecordWait* w, float* coef) {
   constexpr int kBatch = 8;
   const int lane = threadIdx.x & 31;
   // the shift K (written with piece 0's sums), loaded with the first batch
   unsigned long long kw = lane == 0 ? ld_record(rec + 2 * pieces).x : 0ull;
-  Sum2 s1, s2;
+  float nl = 0.0f, rl = 0.0f;                        // this lane's count and reference
+  RefSums sl;
+  const float full_n = static_cast<float>(piece_len);
+  const float last_n = static_cast<float>(span_len - static_cast<long long>(pieces - 1) * piece_len);
   bool ok = true;
   unsigned long long t0 = 0;
   unsigned backoff = 32;                             // ns between polls, doubling to 1 us
@@ -192,8 +167,11 @@ __device__ __forceinline__ bool combine_span(const unsigned long long* rec, int 
 #pragma unroll
     for (int b = 0; b < kBatch; ++b) {
       if (!stop && i + 32 * b < pieces && (!kWait || (tag_of(v[b].x) == w->tag && tag_of(v[b].y) == w->tag))) {
-        s1.add(tagged_value(v[b].x));
-        s2.add(tagged_value(v[b].y));
+        const int k = i + 32 * b;
+        const Moments pc{k == pieces - 1 ? last_n : full_n, tagged_value(v[b].x), tagged_value(v[b].y)};
+        if (nl == 0.0f) rl = pc.u;
+        sl.add(pc, rl);
+        nl = __fadd_rn(nl, pc.n);
         ++took;
       } else {
         stop = true;
@@ -235,18 +213,10 @@ __device__ __forceinline__ bool combine_span(const unsigned long long* rec, int 
     }
   }
   if (!__all_sync(0xffffffffu, ok)) return false;
-#pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) {
-    const Sum2 o1 = shfl_xor_sum2(s1, off), o2 = shfl_xor_sum2(s2, off);
-    s1.merge(o1);
-    s2.merge(o2);
-  }
+  const Moments acc = warp_moments(merged(nl, rl, sl), static_cast<float>(span_len));
   if (lane == 0) {
-    const float inv_l = __frcp_rn(static_cast<float>(span_len));
-    const float m1 = __fmul_rn(s1.value(), inv_l);
-    float var = __fmaf_rn(-m1, m1, __fmul_rn(s2.value(), inv_l));
-    var = var > 0.0f ? var : 0.0f;
-    coef[0] = m1;
+    const float var = __fmul_rn(acc.m, __frcp_rn(static_cast<float>(span_len)));
+    coef[0] = acc.u;
     coef[1] = rsqrtf(__fadd_rn(var, eps));
     coef[2] = tagged_value(kw);
   }
@@ -320,7 +290,17 @@ __global__ void __launch_bounds__(kGnThreads) gn_stats_kernel(const __grid_const
   if (hi > p.span_len) hi = p.span_len;
   float2 first[4];
   Elem<T>::unpack(__ldg(reinterpret_cast<const uint4*>(base)), first);
-  const float2 nk = make_float2(-first[0].x, -first[0].x);
+  // this thread's vectors are tid, tid + kGnThreads, ... of the piece's
+  // nvec; its sums are taken around the first value of its first vector
+  const int nvec = static_cast<int>((hi - lo) / 8);
+  const int my_vec = static_cast<int>(threadIdx.x) < nvec ? (nvec - 1 - static_cast<int>(threadIdx.x)) / kGnThreads + 1 : 0;
+  float kt = 0.0f;
+  if (my_vec > 0) {
+    float2 f[4];
+    Elem<T>::unpack(__ldg(reinterpret_cast<const uint4*>(base + (lo + threadIdx.x * 8) * 2)), f);
+    kt = f[0].x;
+  }
+  const float2 nk = make_float2(-kt, -kt);
   float2 a1 = make_float2(0.0f, 0.0f), a2 = make_float2(0.0f, 0.0f);
   // kGnBatch independent 16-byte loads in flight per thread before any is used
   constexpr long long kStride = kGnThreads * 8;
@@ -345,11 +325,11 @@ __global__ void __launch_bounds__(kGnThreads) gn_stats_kernel(const __grid_const
       }
     }
   }
-  float s1, s2;
-  piece_sums(a1, a2, red, CtaSync(), &s1, &s2);
+  const Moments pm = piece_moments(a1, a2, 8.0f * static_cast<float>(my_vec), __fsub_rn(kt, first[0].x), nvec, red,
+                                   CtaSync());
   if (threadIdx.x == 0) {
     unsigned long long* rec = p.rec + static_cast<long long>(span) * (p.pieces + 1) * 2;
-    st_record(rec + 2 * piece, tagged(0u, s1), tagged(0u, s2));
+    st_record(rec + 2 * piece, tagged(0u, pm.u), tagged(0u, pm.m));
     // the shift, kept here because an in-place apply overwrites x
     if (piece == 0) st_record(rec + 2 * p.pieces, tagged(0u, first[0].x), tagged(0u, 0.0f));
   }
@@ -363,8 +343,8 @@ __global__ void __launch_bounds__(kGnThreads) gn_apply_kernel(const __grid_const
   const char* base = p.x + static_cast<long long>(span) * p.span_len * 2;
   char* obase = p.out + static_cast<long long>(span) * p.span_len * 2;
   if (threadIdx.x < 32)
-    combine_span<false>(p.rec + static_cast<long long>(span) * (p.pieces + 1) * 2, p.pieces, p.span_len, p.eps,
-                        nullptr, coef);
+    combine_span<false>(p.rec + static_cast<long long>(span) * (p.pieces + 1) * 2, p.pieces, p.span_len,
+                        p.piece_len, p.eps, nullptr, coef);
   __syncthreads();
   const float m1 = coef[0], rstd = coef[1];
   const float2 nk = make_float2(-coef[2], -coef[2]);
@@ -697,7 +677,7 @@ __global__ void __launch_bounds__(kGnfThreads, 1) gn_fused_kernel(const __grid_c
       if (!gnf_warp_wait(cempty0 + 8 * e, use_parity ^ 1u, limit, abort_cta, p.status)) break;
       if (!gnf_wait_local(stats_done, t_end, rw)) break;
       if (!combine_span<true>(p.rec + static_cast<long long>(span) * (P + 1) * 2, static_cast<int>(P), p.span_len,
-                              p.eps, &rw, coef + kGnCoefFloats * e))
+                              kGnfChunk, p.eps, &rw, coef + kGnCoefFloats * e))
         break;
       __syncwarp();
       if (lane == 0) mbar_arrive(cfull0 + 8 * e);    // release: the coefficients are visible
@@ -797,8 +777,17 @@ __global__ void __launch_bounds__(kGnfThreads, 1) gn_fused_kernel(const __grid_c
     const int nvec = static_cast<int>(rest < kGnfChunk ? rest : kGnfChunk) / 8;
     float2 first[4];
     Elem<T>::unpack(*reinterpret_cast<const uint4*>(smem + kGnfOffK + 16 * s), first);
-    const float2 nk = make_float2(-first[0].x, -first[0].x);
     const unsigned char* slot = smem + kGnfOffSlot0 + s * kGnfChunkBytes;
+    // vectors tid, tid + kGnfStatsThreads, ... of the chunk, summed around
+    // the first value of the first one (as gn_stats_kernel)
+    const int my_vec = tid < nvec ? (nvec - 1 - tid) / kGnfStatsThreads + 1 : 0;
+    float kt = 0.0f;
+    if (my_vec > 0) {
+      float2 f[4];
+      Elem<T>::unpack(*reinterpret_cast<const uint4*>(slot + tid * 16), f);
+      kt = f[0].x;
+    }
+    const float2 nk = make_float2(-kt, -kt);
     float2 a1 = make_float2(0.0f, 0.0f), a2 = make_float2(0.0f, 0.0f);
     auto one = [&](int v) {
       float2 X[4];
@@ -821,12 +810,12 @@ __global__ void __launch_bounds__(kGnfThreads, 1) gn_fused_kernel(const __grid_c
     // this warp has read the slot for the last time
     __syncwarp();
     if (lane == 0) mbar_arrive(empty0 + 8 * s);
-    float s1, s2;
-    piece_sums(a1, a2, red, GnfStatsSync(), &s1, &s2);
+    const Moments pm = piece_moments(a1, a2, 8.0f * static_cast<float>(my_vec), __fsub_rn(kt, first[0].x), nvec,
+                                     red, GnfStatsSync());
     if (tid == 0) {
       if (!(p.flags & kGnfFlagStallRecords)) {
         unsigned long long* rec = p.rec + static_cast<long long>(span) * (P + 1) * 2;
-        st_record(rec + 2 * piece, tagged(p.tag, s1), tagged(p.tag, s2));
+        st_record(rec + 2 * piece, tagged(p.tag, pm.u), tagged(p.tag, pm.m));
         if (piece == 0) st_record(rec + 2 * P, tagged(p.tag, first[0].x), tagged(p.tag, 0.0f));
       }
       *stats_done = t + 1;

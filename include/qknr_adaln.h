@@ -11,11 +11,14 @@
  *     out[c] = (x[c] - mean) * rsqrt(var + eps) * (1 + scale[b, c]) + shift[b, c]
  *
  * rounded once, to nearest even, into the activation dtype.  The kernel
- * takes mean and variance in fp32 from one pass of sums around a shift K =
- * x[0] of the row: S1 = sum (x - K), S2 = sum (x - K)^2, mean = K + S1/C,
- * var = S2/C - (S1/C)^2, and normalises as (x - K) * r - (S1/C) * r with
- * r = rsqrt(var + eps), so a row whose mean is large against its spread
- * keeps its small differences (x - K is exact for nearby values).
+ * takes mean and variance in fp32 from one pass over the row: each thread
+ * sums x - k and (x - k)^2 around its own first value k, and the threads'
+ * counts, means and sums of squared deviations are merged around the mean
+ * of one of them, so neither an outlier channel nor a large mean cancels
+ * the variance away.  With K = x[0] and m1 = mean - K it normalises as
+ * (x - K) * r - m1 * r with r = rsqrt(var + eps), so a row whose mean is
+ * large against its spread keeps its small differences (x - K is exact for
+ * nearby values).
  *
  * Ownership and errors follow qknr.h: the caller owns every buffer, the
  * library allocates nothing and never synchronises; argument errors return

@@ -10,13 +10,16 @@
  *     y[c, h, w] = (x - mean) / sqrt(var + eps) * gamma[c] + beta[c]
  *     out = y * sigmoid(y) = y / (1 + exp(-y))
  *
- * rounded once into the activation dtype.  The statistics are sums around
- * the group's first element K, S1 = sum (x - K), S2 = sum (x - K)^2, taken
- * per piece in fp32 and combined in compensated fp32 (about twice fp32's
- * precision): mean = K + S1/L, var = S2/L - (S1/L)^2; the output is
- * formed from x - K, as (x - K) * a + (beta - (S1/L) * a) with a = gamma *
- * rsqrt(var + eps), so a group whose mean is large against its spread keeps
- * its small differences (x - K is exact for nearby values).
+ * rounded once into the activation dtype.  The statistics are fp32: each
+ * thread sums x - k and (x - k)^2 around its own first value k, which gives
+ * its count, its mean and its sum of squared deviations; these parts are
+ * merged around the mean of one of them, in each warp, across a piece's
+ * warps and across a group's pieces, so neither an outlier nor a large mean
+ * cancels the variance away.  With K the group's first element and m1 =
+ * mean - K, the output is formed from x - K, as (x - K) * a + (beta - m1 *
+ * a) with a = gamma * rsqrt(var + eps), so a group whose mean is large
+ * against its spread keeps its small differences (x - K is exact for
+ * nearby values).
  *
  * A group is large and there are few of them, so each is cut into pieces
  * whose statistics go to a caller-provided device workspace.  Two paths:

@@ -51,3 +51,24 @@ def compare(got_bits: np.ndarray, ref: np.ndarray, dtype: str, what: str = ""):
     assert worst <= 1, f"{what}: {worst} ulp from the rounded oracle"
     frac = float((ulp != 0).mean()) if ulp.size else 0.0
     return max_abs, frac
+
+def ulp_of(v: np.ndarray, dtype: str) -> np.ndarray:
+    """The spacing of the 16-bit float format at magnitude |v| (normal range)."""
+    mant = {"bf16": 7, "fp16": 10}[dtype]
+    e = np.floor(np.log2(np.maximum(np.abs(v), 2.0 ** -14)))
+    return 2.0 ** (e - mant)
+
+
+def compare_ulps(got_bits: np.ndarray, ref: np.ndarray, dtype: str, ulps: int, what: str = ""):
+    """Assert every output is at most `ulps` units in the last place from the
+    correctly rounded fp64 oracle: |got - ref| <= (ulps + 1/2) spacings of
+    the format at max(|ref|, |got|, 2^-6).  A relative bound for outputs far
+    above 1 (where the pages' absolute limit is below one ulp) and the bound
+    at 2^-6 for smaller ones."""
+    got_bits = got_bits.reshape(ref.shape)
+    got = O.decode(got_bits, dtype)
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    scale = ulp_of(np.maximum(np.maximum(np.abs(ref), np.abs(got)), 2.0 ** -6), dtype)
+    worst = float((np.abs(got - ref) / scale).max()) - 0.5
+    assert worst <= ulps, f"{what}: {worst:.2f} ulps from the rounded oracle (bound {ulps})"
+    return worst

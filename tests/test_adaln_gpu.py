@@ -10,7 +10,7 @@ import torch
 from diffusion_transformer_qk_gb300 import inputs as I
 from diffusion_transformer_qk_gb300 import qknr as Q
 from oracle import adaln_oracle as A
-from tests.gpu_util import TORCH, compare, to_bits, to_dev
+from tests.gpu_util import TORCH, compare, compare_ulps, to_bits, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -96,6 +96,25 @@ def test_large_mean_small_spread(dtype, spread, mean):
     torch.cuda.synchronize()
     ref = A.adaln_modulate(xb, dtype, sc, sh, "fp32", 1e-6, rpb)
     compare(to_bits(res), ref, dtype, f"mean {mean}, spread {spread}")
+
+
+@pytest.mark.parametrize("dtype,C,bound", [("bf16", 6144, 1), ("bf16", 32768, 1), ("fp16", 6144, 1),
+                                           ("fp16", 32768, 3)])
+def test_outlier_channel_at_the_first_element(dtype, C, bound):
+    # channel 0, the shift of every row's sums, carries a massive activation
+    # (10 sqrt(C) against unit noise) that dominates the row's variance
+    g = np.random.Generator(np.random.PCG64(9))
+    T = 64
+    xf = g.standard_normal((T, C)).astype(np.float32)
+    xf[:, 0] = 10.0 * np.sqrt(C)
+    xb = I.to_storage_bits(xf, dtype)
+    sc = (0.1 * g.standard_normal((1, C))).astype(np.float32)
+    sh = (0.1 * g.standard_normal((1, C))).astype(np.float32)
+    res = Q.adaln_modulate(to_dev(xb, dtype), torch.from_numpy(sc).cuda(), torch.from_numpy(sh).cuda(),
+                           rows_per_batch=T, eps=1e-6)
+    torch.cuda.synchronize()
+    ref = A.adaln_modulate(xb, dtype, sc, sh, "fp32", 1e-6, T)
+    compare_ulps(to_bits(res), ref, dtype, bound, f"C {C}")
 
 
 @pytest.mark.parametrize("T,rpb", [(1, 1), (2, 1), (151, 7), (152, 152), (1000, 1), (4099, 4099), (4099, 100)])

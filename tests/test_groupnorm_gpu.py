@@ -6,7 +6,7 @@ import torch
 from diffusion_transformer_qk_gb300 import inputs as I
 from diffusion_transformer_qk_gb300 import qknr as Q
 from oracle import groupnorm_oracle as G
-from tests.gpu_util import compare, to_bits, to_dev
+from tests.gpu_util import compare, compare_ulps, to_bits, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -152,6 +152,24 @@ def test_large_mean_small_spread(dtype, spread, mean, mode):
     torch.cuda.synchronize()
     ref = G.group_norm_silu(inp["x"], dtype, w.groups, inp["gamma"], inp["beta"], w.eps)
     compare(to_bits(res), ref, dtype, f"mean {mean}, spread {spread}")
+
+
+@pytest.mark.parametrize("dtype,spike,bound", [("bf16", 300.0, 1), ("bf16", 3000.0, 1), ("fp16", 300.0, 1),
+                                               ("fp16", 3000.0, 4)])
+@pytest.mark.parametrize("mode", ["fused", "two_pass"])
+def test_outlier_at_the_first_element(dtype, spike, bound, mode):
+    # the group's first element, the shift of every piece's sums, is an
+    # outlier that carries most of the variance: the statistics must not
+    # cancel it away.  fp16 at spike 3000 keeps the mean offset (about
+    # -3000) to fp32 precision, a few spacings at outputs near 2^-6
+    w = I.GroupNormWorkload("o", 1, 64, 128, 128, groups=4, dtype=dtype, seed=5)    # 262144 per group
+    inp = I.make_gn_inputs(w)
+    x = inp["x"].copy()
+    x[0, 0, 0, 0] = I.to_storage_bits(np.array([spike], np.float32), dtype)[0]
+    res = gn_call(to_dev(x, dtype), w, inp, mode=mode)
+    torch.cuda.synchronize()
+    ref = G.group_norm_silu(x, dtype, w.groups, inp["gamma"], inp["beta"], w.eps)
+    compare_ulps(to_bits(res), ref, dtype, bound, f"spike {spike}")
 
 
 def test_fused_in_place_equals_out_of_place_and_repeats():
