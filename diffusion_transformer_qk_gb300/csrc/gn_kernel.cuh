@@ -247,12 +247,6 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
-__device__ __forceinline__ float rcp_approx(float x) {
-  float y;
-  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
 // silu((x - K)*a + b) of one 16-byte vector (a vector never straddles a
 // channel: H*W is a multiple of 8), NK = (-K, -K): y = (x - K)*a + b, e^-y = 2^(-y * log2(e)) on the
 // special-function unit, silu(y) = y * (1 / (1 + e^-y)), the fp32 steps on

@@ -30,7 +30,8 @@ struct Moments {
   float m;   // sum of squared deviations from the mean
 };
 
-__device__ __forceinline__ float rcp_fast(float x) {
+// 1/x on the special-function unit (rcp.approx, about 1 ulp)
+__device__ __forceinline__ float rcp_approx(float x) {
   float y;
   asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
@@ -40,7 +41,7 @@ __device__ __forceinline__ float rcp_fast(float x) {
 __device__ __forceinline__ Moments moments_of(float n, float k_minus_r, float s1, float s2) {
   Moments r{n, 0.0f, 0.0f};
   if (n > 0.0f) {
-    const float mean = __fmul_rn(s1, rcp_fast(n));          // mean of x - k
+    const float mean = __fmul_rn(s1, rcp_approx(n));        // mean of x - k
     r.u = __fadd_rn(k_minus_r, mean);
     r.m = fmaxf(__fmaf_rn(-s1, mean, s2), 0.0f);             // s2 - s1^2 / n
   }
@@ -62,7 +63,7 @@ struct RefSums {
 __device__ __forceinline__ Moments merged(float n, float r, const RefSums& s) {
   Moments o{n, 0.0f, 0.0f};
   if (n > 0.0f) {
-    const float da = __fmul_rn(s.a, rcp_fast(n));
+    const float da = __fmul_rn(s.a, rcp_approx(n));
     o.u = __fadd_rn(r, da);
     o.m = fmaxf(__fmaf_rn(-s.a, da, s.c), 0.0f);
   }
