@@ -14,8 +14,8 @@
 //
 // Statistics in one pass over the staged row (moments.cuh): each thread
 // sums x - k and (x - k)^2 over its values around its own first value k,
-// which gives its count, its mean relative to the row's first element K
-// and its sum of squared deviations; these parts are merged by shuffles
+// which gives its count, its mean relative to the row's shift K (the lower
+// median of its first 8 values) and its sum of squared deviations; these parts are merged by shuffles
 // inside a warp and, through shared memory and one named barrier, across
 // the group's warps, into m1 = mean - K and var.  A second pass over
 // the staged row writes ((x - K) * r - m1 * r) * (1 + scale) + shift with
@@ -194,18 +194,19 @@ __global__ void __launch_bounds__(kAdaMaxThreads, 1) adaln_kernel(const __grid_c
     const unsigned char* st = smem + kAdaOffStage0 + (ring0 + s) * p.stage_bytes;
 
     float2 a1 = make_float2(0.0f, 0.0f), a2 = make_float2(0.0f, 0.0f);
-    float k_minus_k0 = 0.0f;
+    float k_minus_k0 = 0.0f, K = 0.0f;
     if (ok) {
       // one pass: sums of (x - k) and (x - k)^2, k = the first value of this
       // thread's first chunk
       float2 first[4], mine[4];
       Elem<T>::unpack(*reinterpret_cast<const uint4*>(st), first);
+      K = shift_of_first8(first);
       float kt = 0.0f;
       if (lane_g < n_chunks) {
         Elem<T>::unpack(*reinterpret_cast<const uint4*>(st + lane_g * 16), mine);
         kt = mine[0].x;
       }
-      k_minus_k0 = __fsub_rn(kt, first[0].x);
+      k_minus_k0 = __fsub_rn(kt, K);
       const float2 nk = make_float2(-kt, -kt);
 #pragma unroll UNROLL
       for (int k = lane_g; k < n_chunks; k += gthreads) {
@@ -250,13 +251,11 @@ __global__ void __launch_bounds__(kAdaMaxThreads, 1) adaln_kernel(const __grid_c
     const float var = __fmul_rn(row_m.m, inv_c);
     const float r = rsqrtf(__fadd_rn(var, eps));
     const float2 R = make_float2(r, r);
-    float2 first[4];
-    Elem<T>::unpack(*reinterpret_cast<const uint4*>(st), first);
     // normalise as (x - K) * r - m1 * r: x - K is exact for nearby values
     // and m1 = mean - K is rounded only to its own size, where x - (K + m1)
     // would carry the rounding of the mean itself, ulps of a small result
     // when |mean| is large against the spread
-    const float2 nk = make_float2(-first[0].x, -first[0].x);
+    const float2 nk = make_float2(-K, -K);
     const float c0 = __fmul_rn(-m1, r);
     const float2 C0 = make_float2(c0, c0);
     // second pass over the staged row: normalise, modulate, store

@@ -4,10 +4,11 @@
 // Activations are NCHW, so the (C/G)*H*W elements of sample n, group g are
 // one contiguous span.  A group has few and large spans (32 groups of up to
 // millions of elements in a VAE decoder), so each span is cut into P pieces.
-// Per piece: its count, mean relative to the span's first element K and
-// sum of squared deviations (moments.cuh: each thread's part from fp32 sums
-// around its own first element, merged pairwise in an xor tree in each
-// warp, the warps' parts merged in order).  Per span: the P pieces' parts
+// Per piece: its count, its mean relative to the span's shift K (the lower
+// median of the span's first 8 values) and its sum of squared deviations
+// (moments.cuh: each thread's part from fp32 sums around its own first
+// element, merged in an xor tree in each warp, the warps' parts merged in
+// order).  Per span: the P pieces' parts
 // merged pairwise in one fixed order (combine_span) into m1 (the mean is
 // K + m1) and var, then per channel a = gamma[c] * rstd, b = beta[c] -
 // m1 * a, y = (x - K)*a + b and out = silu(y) = y / (1 + exp(-y)).
@@ -77,16 +78,13 @@ __device__ __forceinline__ ulonglong2 ld_record(const unsigned long long* p) {
   return make_ulonglong2(a, b);
 }
 
-// The part of one piece (moments.cuh) from per-thread fp32 pair sums a1, a2
-// of x - k over the thread's n values, k its first value (k_minus_k0 = k -
-// K): an xor tree in each warp, then thread 0 merges the warps' parts in
-// order (warp w covers vectors tid, tid + kGnThreads, ... of the piece's
-// nvec 16-byte vectors for its lanes tid).  `red` holds 2 * kGnWarps floats;
-// `sync` is the barrier over the kGnThreads threads.  Valid in thread 0.
+// The part of one piece (moments.cuh) from the threads' parts: an xor tree
+// in each warp, then thread 0 merges the warps' parts in order (warp w
+// covers vectors tid, tid + kGnThreads, ... of the piece's nvec 16-byte
+// vectors for its lanes tid).  `red` holds 2 * kGnWarps floats; `sync` is
+// the barrier over the kGnThreads threads.  Valid in thread 0.
 template <typename Sync>
-__device__ __forceinline__ Moments piece_moments(float2 a1, float2 a2, float n, float k_minus_k0, int nvec,
-                                                 float* red, Sync sync) {
-  const Moments mine = moments_of(n, k_minus_k0, __fadd_rn(a1.x, a1.y), __fadd_rn(a2.x, a2.y));
+__device__ __forceinline__ Moments piece_moments(const Moments& mine, int nvec, float* red, Sync sync) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const Moments wp = warp_moments(mine, warp_count(warp, nvec, kGnThreads, 8));
   if (lane == 0) {
@@ -284,18 +282,16 @@ __global__ void __launch_bounds__(kGnThreads) gn_stats_kernel(const __grid_const
   if (hi > p.span_len) hi = p.span_len;
   float2 first[4];
   Elem<T>::unpack(__ldg(reinterpret_cast<const uint4*>(base)), first);
+  const float K = shift_of_first8(first);
   // this thread's vectors are tid, tid + kGnThreads, ... of the piece's
-  // nvec; its sums are taken around the first value of its first vector
+  // nvec, in batches of kGnBatch; each batch is a part, summed around the
+  // first value of its first vector (so a large value holds down the
+  // precision of at most its batch), and the parts are merged around the
+  // first one.  A piece of at most kGnBatch vectors per thread is one batch,
+  // the fused kernel's stats warps' part.
   const int nvec = static_cast<int>((hi - lo) / 8);
-  const int my_vec = static_cast<int>(threadIdx.x) < nvec ? (nvec - 1 - static_cast<int>(threadIdx.x)) / kGnThreads + 1 : 0;
-  float kt = 0.0f;
-  if (my_vec > 0) {
-    float2 f[4];
-    Elem<T>::unpack(__ldg(reinterpret_cast<const uint4*>(base + (lo + threadIdx.x * 8) * 2)), f);
-    kt = f[0].x;
-  }
-  const float2 nk = make_float2(-kt, -kt);
-  float2 a1 = make_float2(0.0f, 0.0f), a2 = make_float2(0.0f, 0.0f);
+  float tn = 0.0f, tr = 0.0f;
+  RefSums ts;
   // kGnBatch independent 16-byte loads in flight per thread before any is used
   constexpr long long kStride = kGnThreads * 8;
   for (long long e0 = lo + threadIdx.x * 8; e0 < hi; e0 += kStride * kGnBatch) {
@@ -305,6 +301,12 @@ __global__ void __launch_bounds__(kGnThreads) gn_stats_kernel(const __grid_const
       const long long e = e0 + b * kStride;
       v[b] = e < hi ? __ldg(reinterpret_cast<const uint4*>(base + e * 2)) : make_uint4(0, 0, 0, 0);
     }
+    float2 f[4];
+    Elem<T>::unpack(v[0], f);
+    const float kb = f[0].x;
+    const float2 nk = make_float2(-kb, -kb);
+    float2 a1 = make_float2(0.0f, 0.0f), a2 = make_float2(0.0f, 0.0f);
+    float nb = 0.0f;
 #pragma unroll
     for (int b = 0; b < kGnBatch; ++b) {
       if (e0 + b * kStride < hi) {
@@ -316,16 +318,21 @@ __global__ void __launch_bounds__(kGnThreads) gn_stats_kernel(const __grid_const
           a1 = __fadd2_rn(a1, d);
           a2 = __ffma2_rn(d, d, a2);
         }
+        nb = __fadd_rn(nb, 8.0f);
       }
     }
+    const Moments bp = moments_of(nb, __fsub_rn(kb, K), __fadd_rn(a1.x, a1.y), __fadd_rn(a2.x, a2.y));
+    if (tn == 0.0f) tr = bp.u;
+    ts.add(bp, tr);
+    tn = __fadd_rn(tn, nb);
   }
-  const Moments pm = piece_moments(a1, a2, 8.0f * static_cast<float>(my_vec), __fsub_rn(kt, first[0].x), nvec, red,
-                                   CtaSync());
+  const Moments mine = tn == 0.0f ? Moments{0.0f, 0.0f, 0.0f} : merged(tn, tr, ts);
+  const Moments pm = piece_moments(mine, nvec, red, CtaSync());
   if (threadIdx.x == 0) {
     unsigned long long* rec = p.rec + static_cast<long long>(span) * (p.pieces + 1) * 2;
     st_record(rec + 2 * piece, tagged(0u, pm.u), tagged(0u, pm.m));
     // the shift, kept here because an in-place apply overwrites x
-    if (piece == 0) st_record(rec + 2 * p.pieces, tagged(0u, first[0].x), tagged(0u, 0.0f));
+    if (piece == 0) st_record(rec + 2 * p.pieces, tagged(0u, K), tagged(0u, 0.0f));
   }
 }
 
@@ -771,6 +778,7 @@ __global__ void __launch_bounds__(kGnfThreads, 1) gn_fused_kernel(const __grid_c
     const int nvec = static_cast<int>(rest < kGnfChunk ? rest : kGnfChunk) / 8;
     float2 first[4];
     Elem<T>::unpack(*reinterpret_cast<const uint4*>(smem + kGnfOffK + 16 * s), first);
+    const float K = shift_of_first8(first);
     const unsigned char* slot = smem + kGnfOffSlot0 + s * kGnfChunkBytes;
     // vectors tid, tid + kGnfStatsThreads, ... of the chunk, summed around
     // the first value of the first one (as gn_stats_kernel)
@@ -804,13 +812,14 @@ __global__ void __launch_bounds__(kGnfThreads, 1) gn_fused_kernel(const __grid_c
     // this warp has read the slot for the last time
     __syncwarp();
     if (lane == 0) mbar_arrive(empty0 + 8 * s);
-    const Moments pm = piece_moments(a1, a2, 8.0f * static_cast<float>(my_vec), __fsub_rn(kt, first[0].x), nvec,
-                                     red, GnfStatsSync());
+    const Moments pm = piece_moments(
+        moments_of(8.0f * static_cast<float>(my_vec), __fsub_rn(kt, K), __fadd_rn(a1.x, a1.y), __fadd_rn(a2.x, a2.y)),
+        nvec, red, GnfStatsSync());
     if (tid == 0) {
       if (!(p.flags & kGnfFlagStallRecords)) {
         unsigned long long* rec = p.rec + static_cast<long long>(span) * (P + 1) * 2;
         st_record(rec + 2 * piece, tagged(p.tag, pm.u), tagged(p.tag, pm.m));
-        if (piece == 0) st_record(rec + 2 * P, tagged(p.tag, first[0].x), tagged(p.tag, 0.0f));
+        if (piece == 0) st_record(rec + 2 * P, tagged(p.tag, K), tagged(p.tag, 0.0f));
       }
       *stats_done = t + 1;
     }

@@ -85,6 +85,24 @@ __device__ __forceinline__ Moments warp_moments(const Moments& v, float n_warp) 
   return merged(n_warp, r, s);
 }
 
+// The shift of a row's or group's statistics and output: the lower median
+// (4th smallest) of its first 8 values v.  It is one of the values, so x - K
+// is exact for values near it, and it lies among the bulk unless 4 of the 8
+// are outliers, which keeps mean - K small and exactly representable to
+// fp32 precision of its own size.  A sorting network of 19 compare-swaps.
+__device__ __forceinline__ float shift_of_first8(const float2 (&v)[4]) {
+  float a[8] = {v[0].x, v[0].y, v[1].x, v[1].y, v[2].x, v[2].y, v[3].x, v[3].y};
+  constexpr int kNet[19][2] = {{0, 2}, {1, 3}, {4, 6}, {5, 7}, {0, 4}, {1, 5}, {2, 6}, {3, 7}, {0, 1},
+                               {2, 3}, {4, 5}, {6, 7}, {2, 4}, {3, 5}, {1, 4}, {3, 6}, {1, 2}, {3, 4}, {5, 6}};
+#pragma unroll
+  for (int i = 0; i < 19; ++i) {
+    const float lo = fminf(a[kNet[i][0]], a[kNet[i][1]]), hi = fmaxf(a[kNet[i][0]], a[kNet[i][1]]);
+    a[kNet[i][0]] = lo;
+    a[kNet[i][1]] = hi;
+  }
+  return a[3];
+}
+
 // Values a warp covers when T threads take items j, j + T, j + 2T, ... of
 // V items of `per` values each: 32 * (V / T) items plus the warp's share of
 // the V % T left over, lanes 32w .. 32w + 31.

@@ -15,10 +15,11 @@
  * sums x - k and (x - k)^2 around its own first value k, and the threads'
  * counts, means and sums of squared deviations are merged around the mean
  * of one of them, so neither an outlier channel nor a large mean cancels
- * the variance away.  With K = x[0] and m1 = mean - K it normalises as
- * (x - K) * r - m1 * r with r = rsqrt(var + eps), so a row whose mean is
- * large against its spread keeps its small differences (x - K is exact for
- * nearby values).
+ * the variance away.  With K the lower median of x[0..7] (one of the row's
+ * values, among the bulk unless 4 of those 8 are outliers) and m1 = mean -
+ * K, it normalises as (x - K) * r - m1 * r with r = rsqrt(var + eps), so a
+ * row whose mean is large against its spread keeps its small differences
+ * (x - K is exact for nearby values).
  *
  * Ownership and errors follow qknr.h: the caller owns every buffer, the
  * library allocates nothing and never synchronises; argument errors return

@@ -15,11 +15,12 @@
  * its count, its mean and its sum of squared deviations; these parts are
  * merged around the mean of one of them, in each warp, across a piece's
  * warps and across a group's pieces, so neither an outlier nor a large mean
- * cancels the variance away.  With K the group's first element and m1 =
- * mean - K, the output is formed from x - K, as (x - K) * a + (beta - m1 *
- * a) with a = gamma * rsqrt(var + eps), so a group whose mean is large
- * against its spread keeps its small differences (x - K is exact for
- * nearby values).
+ * cancels the variance away.  With K the lower median of the group's
+ * first 8 values (one of its values, among the bulk unless 4 of those 8
+ * are outliers) and m1 = mean - K, the output is formed from x - K, as
+ * (x - K) * a + (beta - m1 * a) with a = gamma * rsqrt(var + eps), so a
+ * group whose mean is large against its spread keeps its small differences
+ * (x - K is exact for nearby values).
  *
  * A group is large and there are few of them, so each is cut into pieces
  * whose statistics go to a caller-provided device workspace.  Two paths:

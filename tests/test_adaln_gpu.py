@@ -98,9 +98,9 @@ def test_large_mean_small_spread(dtype, spread, mean):
     compare(to_bits(res), ref, dtype, f"mean {mean}, spread {spread}")
 
 
-@pytest.mark.parametrize("dtype,C,bound", [("bf16", 6144, 1), ("bf16", 32768, 1), ("fp16", 6144, 1),
-                                           ("fp16", 32768, 3)])
-def test_outlier_channel_at_the_first_element(dtype, C, bound):
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("C", [6144, 32768])
+def test_outlier_channel_at_the_first_element(dtype, C):
     # channel 0, the shift of every row's sums, carries a massive activation
     # (10 sqrt(C) against unit noise) that dominates the row's variance
     g = np.random.Generator(np.random.PCG64(9))
@@ -114,7 +114,7 @@ def test_outlier_channel_at_the_first_element(dtype, C, bound):
                            rows_per_batch=T, eps=1e-6)
     torch.cuda.synchronize()
     ref = A.adaln_modulate(xb, dtype, sc, sh, "fp32", 1e-6, T)
-    compare_ulps(to_bits(res), ref, dtype, bound, f"C {C}")
+    compare_ulps(to_bits(res), ref, dtype, 1, f"C {C}")
 
 
 @pytest.mark.parametrize("T,rpb", [(1, 1), (2, 1), (151, 7), (152, 152), (1000, 1), (4099, 4099), (4099, 100)])
