@@ -3,10 +3,10 @@
 //
 // A part of the values is (n, u, m): its count n, its mean u taken
 // relative to a reference R common to every part, and m, the sum of
-// squared deviations from its own mean.  A thread forms its part from sums
-// around its own first value k, s1 = sum (x - k) and s2 = sum (x - k)^2,
-// so the cancellation in m = s2 - s1^2 / n is bounded by the thread's own
-// few values.  Parts are merged around the mean r of one of them (the
+// squared deviations from its own mean.  A thread forms its part (or one
+// per batch of its values) from sums around its own first value k, s1 =
+// sum (x - k) and s2 = sum (x - k)^2, so the cancellation in m = s2 - s1^2
+// / n is bounded by those few values.  Parts are merged around the mean r of one of them (the
 // pairwise-update identity of Chan, Golub and LeVeque, "Updating formulae
 // and a pairwise algorithm for computing sample variances", 1979, summed
 // over all parts at once):
