@@ -214,6 +214,40 @@ def expand_per_head(table: np.ndarray, n_heads: int) -> np.ndarray:
         np.broadcast_to(table[:, None, :], (table.shape[0], n_heads, table.shape[1])))
 
 
+def per_head_tables(rows: int, n_heads: int, head_dim: int, rope_style: str, cos_dtype: str, seed: int,
+                    per_dim: bool = False) -> Tuple[np.ndarray, np.ndarray]:
+    """Per-head expanded cos/sin tables [rows, H, D] whose rows differ from
+    head to head: every (row, head, pair) gets its own angle, uniform in
+    [-pi, pi), drawn from numpy PCG64(seed) in fp32.  Both members of a pair
+    hold the pair's angle (interleaved: dims 2k, 2k+1; rotate-half: k,
+    k + D/2).  With ``per_dim`` every (row, head, dimension) gets an angle
+    of its own instead, so the two members of a pair differ too.
+
+    Returns fp32 arrays, or bf16 bit patterns when ``cos_dtype`` is bf16.
+    """
+    g = np.random.Generator(np.random.PCG64(seed))
+    D = head_dim
+    if per_dim:
+        full = g.uniform(-np.pi, np.pi, size=(rows, n_heads, D)).astype(np.float32)
+    else:
+        ang = g.uniform(-np.pi, np.pi, size=(rows, n_heads, D // 2)).astype(np.float32)
+        if rope_style == "interleaved":
+            full = np.repeat(ang, 2, axis=2)
+        elif rope_style == "rotate_half":
+            full = np.concatenate([ang, ang], axis=2)
+        else:
+            raise ValueError(rope_style)
+        del ang
+    c = np.cos(full)
+    s = np.sin(full)
+    del full
+    if cos_dtype == "bf16":
+        return to_storage_bits(c, "bf16"), to_storage_bits(s, "bf16")
+    if cos_dtype != "fp32":
+        raise ValueError(cos_dtype)
+    return np.ascontiguousarray(c), np.ascontiguousarray(s)
+
+
 # --------------------------------------------------------------------------
 # activations
 

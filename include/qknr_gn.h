@@ -123,8 +123,13 @@ size_t qknr_gn_sizeof_args(void);
  * fewer bytes).  It calls no allocator.
  *
  * The first call on a device looks up the array's device address (with
- * that device current) and caches it; make that first call before any
- * stream capture.  Every call on a device shares the one array, and
+ * that device current) and caches it for the life of the process; make
+ * that first call before any stream capture.  The cached address belongs
+ * to the context that was current then: after cudaDeviceReset() (or with
+ * another context made current on that device) the library's module is
+ * loaded again at an address the cache does not know, so do not use this
+ * entry point in a process that resets a device it has already used it
+ * on.  Every call on a device shares the one array, and
  * nothing in it needs clearing: the two-pass path reads only what the same
  * call wrote, and the fused path accepts only statistics tagged with its
  * own call's tag.  Calls whose kernels overlap on the GPU (different

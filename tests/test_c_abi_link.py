@@ -10,6 +10,7 @@ import subprocess
 import pytest
 
 from diffusion_transformer_qk_gb300 import build as B
+from diffusion_transformer_qk_gb300 import qknr as Q
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 INCLUDE = os.path.join(ROOT, "include")
@@ -73,7 +74,7 @@ int main(void) {
   CHECK(qknr_gn_query(&g, NULL) == QKNR_ERR_NULL, 45);
   g.mode = 7;
   CHECK(qknr_gn_workspace_bytes(&g, &ws) == QKNR_ERR_UNSUPPORTED, 46);
-  printf("ok\n");
+  printf("ok %d\n", QKNR_GN_NOALLOC_SCRATCH_BYTES);
   return 0;
 }
 """
@@ -94,4 +95,5 @@ def test_c99_program_links_and_runs(tmp_path, built_lib):
     assert r.returncode == 0, r.stderr
     run = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
     assert run.returncode == 0, (run.returncode, run.stdout, run.stderr)
-    assert run.stdout.strip() == "ok"
+    # the binding's copy of the no-allocation scratch size is the header's
+    assert run.stdout.strip() == f"ok {Q.GN_NOALLOC_SCRATCH_BYTES}"

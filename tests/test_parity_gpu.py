@@ -258,3 +258,108 @@ def test_host_pipeline_batch_broadcast_table():
         Q.HostPipeline(host.shape[1], torch.bfloat16, chunk_rows=700)(
             host, 24, 24, 24, 128, torch.from_numpy(inp["gamma_q"]), torch.from_numpy(inp["gamma_k"]),
             torch.from_numpy(inp["cos"]), torch.from_numpy(inp["sin"]))
+
+
+# ---------------------------------------------------------------------------
+# per-head expanded tables whose rows differ from head to head: head h of Q
+# and head h of K must read table row [t, h] ("VisualGen Wan: deduplicate
+# shared RoPE SMEM staging", Description: materialised per-head embeddings;
+# Test Coverage: shared and per-head tables).  Tables that repeat one row
+# for every head cannot tell a wrong head index from the right one; these
+# can.
+
+def _dev_table(t, cos_dtype):
+    return table_to_dev(t, cos_dtype)
+
+
+@pytest.mark.parametrize("out", [False, True], ids=["in_place", "out_of_place"])
+@pytest.mark.parametrize("cos_dtype", ["fp32", "bf16"])
+@pytest.mark.parametrize("style", ["interleaved", "rotate_half"])
+@pytest.mark.parametrize("H,D", [(24, 64), (24, 128), (40, 128)])
+def test_expanded_distinct_heads_packed(H, D, style, cos_dtype, out):
+    w = I.Workload("expanded_distinct", 1, 613, H, H, H, D, "bf16", True, style, cos_dtype, "per_head_expanded",
+                   "1d", (), (D,), seed=11)
+    inp = I.make_inputs(w)
+    ce, se = I.per_head_tables(w.seq, H, D, style, cos_dtype, seed=100 + H + D)
+    res, src = run_packed(w, inp, out=out, dev_tabs=(_dev_table(ce, cos_dtype), _dev_table(se, cos_dtype)))
+    ref = oracle_packed(w, inp, cos_layout="per_head_expanded", tables=(ce, se))
+    bits = to_bits(res)
+    compare(bits[:, : H * D], ref["q"], "bf16", "Q")
+    compare(bits[:, H * D:2 * H * D], ref["k"], "bf16", "K")
+    np.testing.assert_array_equal(bits[:, 2 * H * D:], ref["v"])
+    if out:
+        np.testing.assert_array_equal(to_bits(src), inp["qkv"])
+
+
+@pytest.mark.parametrize("style", ["interleaved", "rotate_half"])
+def test_expanded_distinct_per_dimension_angles(style):
+    # every dimension of every head has its own angle, so the two members of
+    # a pair read different table entries: the entry used for output d must
+    # be entry d of head h
+    H, D = 24, 128
+    w = I.Workload("expanded_per_dim", 1, 300, H, H, 0, D, "fp16", True, style, "fp32", "per_head_expanded",
+                   "1d", (), (D,), seed=12)
+    inp = I.make_inputs(w)
+    ce, se = I.per_head_tables(w.seq, H, D, style, "fp32", seed=5, per_dim=True)
+    res, _ = run_packed(w, inp, dev_tabs=(_dev_table(ce, "fp32"), _dev_table(se, "fp32")))
+    ref = oracle_packed(w, inp, cos_layout="per_head_expanded", tables=(ce, se))
+    bits = to_bits(res)
+    compare(bits[:, : H * D], ref["q"], "fp16", "Q")
+    compare(bits[:, H * D:], ref["k"], "fp16", "K")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+@pytest.mark.parametrize("cos_dtype", ["fp32", "bf16"])
+def test_expanded_distinct_heads_separate_tensors(dtype, cos_dtype):
+    # the per-tensor launch (k = NULL: one tensor's heads against the table)
+    # and the single-launch Q+K form (with a V copy), batch-broadcast table
+    H, D, S, B = 48, 128, 250, 2
+    T = B * S
+    g = np.random.Generator(np.random.PCG64(21))
+    xs = {n: I.to_storage_bits(g.standard_normal((T, H * D)).astype(np.float32), dtype) for n in "qkv"}
+    gq = (1 + 0.1 * g.standard_normal(D)).astype(np.float32)
+    gk = (1 + 0.1 * g.standard_normal(D)).astype(np.float32)
+    ce, se = I.per_head_tables(S, H, D, "rotate_half", cos_dtype, seed=22)
+    cos, sin = _dev_table(ce, cos_dtype), _dev_table(se, cos_dtype)
+    kw = dict(rope_style="rotate_half", cos_layout="per_head_expanded")
+    refs = {n: O.forward_separate(xs[n], dtype, H, D, gam, 1e-6, ce, se, cos_dtype, "rotate_half",
+                                  "per_head_expanded") for n, gam in (("q", gq), ("k", gk))}
+    # one launch per tensor
+    q, k = to_dev(xs["q"], dtype), to_dev(xs["k"], dtype)
+    Q.qk_norm_rope_tensor(q, H, D, torch.from_numpy(gq).cuda(), cos, sin, **kw)
+    Q.qk_norm_rope_tensor(k, H, D, torch.from_numpy(gk).cuda(), cos, sin, **kw)
+    torch.cuda.synchronize()
+    compare(to_bits(q), refs["q"], dtype, "Q per tensor")
+    compare(to_bits(k), refs["k"], dtype, "K per tensor")
+    # Q and K in one launch, out of place, V copied
+    q2, k2, v2 = (to_dev(xs[n], dtype) for n in "qkv")
+    qo, ko, vo = torch.empty_like(q2), torch.empty_like(k2), torch.empty_like(v2)
+    Q.qk_norm_rope_separate(q2, k2, H, D, torch.from_numpy(gq).cuda(), torch.from_numpy(gk).cuda(), cos, sin,
+                            v=v2, q_out=qo, k_out=ko, v_out=vo, **kw)
+    torch.cuda.synchronize()
+    compare(to_bits(qo), refs["q"], dtype, "Q single launch")
+    compare(to_bits(ko), refs["k"], dtype, "K single launch")
+    np.testing.assert_array_equal(to_bits(vo), xs["v"])
+    assert torch.equal(qo.view(torch.int16), q.view(torch.int16))
+    assert torch.equal(ko.view(torch.int16), k.view(torch.int16))
+    for n, t in (("q", q2), ("k", k2), ("v", v2)):
+        np.testing.assert_array_equal(to_bits(t), xs[n])
+
+
+@pytest.mark.parametrize("style,cos_dtype", [("interleaved", "fp32"), ("rotate_half", "fp32"),
+                                             ("interleaved", "bf16"), ("rotate_half", "bf16")])
+def test_wan_expanded_distinct_heads_sampled(wan, style, cos_dtype):
+    # the full Wan shape in the launch the benchmark times, with a table
+    # [32760, 40, 128] that differs per head; sampled rows vs the oracle
+    w0, inp = wan
+    w = w0.with_(rope_style=style, cos_dtype=cos_dtype, cos_layout="per_head_expanded")
+    H, D = w.n_heads_q, w.head_dim
+    ce, se = I.per_head_tables(w.tokens, H, D, style, cos_dtype, seed=31)
+    res, _ = run_packed(w, inp, dev_tabs=(_dev_table(ce, cos_dtype), _dev_table(se, cos_dtype)))
+    bits = to_bits(res)
+    rows = sample_rows(w.tokens, 96, seed=3)
+    sub = dict(inp, qkv=inp["qkv"][rows])
+    ref = oracle_packed(w, sub, cos_layout="per_head_expanded", tables=(ce[rows], se[rows]))
+    compare(bits[rows][:, : H * D], ref["q"], "bf16", "Q")
+    compare(bits[rows][:, H * D:2 * H * D], ref["k"], "bf16", "K")
+    np.testing.assert_array_equal(bits[:, 2 * H * D:], inp["qkv"][:, 2 * H * D:])

@@ -1,6 +1,7 @@
 """Seeded random configurations of the fused QK-norm + RoPE call vs the fp64
 oracle: shapes, dtypes, pairing, table dtype and layout, batch-broadcast
-tables, padded row strides, in place / out of place and launch knobs."""
+tables, padded row strides, in place / out of place and launch knobs.
+Per-head expanded tables hold a different angle for every head."""
 import numpy as np
 import pytest
 import torch
@@ -50,22 +51,22 @@ def test_random_configuration(seed):
     width = (hq + hk + hv) * D
     x = (g.standard_normal((T, width)) * c["scale"]).astype(np.float32)
     bits = I.to_storage_bits(x, c["dtype"])
-    ang = g.uniform(-np.pi, np.pi, size=(c["rows"], D // 2))
-    full = np.repeat(ang, 2, axis=1) if c["style"] == "interleaved" else np.concatenate([ang, ang], axis=1)
-    cos, sin = np.cos(full).astype(np.float32), np.sin(full).astype(np.float32)
-    if c["cos_dtype"] == "bf16":
-        cos, sin = I.to_storage_bits(cos, "bf16"), I.to_storage_bits(sin, "bf16")
+    if c["layout"] == "per_head_expanded":
+        # [rows, H, D] with an angle of its own per (row, head, pair)
+        cos, sin = I.per_head_tables(c["rows"], hq, D, c["style"], c["cos_dtype"], seed=5000 + seed)
+    else:
+        ang = g.uniform(-np.pi, np.pi, size=(c["rows"], D // 2))
+        full = np.repeat(ang, 2, axis=1) if c["style"] == "interleaved" else np.concatenate([ang, ang], axis=1)
+        cos, sin = np.cos(full).astype(np.float32), np.sin(full).astype(np.float32)
+        if c["cos_dtype"] == "bf16":
+            cos, sin = I.to_storage_bits(cos, "bf16"), I.to_storage_bits(sin, "bf16")
     gq = (1 + 0.1 * g.standard_normal(D)).astype(np.float32)
     gk = (1 + 0.1 * g.standard_normal(D)).astype(np.float32)
 
     def dev_tab(t):
         if c["cos_dtype"] == "fp32":
-            d = torch.from_numpy(t).cuda()
-        else:
-            d = to_dev(t, "bf16")
-        if c["layout"] == "per_head_expanded":
-            d = d[:, None, :].expand(d.shape[0], hq, D).contiguous()
-        return d
+            return torch.from_numpy(t).cuda()
+        return to_dev(t, "bf16")
 
     buf = torch.zeros((T, width + c["pad"]), dtype=torch.bfloat16 if c["dtype"] == "bf16" else torch.float16,
                       device="cuda")
@@ -86,7 +87,8 @@ def test_random_configuration(seed):
         call({})
     torch.cuda.synchronize()
     got = to_bits(out if out is not None else qkv)
-    ref = O.forward_packed(bits, c["dtype"], hq, hk, hv, D, gq, gk, 1e-6, cos, sin, c["cos_dtype"], c["style"])
+    ref = O.forward_packed(bits, c["dtype"], hq, hk, hv, D, gq, gk, 1e-6, cos, sin, c["cos_dtype"], c["style"],
+                           c["layout"])
     if hq:
         compare(got[:, : hq * D], ref["q"], c["dtype"], f"Q {c}")
     if hk:
