@@ -344,14 +344,15 @@ class Runner:
     a packed QKV activation, one per tensor (Q, then K) for FLUX.2's
     separate tensors."""
 
-    def __init__(self, w, dev, tune, status, tokens=None):
+    def __init__(self, w, dev, tune, status, tokens=None, inp=None):
         import torch
 
         from diffusion_transformer_qk_gb300 import qknr as Q
 
         self.Q, self.w, self.dev = Q, w, dev
         self.tokens = w.tokens if tokens is None else tokens
-        inp = I.make_inputs(w, tokens=self.tokens)
+        if inp is None:
+            inp = I.make_inputs(w, tokens=self.tokens)
         self.inp = inp
         D = w.head_dim
 
@@ -725,8 +726,169 @@ def run_ours(args, w):
                                 "sample": f"{nn} token rows in tasks of {rows} on {cores} processes, {dtn:.1f} s, "
                                           f"fp64 numpy, scaled to a full call of {run.tokens} rows by tokens",
                                 "single_thread": single}
+    if world == 1 and args.configs == "all" and w.name == DEFAULT_WORKLOAD and args.tokens is None:
+        line["configs"] = run_config_sweep(dev, status, args.config_steps, 5, peak)
+        line["configs_note"] = ("every workload and variant at its full size, default launch shapes, "
+                                f"{args.config_steps} calls each after 5 warm-up calls; frac = achieved / "
+                                f"{peak_kind} hbm_gbs {peak:.1f} GB/s; kernel sources sha256 "
+                                f"{kernel_source_hash()[:16]}")
     print(json.dumps(line), flush=True)
     return 0
+
+
+# ---------------------------------------------------------------------------
+# every workload and variant, timed in the same run as the headline
+
+# (workload, overrides): the five configurations the pages' kernels are
+# quoted on and their table, pairing, dtype and launch-form variants, then
+# the next rows (AdaLN scale/shift, VAE group norm + SiLU).  Consecutive
+# entries with the same activation shape, dtype and seed share one drawn
+# activation.
+CONFIG_SWEEP = (
+    ("tiny_256x24x64", {}),
+    ("dense_4096x24x128", {}),
+    ("dense_4096x24x128", {"dtype": "fp16"}),
+    ("wan_32760x40x128", {}),
+    ("wan_32760x40x128", {"rope_style": "rotate_half"}),
+    ("wan_32760x40x128_bf16cos", {}),
+    ("wan_32760x40x128_expanded", {}),
+    ("wan_32760x40x128_expanded", {"rope_style": "rotate_half"}),
+    ("wan_32760x40x128_expanded_bf16cos", {}),
+    ("wan_32760x40x128_expanded_bf16cos", {"rope_style": "rotate_half"}),
+    ("wan_32760x40x128_out_of_place", {}),
+    ("flux2_2x4608x48x128", {}),
+    ("flux2_2x4608x48x128_single_launch", {}),
+    ("flux2_2x4608x48x128", {"dtype": "fp16"}),
+    ("flux2_2x4608x48x128_single_launch", {"dtype": "fp16"}),
+    ("adaln_flux2_2x4608x6144", {}),
+    ("adaln_wan_32760x5120", {}),
+    ("gn_vae_1x128x1024x1024", {}),
+    ("gn_vae_1x256x512x512", {}),
+    ("gn_vae_1x512x256x256", {}),
+    ("gn_vae_1x512x128x128", {}),
+)
+
+
+def sweep_entry_name(name: str, over: dict) -> str:
+    return name + "".join(f"[{v}]" for v in over.values())
+
+
+def _activation_key(w):
+    if not isinstance(w, I.Workload):
+        return None
+    return (w.batch, w.seq, w.n_heads_q, w.n_heads_k, w.n_heads_v, w.head_dim, w.dtype, w.packed, w.scale,
+            w.seed)
+
+
+def time_steps(step, stream, steps: int, flush, dev) -> float:
+    """Seconds per step: with `flush` (a buffer of twice the L2) each step
+    follows a write of it and is timed by its own pair of CUDA events;
+    without, the steps run back to back between one pair of events."""
+    import torch
+
+    if flush is None:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / 1e3 / steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for i in range(steps):
+        flush.fill_(1.0)
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    return statistics.fmean(a.elapsed_time(b) for a, b in zip(starts, ends)) / 1e3
+
+
+def copy_rate(bytes_moved: int, flush, stream, dev, steps: int) -> float:
+    """GB/s of a device copy (torch copy_) that reads and writes
+    `bytes_moved` in all, timed like the kernel it is set against."""
+    import torch
+
+    n = max(8, bytes_moved // 4)
+    a = torch.ones(n, dtype=torch.bfloat16, device=dev)
+    b = torch.empty_like(a)
+    for _ in range(5):
+        b.copy_(a)
+    t = time_steps(lambda: b.copy_(a), stream, steps, flush, dev)
+    moved = 2 * a.numel() * a.element_size()
+    del a, b
+    return moved / t / 1e9
+
+
+def run_config_sweep(dev, status, steps: int, warmup: int, peak: float):
+    """Time every entry of CONFIG_SWEEP once (default launch shapes).  An
+    entry's step is one call of the workload: one launch, or for FLUX.2's
+    separate tensors one launch per tensor (Q, then K) back to back.  Calls
+    whose launches move under twice the L2 are flushed between calls and
+    timed per call; larger ones run back to back."""
+    import torch
+
+    stream = torch.cuda.current_stream(dev)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 0) or 129 * 2 ** 20
+    flush_buf = torch.empty(2 * l2 // 4, dtype=torch.float32, device=dev)
+    out = {}
+    cache_key, cache_inp = None, None
+    for name, over in CONFIG_SWEEP:
+        base = I.WORKLOADS.get(name) or I.ADALN_WORKLOADS.get(name) or I.GN_WORKLOADS[name]
+        w = base.with_(**over) if over else base
+        inp = None
+        key = _activation_key(w)
+        if key is not None:
+            if key != cache_key:
+                cache_key, cache_inp = None, None
+                cache_key, cache_inp = key, I.make_inputs(w)
+            inp = dict(cache_inp)
+            inp["cos"], inp["sin"] = I.rope_table(w)
+        if isinstance(w, I.GroupNormWorkload):
+            run = GroupNormRunner(w, dev, dict(gn_mode="auto"), status)
+        elif isinstance(w, I.AdaLNWorkload):
+            run = AdaLNRunner(w, dev, {}, status)
+        else:
+            run = Runner(w, dev, {}, status, inp=inp)
+        L = len(run.args)
+        step_bytes = run.bytes_per_launch * L
+        flush = flush_buf if run.bytes_per_launch < 2 * l2 else None
+        for _ in range(warmup):
+            run.step(stream)
+        torch.cuda.synchronize(dev)
+        t = time_steps(lambda: run.step(stream), stream, steps, flush, dev)
+        achieved = step_bytes / t / 1e9
+        copy = copy_rate(step_bytes, flush, stream, dev, min(steps, 100))
+        info = run.info
+        entry = {
+            "us_per_call": t * 1e6, "launches_per_call": L * getattr(run, "launches_per_call", 1),
+            "algorithmic_bytes": step_bytes, "achieved_gbs": achieved, "frac": achieved / peak,
+            "same_size_copy_gbs": copy, "frac_of_same_size_copy": achieved / copy,
+            "l2": ("flushed between calls (write of 2x L2), each call timed by its own pair of CUDA events"
+                   if flush is not None else
+                   "launches move more than 2x L2: calls back to back between one pair of CUDA events"),
+            "dtype": w.dtype, "kernel": info["kernel"],
+            "launch": {k: info[k] for k in ("grid", "block", "dyn_smem", "stages", "consumer_warps", "group_warps",
+                                            "registers") if k in info},
+        }
+        if isinstance(w, I.Workload):
+            entry.update(cos_dtype=w.cos_dtype, cos_layout=w.cos_layout, rope=w.rope_style,
+                         launch_form=(("packed, out of place (V copied)" if w.out_of_place else "packed, in place")
+                                      if w.packed else ("q+k in one launch" if w.single_launch
+                                                        else "one launch per tensor (Q, then K)")))
+        if L > 1:
+            entry["us_per_launch"] = t * 1e6 / L
+        st = int(status.item())
+        if st != 0:
+            raise RuntimeError(f"{name}: kernel reported status {st}")
+        out[sweep_entry_name(name, over)] = entry
+        del run
+        torch.cuda.empty_cache()
+    del flush_buf, cache_inp
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_copy_calibration(args):
@@ -794,6 +956,10 @@ def main(argv=None):
                    help="group-norm workloads: which path to time")
     p.add_argument("--copy-calibration", action="store_true",
                    help="print the device copy rate at the workloads' sizes (one JSON line each) and exit")
+    p.add_argument("--configs", choices=["all", "none"], default="all",
+                   help="with the default workload on one GPU: also time every workload and variant "
+                        "(the line's 'configs' object)")
+    p.add_argument("--config-steps", type=int, default=300)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
