@@ -726,7 +726,7 @@ def run_ours(args, w):
                                 "sample": f"{nn} token rows in tasks of {rows} on {cores} processes, {dtn:.1f} s, "
                                           f"fp64 numpy, scaled to a full call of {run.tokens} rows by tokens",
                                 "single_thread": single}
-    if world == 1 and args.configs == "all" and w.name == DEFAULT_WORKLOAD and args.tokens is None:
+    if world == 1 and args.configs == "all" and w == I.WORKLOADS[DEFAULT_WORKLOAD] and args.tokens is None:
         line["configs"] = run_config_sweep(dev, status, args.config_steps, 5, peak)
         line["configs_note"] = ("every workload and variant at its full size, default launch shapes, "
                                 f"{args.config_steps} calls each after 5 warm-up calls; frac = achieved / "
@@ -952,6 +952,8 @@ def main(argv=None):
     p.add_argument("--l2-flush", choices=["auto", "on", "off"], default="auto")
     p.add_argument("--dtype", choices=["bf16", "fp16"], default=None,
                    help="activation dtype of the workload (default: the workload's own, bf16)")
+    p.add_argument("--rope-style", choices=["interleaved", "rotate_half"], default=None,
+                   help="QK workloads: pairing (default: the workload's own)")
     p.add_argument("--gn-mode", choices=["auto", "fused", "two_pass"], default="auto",
                    help="group-norm workloads: which path to time")
     p.add_argument("--copy-calibration", action="store_true",
@@ -976,6 +978,8 @@ def main(argv=None):
         if isinstance(w, I.AdaLNWorkload) and w.mod_dtype != "fp32":
             kw["mod_dtype"] = args.dtype                  # modulation rows in the activation dtype
         w = w.with_(**kw)
+    if args.rope_style and isinstance(w, I.Workload) and args.rope_style != w.rope_style:
+        w = w.with_(rope_style=args.rope_style)
     if args.impl == "reference":
         if not isinstance(w, I.Workload):
             p.error("--impl reference times the QK-norm + RoPE oracle; pick a QK workload")

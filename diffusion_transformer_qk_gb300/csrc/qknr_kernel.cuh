@@ -9,13 +9,17 @@
 // stages, which it drains strictly in order (so a group never waits on a
 // stage phase more than one ahead of the barrier).  A group normalises and
 // rotates every head of its row in fp32 registers, stores the result with
-// 16-byte stores and hands the stage back.
+// 16-byte (interleaved) or 8-byte (rotate-half) stores and hands the stage
+// back.
 //
-// Lane mapping: a lane owns 8 consecutive dimensions (16 bytes) of a head,
-// so a head of D dims spans LPH = D/8 lanes and a warp covers HPW = 32/LPH
-// heads at once.  The per-head sum of squares is a shuffle-xor reduction
-// inside those LPH lanes; a rotate-half partner lives in lane ^ (LPH/2),
-// an interleaved partner in the same lane.  Consumer warps form groups
+// Lane mapping: a lane owns 8 dimensions (16 bytes) of a head, so a head of
+// D dims spans LPH = D/8 lanes and a warp covers HPW = 32/LPH heads at
+// once.  With interleaved pairing lane j of a head owns the consecutive dims
+// [8j, 8j+8) (one 16-byte access); with rotate-half pairing it owns
+// [4j, 4j+4) and [D/2+4j, D/2+4j+4) (two 8-byte accesses), so in both
+// styles every rotation partner sits in the same lane and the rotation
+// needs no shuffle.  The per-head sum of squares is a shuffle-xor reduction
+// inside the head's LPH lanes.  Consumer warps form groups
 // that each take whole rows, so several rows are in flight at once; inside
 // a group the warps are split between Q and K heads, so each folds only its
 // own tensor's gain, and a warp works on two passes of heads at a time to
@@ -93,50 +97,79 @@ template <int D, bool RH>
 struct Geometry {
   static constexpr int LPH = D / 8;       // lanes per head
   static constexpr int HPW = 32 / LPH;    // heads per warp pass
-  // true when element j of the lane is the first member of its pair
-  static __device__ __forceinline__ bool first_member(int d0, int j) {
-    return RH ? (d0 < D / 2) : ((j & 1) == 0);
-  }
+  // first dimension of the lane's low and high group of four (j = lane
+  // index within its head); interleaved: [8j, 8j+8), rotate-half: [4j, 4j+4)
+  // and its partners [D/2+4j, D/2+4j+4)
+  static __device__ __forceinline__ int lo(int j) { return RH ? 4 * j : 8 * j; }
+  static __device__ __forceinline__ int hi(int j) { return RH ? D / 2 + 4 * j : 8 * j + 4; }
 };
 
-// a[j] = g[d]*c[j]; b[j] = s(d) * g[p(d)] * s[j]  (each product rounded in fp32),
-// held as pairs A[i] = (a[2i], a[2i+1]).  gamma points at the tensor's gains
-// in shared memory.
+// The lane's 8 activation values of one head (16 bytes at `head` + lo and
+// + hi elements; one access when they are adjacent).
+template <bool RH>
+__device__ __forceinline__ uint4 load_lane8(const unsigned char* head, int lo, int hi) {
+  if (!RH) return *reinterpret_cast<const uint4*>(head + lo * 2);
+  const uint2 a = *reinterpret_cast<const uint2*>(head + lo * 2);
+  const uint2 b = *reinterpret_cast<const uint2*>(head + hi * 2);
+  return make_uint4(a.x, a.y, b.x, b.y);
+}
+
+template <bool RH>
+__device__ __forceinline__ void store_lane8(char* head, int lo, int hi, const uint4& v) {
+  if (!RH) {
+    store16(head + lo * 2, v);
+  } else {
+    store8(head + lo * 2, make_uint2(v.x, v.y));
+    store8(head + hi * 2, make_uint2(v.z, v.w));
+  }
+}
+
+// The lane's 8 cos (or sin) values of one table row, widened to fp32 pairs.
+template <typename CT, bool RH>
+__device__ __forceinline__ void load_table_lane(const unsigned char* row, int lo, int hi, float2 (&c)[4]) {
+  constexpr int CES = sizeof(CT);
+  if (!RH) {
+    load_table8<CT>(row + lo * CES, c);
+  } else {
+    float2 a[2], b[2];
+    load_table4<CT>(row + lo * CES, a);
+    load_table4<CT>(row + hi * CES, b);
+    c[0] = a[0]; c[1] = a[1]; c[2] = b[0]; c[3] = b[1];
+  }
+}
+
+// a[d] = g[d]*c[d]; b[d] = s(d) * g[p(d)] * s[d]  (each product rounded in fp32),
+// held as pairs A[i] for the lane's elements 2i, 2i+1 (see Geometry).
+// gamma points at the tensor's gains in shared memory.
 template <int D, bool RH>
-__device__ __forceinline__ void fold_coefficients(const float* gamma, int d0, const float2 (&C)[4],
+__device__ __forceinline__ void fold_coefficients(const float* gamma, int lo, int hi, const float2 (&C)[4],
                                                   const float2 (&Sn)[4], float2 (&A)[4], float2 (&B)[4]) {
-  const float4 g0 = *reinterpret_cast<const float4*>(gamma + d0);
-  const float4 g1 = *reinterpret_cast<const float4*>(gamma + d0 + 4);
+  const float4 g0 = *reinterpret_cast<const float4*>(gamma + lo);
+  const float4 g1 = *reinterpret_cast<const float4*>(gamma + hi);
   const float2 G[4] = {make_float2(g0.x, g0.y), make_float2(g0.z, g0.w), make_float2(g1.x, g1.y),
                        make_float2(g1.z, g1.w)};
+  // gains of the rotation partners: the other group of four (rotate-half),
+  // the other member of the same pair (interleaved)
   float2 GP[4];
-  if (RH) {
-    const int pd = (d0 + D / 2) % D;
-    const float4 p0 = *reinterpret_cast<const float4*>(gamma + pd);
-    const float4 p1 = *reinterpret_cast<const float4*>(gamma + pd + 4);
-    GP[0] = make_float2(p0.x, p0.y); GP[1] = make_float2(p0.z, p0.w);
-    GP[2] = make_float2(p1.x, p1.y); GP[3] = make_float2(p1.z, p1.w);
-  } else {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) GP[i] = make_float2(G[i].y, G[i].x);
-  }
+  for (int i = 0; i < 4; ++i) GP[i] = RH ? G[i ^ 2] : make_float2(G[i].y, G[i].x);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     A[i] = __fmul2_rn(G[i], C[i]);
     const float2 t = __fmul2_rn(GP[i], Sn[i]);
-    // first pair members take -partner*sin: even dims (interleaved), the
-    // lower half (rotate-half)
+    // first pair members take -partner*sin: the lower half (rotate-half),
+    // even dims (interleaved)
     if (RH)
-      B[i] = d0 < D / 2 ? make_float2(-t.x, -t.y) : t;
+      B[i] = i < 2 ? make_float2(-t.x, -t.y) : t;
     else
       B[i] = make_float2(-t.x, t.y);
   }
 }
 
 // Normalise and rotate the 8 elements this lane holds of one head (raw
-// storage in `raw`), giving fp32 outputs O[i] = (o[2i], o[2i+1]).  Every
-// lane of the warp must call it: the reduction and the partner exchange
-// shuffle the warp.
+// storage in `raw`, element order of Geometry), giving fp32 outputs O[i]
+// for elements 2i, 2i+1.  Every lane of the warp must call it: the
+// reduction shuffles the warp.
 template <typename T, int D, bool RH>
 __device__ __forceinline__ void head_math(const uint4& raw, const float2 (&A)[4], const float2 (&B)[4],
                                           float eps, float inv_d, float2 (&O)[4]) {
@@ -154,15 +187,11 @@ __device__ __forceinline__ void head_math(const uint4& raw, const float2 (&A)[4]
   for (int off = LPH / 2; off >= 1; off >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, off));
   const float r = rsqrtf(__fmaf_rn(ss, inv_d, eps));
   const float2 R = make_float2(r, r);
-  // XP[i] holds the rotation partners of X[i]
+  // XP[i] holds the rotation partners of X[i], all in this lane
   float2 XP[4];
   if (RH) {
-    uint4 pr;
-    pr.x = __shfl_xor_sync(0xffffffffu, raw.x, LPH / 2);
-    pr.y = __shfl_xor_sync(0xffffffffu, raw.y, LPH / 2);
-    pr.z = __shfl_xor_sync(0xffffffffu, raw.z, LPH / 2);
-    pr.w = __shfl_xor_sync(0xffffffffu, raw.w, LPH / 2);
-    Elem<T>::unpack(pr, XP);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) XP[i] = X[i ^ 2];
   } else {
     Elem<T>::unpack_swapped(raw, XP);
   }
@@ -183,15 +212,15 @@ __device__ __forceinline__ void process_tensor(const unsigned char* seg, const u
   constexpr int HPW = Geo::HPW;
   constexpr int ES = 2;
   constexpr int CES = sizeof(CT);
-  const int d0 = (lane % LPH) * 8;
+  const int lo = Geo::lo(lane % LPH), hi = Geo::hi(lane % LPH);
   const int hslot = lane / LPH;
   float2 a[4], b[4];
   if (!EXPANDED) {
     // the row's one cos/sin row, folded once for every head this lane visits
     float2 c[4], s[4];
-    load_table8<CT>(cos_s + d0 * CES, c);
-    load_table8<CT>(sin_s + d0 * CES, s);
-    fold_coefficients<D, RH>(gamma, d0, c, s, a, b);
+    load_table_lane<CT, RH>(cos_s, lo, hi, c);
+    load_table_lane<CT, RH>(sin_s, lo, hi, s);
+    fold_coefficients<D, RH>(gamma, lo, hi, c, s, a, b);
   }
   int t = lw;
   for (; t + G < n_pass; t += 2 * G) {
@@ -199,40 +228,40 @@ __device__ __forceinline__ void process_tensor(const unsigned char* seg, const u
     const int h1 = (t + G) * HPW + hslot;
     const bool act0 = h0 < n_heads, act1 = h1 < n_heads;
     const int hc0 = act0 ? h0 : 0, hc1 = act1 ? h1 : 0;
-    const uint4 r0 = *reinterpret_cast<const uint4*>(seg + (hc0 * D + d0) * ES);
-    const uint4 r1 = *reinterpret_cast<const uint4*>(seg + (hc1 * D + d0) * ES);
+    const uint4 r0 = load_lane8<RH>(seg + hc0 * D * ES, lo, hi);
+    const uint4 r1 = load_lane8<RH>(seg + hc1 * D * ES, lo, hi);
     float2 o0[4], o1[4];
     if (EXPANDED) {
       float2 c[4], s[4], a1[4], b1[4];
-      load_table8<CT>(cos_s + (hc0 * D + d0) * CES, c);
-      load_table8<CT>(sin_s + (hc0 * D + d0) * CES, s);
-      fold_coefficients<D, RH>(gamma, d0, c, s, a, b);
-      load_table8<CT>(cos_s + (hc1 * D + d0) * CES, c);
-      load_table8<CT>(sin_s + (hc1 * D + d0) * CES, s);
-      fold_coefficients<D, RH>(gamma, d0, c, s, a1, b1);
+      load_table_lane<CT, RH>(cos_s + hc0 * D * CES, lo, hi, c);
+      load_table_lane<CT, RH>(sin_s + hc0 * D * CES, lo, hi, s);
+      fold_coefficients<D, RH>(gamma, lo, hi, c, s, a, b);
+      load_table_lane<CT, RH>(cos_s + hc1 * D * CES, lo, hi, c);
+      load_table_lane<CT, RH>(sin_s + hc1 * D * CES, lo, hi, s);
+      fold_coefficients<D, RH>(gamma, lo, hi, c, s, a1, b1);
       head_math<T, D, RH>(r0, a, b, eps, inv_d, o0);
       head_math<T, D, RH>(r1, a1, b1, eps, inv_d, o1);
     } else {
       head_math<T, D, RH>(r0, a, b, eps, inv_d, o0);
       head_math<T, D, RH>(r1, a, b, eps, inv_d, o1);
     }
-    if (act0) store16(out_row + (h0 * D + d0) * ES, Elem<T>::pack(o0));
-    if (act1) store16(out_row + (h1 * D + d0) * ES, Elem<T>::pack(o1));
+    if (act0) store_lane8<RH>(out_row + h0 * D * ES, lo, hi, Elem<T>::pack(o0));
+    if (act1) store_lane8<RH>(out_row + h1 * D * ES, lo, hi, Elem<T>::pack(o1));
   }
   if (t < n_pass) {
     const int h0 = t * HPW + hslot;
     const bool act0 = h0 < n_heads;
     const int hc0 = act0 ? h0 : 0;
-    const uint4 r0 = *reinterpret_cast<const uint4*>(seg + (hc0 * D + d0) * ES);
+    const uint4 r0 = load_lane8<RH>(seg + hc0 * D * ES, lo, hi);
     if (EXPANDED) {
       float2 c[4], s[4];
-      load_table8<CT>(cos_s + (hc0 * D + d0) * CES, c);
-      load_table8<CT>(sin_s + (hc0 * D + d0) * CES, s);
-      fold_coefficients<D, RH>(gamma, d0, c, s, a, b);
+      load_table_lane<CT, RH>(cos_s + hc0 * D * CES, lo, hi, c);
+      load_table_lane<CT, RH>(sin_s + hc0 * D * CES, lo, hi, s);
+      fold_coefficients<D, RH>(gamma, lo, hi, c, s, a, b);
     }
     float2 o0[4];
     head_math<T, D, RH>(r0, a, b, eps, inv_d, o0);
-    if (act0) store16(out_row + (h0 * D + d0) * ES, Elem<T>::pack(o0));
+    if (act0) store_lane8<RH>(out_row + h0 * D * ES, lo, hi, Elem<T>::pack(o0));
   }
 }
 

@@ -179,10 +179,31 @@ __device__ __forceinline__ void load_table8<__nv_bfloat16>(const unsigned char* 
   Elem<__nv_bfloat16>::unpack(*reinterpret_cast<const uint4*>(p), c);
 }
 
+// 4 consecutive cos (or sin) values from shared memory, widened to fp32 pairs.
+template <typename CT>
+__device__ __forceinline__ void load_table4(const unsigned char* p, float2 (&c)[2]);
 
-// 16-byte streaming store to global memory (written once, not re-read).
+template <>
+__device__ __forceinline__ void load_table4<float>(const unsigned char* p, float2 (&c)[2]) {
+  const float4 a = *reinterpret_cast<const float4*>(p);
+  c[0] = make_float2(a.x, a.y); c[1] = make_float2(a.z, a.w);
+}
+
+template <>
+__device__ __forceinline__ void load_table4<__nv_bfloat16>(const unsigned char* p, float2 (&c)[2]) {
+  const uint2 w = *reinterpret_cast<const uint2*>(p);
+  c[0] = make_float2(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u));
+  c[1] = make_float2(__uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
+}
+
+
+// 16- and 8-byte streaming stores to global memory (written once, not re-read).
 __device__ __forceinline__ void store16(char* dst, const uint4& v) {
   __stcs(reinterpret_cast<uint4*>(dst), v);
+}
+
+__device__ __forceinline__ void store8(char* dst, const uint2& v) {
+  __stcs(reinterpret_cast<uint2*>(dst), v);
 }
 
 }  // namespace qknr
