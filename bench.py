@@ -578,7 +578,7 @@ def run_ours(args, w):
         tune = dict(gn_mode=args.gn_mode)
     else:
         tune = dict(ctas_per_sm=args.ctas_per_sm, stages=args.stages, consumer_warps=args.consumer_warps,
-                    group_warps=args.group_warps)
+                    group_warps=args.group_warps, flags=Q.FLAG_NO_OVERLAP if args.no_overlap else 0)
     runner = {I.AdaLNWorkload: AdaLNRunner, I.GroupNormWorkload: GroupNormRunner}.get(type(w), Runner)
     run = runner(w, dev, tune, status, args.tokens)
     stream = torch.cuda.current_stream(dev)
@@ -769,6 +769,11 @@ CONFIG_SWEEP = (
 )
 
 
+# workloads also timed with plain launches (no programmatic dependent
+# launch), beside the default entry
+SWEEP_PLAIN_LAUNCH = ("dense_4096x24x128", "flux2_2x4608x48x128")
+
+
 def sweep_entry_name(name: str, over: dict) -> str:
     return name + "".join(f"[{v}]" for v in over.values())
 
@@ -835,7 +840,12 @@ def run_config_sweep(dev, status, steps: int, warmup: int, peak: float):
     flush_buf = torch.empty(2 * l2 // 4, dtype=torch.float32, device=dev)
     out = {}
     cache_key, cache_inp = None, None
+    plan = []
     for name, over in CONFIG_SWEEP:
+        plan.append((name, over, False))
+        if not over and name in SWEEP_PLAIN_LAUNCH:
+            plan.append((name, over, True))
+    for name, over, plain in plan:
         base = I.WORKLOADS.get(name) or I.ADALN_WORKLOADS.get(name) or I.GN_WORKLOADS[name]
         w = base.with_(**over) if over else base
         inp = None
@@ -846,12 +856,15 @@ def run_config_sweep(dev, status, steps: int, warmup: int, peak: float):
                 cache_key, cache_inp = key, I.make_inputs(w)
             inp = dict(cache_inp)
             inp["cos"], inp["sin"] = I.rope_table(w)
+        from diffusion_transformer_qk_gb300 import qknr as Q
+
+        flags = dict(flags=Q.FLAG_NO_OVERLAP) if plain else {}
         if isinstance(w, I.GroupNormWorkload):
             run = GroupNormRunner(w, dev, dict(gn_mode="auto"), status)
         elif isinstance(w, I.AdaLNWorkload):
-            run = AdaLNRunner(w, dev, {}, status)
+            run = AdaLNRunner(w, dev, flags, status)
         else:
-            run = Runner(w, dev, {}, status, inp=inp)
+            run = Runner(w, dev, flags, status, inp=inp)
         L = len(run.args)
         step_bytes = run.bytes_per_launch * L
         flush = flush_buf if run.bytes_per_launch < 2 * l2 else None
@@ -880,10 +893,13 @@ def run_config_sweep(dev, status, steps: int, warmup: int, peak: float):
                                                         else "one launch per tensor (Q, then K)")))
         if L > 1:
             entry["us_per_launch"] = t * 1e6 / L
+        if not isinstance(w, I.GroupNormWorkload):
+            entry["launch_mode"] = ("plain stream order" if plain else
+                                    "programmatic dependent launch (the default)")
         st = int(status.item())
         if st != 0:
             raise RuntimeError(f"{name}: kernel reported status {st}")
-        out[sweep_entry_name(name, over)] = entry
+        out[sweep_entry_name(name, over) + ("[plain launch]" if plain else "")] = entry
         del run
         torch.cuda.empty_cache()
     del flush_buf, cache_inp
@@ -952,6 +968,8 @@ def main(argv=None):
     p.add_argument("--l2-flush", choices=["auto", "on", "off"], default="auto")
     p.add_argument("--dtype", choices=["bf16", "fp16"], default=None,
                    help="activation dtype of the workload (default: the workload's own, bf16)")
+    p.add_argument("--no-overlap", action="store_true",
+                   help="launch without programmatic dependent launch (plain stream order)")
     p.add_argument("--rope-style", choices=["interleaved", "rotate_half"], default=None,
                    help="QK workloads: pairing (default: the workload's own)")
     p.add_argument("--gn-mode", choices=["auto", "fused", "two_pass"], default="auto",

@@ -168,8 +168,8 @@ qknr_status plan(const qknr_adaln_args* a, AdaPlan* pl, bool size_device) {
   if (st != QKNR_OK) return st;
   const int block = 32 * (warps + 1);
   int occ = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, pl->fn, block, static_cast<size_t>(smem));
-  if (e != cudaSuccess) return qknr_host::cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+  st = qknr_host::occupancy(pl->fn, dev, block, static_cast<size_t>(smem), &occ);
+  if (st != QKNR_OK) return st;
   if (occ < 1) return fail(QKNR_ERR_UNSUPPORTED, "kernel does not fit on an SM with %lld B shared memory", smem);
   const int per_sm = cps < occ ? cps : occ;
   long long grid = (long long)di.num_sms * per_sm;
@@ -232,10 +232,9 @@ qknr_status qknr_adaln_forward(const qknr_adaln_args* args, qknr_stream_t stream
   st = plan(args, &pl, true);
   if (st != QKNR_OK) return st;
   void* kargs[] = {&pl.kp};
-  cudaError_t e = cudaLaunchKernel(pl.fn, dim3(pl.grid), dim3(pl.block), kargs, static_cast<size_t>(pl.smem),
-                                   reinterpret_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return qknr_host::cuda_fail(e, "cudaLaunchKernel");
-  return QKNR_OK;
+  return qknr_host::launch_kernel(pl.fn, pl.grid, pl.block, static_cast<size_t>(pl.smem),
+                                  reinterpret_cast<cudaStream_t>(stream), kargs, !(args->flags & QKNR_FLAG_NO_OVERLAP),
+                                  "cudaLaunchKernelExC(AdaLN)");
 }
 
 size_t qknr_adaln_sizeof_args(void) { return sizeof(qknr_adaln_args); }

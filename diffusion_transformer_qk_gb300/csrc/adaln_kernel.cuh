@@ -117,6 +117,9 @@ __global__ void __launch_bounds__(kAdaMaxThreads, 1) adaln_kernel(const __grid_c
     fence_barrier_init();
   }
   __syncthreads();
+  // all global memory accesses come after the previous kernel in the stream
+  // has completed (programmatic dependent launch; see the QK kernel)
+  grid_dependency_wait();
   const unsigned long long limit = p.wait_limit_ns;
 
   if (warp == NW) {
@@ -151,6 +154,7 @@ __global__ void __launch_bounds__(kAdaMaxThreads, 1) adaln_kernel(const __grid_c
         }
       }
     }
+    grid_dependents_launch();
     if (!ok || *abort_flag) {
       // wait (bounded) for the copies of the latest use of every stage
       const long long total = static_cast<long long>(n_groups) * S;

@@ -8,6 +8,7 @@
 #include <cstring>
 #include <map>
 #include <mutex>
+#include <tuple>
 #include <unordered_map>
 #include <utility>
 
@@ -77,6 +78,46 @@ qknr_status configure_kernel(const void* fn, int dev, const DeviceInfo& di, int*
     it = g_configured.emplace(key, fa.numRegs).first;
   }
   *regs = it->second;
+  return QKNR_OK;
+}
+
+qknr_status occupancy(const void* fn, int dev, int block, size_t smem, int* blocks_per_sm) {
+  static std::map<std::tuple<const void*, int, int, size_t>, int> cache;
+  const auto key = std::make_tuple(fn, dev, block, smem);
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) {
+      *blocks_per_sm = it->second;
+      return QKNR_OK;
+    }
+  }
+  int occ = 0;
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, block, smem);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+  std::lock_guard<std::mutex> lk(g_mu);
+  cache[key] = occ;
+  *blocks_per_sm = occ;
+  return QKNR_OK;
+}
+
+qknr_status launch_kernel(const void* fn, int grid, int block, size_t smem, cudaStream_t stream, void** kargs,
+                          bool overlap, const char* what) {
+  // programmatic stream serialization: the kernel may launch while the
+  // previous kernel in the stream finishes; it waits for that kernel
+  // before its first global memory access (griddepcontrol.wait)
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = overlap ? 1 : 0;
+  cudaError_t e = cudaLaunchKernelExC(&cfg, fn, kargs);
+  if (e != cudaSuccess) return cuda_fail(e, what);
   return QKNR_OK;
 }
 
@@ -372,8 +413,8 @@ qknr_status size_launch(const qknr_args* a, Plan* pl) {
                 stage_bytes, smem, di.smem_optin);
   const int block = 32 * (warps + 1);
   int occ = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, pl->fn, block, static_cast<size_t>(smem));
-  if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+  st = qknr_host::occupancy(pl->fn, dev, block, static_cast<size_t>(smem), &occ);
+  if (st != QKNR_OK) return st;
   if (occ < 1) return fail(QKNR_ERR_UNSUPPORTED, "kernel does not fit on an SM with %lld B shared memory", smem);
   const int per_sm = cps < occ ? cps : occ;
   long long grid = (long long)di.num_sms * per_sm;
@@ -448,10 +489,9 @@ qknr_status qknr_forward(const qknr_args* args, qknr_stream_t stream) {
   st = size_launch(args, &pl);
   if (st != QKNR_OK) return st;
   void* kargs[] = {&pl.kp};
-  cudaError_t e = cudaLaunchKernel(pl.fn, dim3(pl.grid), dim3(pl.block), kargs, static_cast<size_t>(pl.smem),
-                                   reinterpret_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return cuda_fail(e, "cudaLaunchKernel");
-  return QKNR_OK;
+  return qknr_host::launch_kernel(pl.fn, pl.grid, pl.block, static_cast<size_t>(pl.smem),
+                                  reinterpret_cast<cudaStream_t>(stream), kargs,
+                                  !(args->flags & qknr::kFlagNoOverlap), "cudaLaunchKernelExC");
 }
 
 const char* qknr_status_string(int32_t s) {

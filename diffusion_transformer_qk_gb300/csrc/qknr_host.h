@@ -31,6 +31,16 @@ qknr_status device_info(int dev, DeviceInfo* out);
 // (once per kernel and device) and return its register count.
 qknr_status configure_kernel(const void* fn, int dev, const DeviceInfo& di, int* regs);
 
+// Resident blocks per SM of `fn` at this block size and dynamic shared
+// memory on device `dev` (queried once per combination and cached).
+qknr_status occupancy(const void* fn, int dev, int block, size_t smem, int* blocks_per_sm);
+
+// Launch `fn` on `stream`; with `overlap`, with programmatic stream
+// serialization (the kernel must call griddepcontrol.wait before its first
+// global memory access).
+qknr_status launch_kernel(const void* fn, int grid, int block, size_t smem, cudaStream_t stream, void** kargs,
+                          bool overlap, const char* what);
+
 struct Span {
   uintptr_t lo, hi;   // [lo, hi)
 };

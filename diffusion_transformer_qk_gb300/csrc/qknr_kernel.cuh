@@ -56,6 +56,7 @@ constexpr int kOffStage0 = 2048;      // stage rings
 constexpr int kStageAlign = 128;
 
 constexpr unsigned kFlagTestStall = 1u;
+constexpr unsigned kFlagNoOverlap = 2u;     // host side only: plain launch
 
 struct KernelParams {
   const char* q;
@@ -293,11 +294,12 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qknr_fused_kernel(const __grid
     *abort_flag = 0;
     fence_barrier_init();
   }
-  for (int i = threadIdx.x; i < 2 * D; i += blockDim.x) {
-    const float* g = i < D ? p.gamma_q : p.gamma_k;
-    gam[i] = g ? g[i < D ? i : i - D] : 1.0f;
-  }
   __syncthreads();
+  // Nothing above touches global memory, so under programmatic dependent
+  // launch it overlaps the end of the kernel before this one in the stream.
+  // Every global read and write comes after this wait: the inputs may be
+  // that kernel's outputs, and an in-place output may be its input.
+  grid_dependency_wait();
 
   const unsigned long long limit = p.wait_limit_ns;
 
@@ -360,6 +362,9 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qknr_fused_kernel(const __grid
         }
       }
     }
+    // every load of this CTA is issued: the next kernel in the stream may
+    // start launching (its CTAs take an SM as this grid's CTAs leave it)
+    grid_dependents_launch();
     if (!ok || *abort_flag) {
       // copies of the last n_groups * S issued rows (the latest use of every
       // stage) may still be landing: wait for them before this CTA's shared
@@ -379,6 +384,14 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qknr_fused_kernel(const __grid
   }
 
   // ---------------- consumer warps
+  // The gains go to shared memory while the producer's first loads are in
+  // flight; the consumer warps alone wait for them (named barrier 1).
+  for (int i = threadIdx.x; i < 2 * D; i += NW * 32) {
+    const float* g = i < D ? p.gamma_q : p.gamma_k;
+    gam[i] = g ? g[i < D ? i : i - D] : 1.0f;
+  }
+  named_barrier_sync(1, NW * 32);
+
   // The consumer warps form NW / GW groups of GW warps; group g takes the
   // CTA's rows g, g + NW/GW, ... so several rows are in flight at once.
   // Inside a group, warps [0, warps_q) normalise Q heads and warps

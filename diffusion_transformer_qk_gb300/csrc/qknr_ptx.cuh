@@ -69,6 +69,23 @@ __device__ __forceinline__ unsigned long long global_timer_ns() {
   return t;
 }
 
+// Programmatic dependent launch.  A kernel launched with programmatic
+// stream serialization may start while the kernel before it in the stream
+// is still finishing; grid_dependency_wait() returns once that kernel has
+// completed and its memory operations are visible (at once when there is no
+// such kernel).  grid_dependents_launch() lets the kernel after this one
+// start launching once every CTA of this grid has issued it or exited.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void grid_dependents_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// bar.sync on a named barrier for `threads` threads (a multiple of 32).
+__device__ __forceinline__ void named_barrier_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
 // 1-D bulk copy global -> this CTA's shared memory, completion counted in
 // bytes on `bar`.  Both addresses 16-byte aligned, bytes a multiple of 16.
 // The source is marked evict-first in L2: every byte is streamed once.

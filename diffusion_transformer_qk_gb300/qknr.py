@@ -32,6 +32,7 @@ STATUS = {
 }
 OK, ERR_TIMEOUT = 0, 6
 FLAG_TEST_STALL = 0x1
+FLAG_NO_OVERLAP = 0x2
 ABI_VERSION = 2
 
 EXPORTS = (

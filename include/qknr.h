@@ -81,6 +81,8 @@ typedef enum {
 /* Launch-time flags (qknr_args.flags). */
 #define QKNR_FLAG_TEST_STALL 0x1u /* test only: issue no loads, so every wait runs out
                                      and the kernel reports QKNR_ERR_TIMEOUT */
+#define QKNR_FLAG_NO_OVERLAP 0x2u /* launch without programmatic dependent launch (see
+                                     qknr_forward) */
 
 /*
  * Arguments of one call.  Fill with qknr_args_init() and then set fields.
@@ -161,6 +163,18 @@ void qknr_args_init(qknr_args *a);
  * Returns QKNR_OK after enqueueing, an argument error (nothing launched),
  * or QKNR_ERR_CUDA if the launch failed.  Kernel-side wait timeouts are
  * reported through args->dev_status only.
+ *
+ * Unless args->flags has QKNR_FLAG_NO_OVERLAP, the kernel is launched with
+ * programmatic stream serialization: when the previous operation in the
+ * stream is a kernel, this one may launch while that kernel finishes, sets
+ * up its shared memory, and then waits for it to complete before it reads
+ * or writes any global memory, so stream order holds as with a plain
+ * launch.  Each CTA signals dependents once all of its loads are issued, so
+ * a kernel launched after this one the same way (another qknr_forward, for
+ * example the K launch after the Q launch) overlaps this one's last rows in
+ * the same manner.  A kernel the caller launches after this one with that
+ * attribute must itself wait for the grid it depends on before reading the
+ * results (cudaGridDependencySynchronize).
  * Thread-safe.
  */
 qknr_status qknr_forward(const qknr_args *args, qknr_stream_t stream);
