@@ -536,9 +536,13 @@ __device__ __forceinline__ bool gnf_warp_wait(uint32_t bar, uint32_t parity, uns
 }
 
 // one lane waits (bounded, sleeping) until the shared word reaches `target`;
-// the result goes to the whole warp
-static __device__ __noinline__ bool gnf_wait_local(const volatile unsigned* word, unsigned target,
-                                                   const RecordWait& w) {
+// the result goes to the whole warp.  Out of line, so it takes the wait
+// context as scalars: a struct passed by reference to a call that is not
+// inlined would have to live in local memory.
+static __device__ __noinline__ bool gnf_wait_local(const volatile unsigned* word, unsigned target, unsigned tag,
+                                                   unsigned long long limit_ns, volatile int* abort_cta,
+                                                   unsigned* abort_grid, int* status) {
+  const RecordWait w{tag, limit_ns, abort_cta, abort_grid, status};
   bool ok = true;
   if ((threadIdx.x & 31) == 0 && *word < target) {
     const unsigned long long t0 = global_timer_ns();
@@ -676,7 +680,7 @@ __global__ void __launch_bounds__(kGnfThreads, 1) gn_fused_kernel(const __grid_c
       const int e = static_cast<int>(kk % kGnfCoefSlots);
       const uint32_t use_parity = (kk / kGnfCoefSlots) & 1u;
       if (!gnf_warp_wait(cempty0 + 8 * e, use_parity ^ 1u, limit, abort_cta, p.status)) break;
-      if (!gnf_wait_local(stats_done, t_end, rw)) break;
+      if (!gnf_wait_local(stats_done, t_end, rw.tag, rw.limit_ns, rw.abort_cta, rw.abort_grid, rw.status)) break;
       if (!combine_span<true>(p.rec + static_cast<long long>(span) * (P + 1) * 2, static_cast<int>(P), p.span_len,
                               kGnfChunk, p.eps, &rw, coef + kGnCoefFloats * e))
         break;
