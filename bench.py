@@ -668,9 +668,11 @@ def run_ours(args, w):
         e2e_s = max_over_ranks(s0.elapsed_time(s1) / 1e3, dev)
         e2e = {"value": whole_job_us_per_call(e2e_s, n_e2e, world), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "steps": n_e2e,
-               "path": ("HostPipeline, in place on the pinned host activation: the Q|K columns of rows in chunks "
-                        "of %d copied host->device, qknr_forward, and copied back, overlapped on three streams "
-                        "(V is neither read nor written by the operation, so it never leaves the host)"
+               "path": ("one qknr_forward_host call per step (C ABI, through the binding's HostPipeline), in "
+                        "place on the pinned host activation: the library copies the Q|K columns of rows in "
+                        "chunks of %d host->device, runs qknr_forward on each and copies them back, overlapped "
+                        "on three streams; the gains and tables are copied host->device each step (V is neither "
+                        "read nor written by the operation, so it never leaves the host)"
                         % args.e2e_chunk_rows) if run.pipe else
                        "pinned host -> device copies, qknr_forward via the Python binding, device -> pinned host, "
                        "one stream"}

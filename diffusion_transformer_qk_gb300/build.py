@@ -28,6 +28,7 @@ CXX_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xptxas",
 
 SOURCES = [
     "qknr_api.cu",
+    "qknr_host_api.cu",
     "qknr_inst_bf16_f32.cu",
     "qknr_inst_bf16_bf16.cu",
     "qknr_inst_fp16_f32.cu",

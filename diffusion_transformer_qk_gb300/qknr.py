@@ -41,10 +41,12 @@ EXPORTS = (
     "qknr_adaln_args_init", "qknr_adaln_forward", "qknr_adaln_query", "qknr_adaln_sizeof_args",
     "qknr_gn_args_init", "qknr_gn_workspace_bytes", "qknr_gn_silu_forward", "qknr_gn_sizeof_args",
     "qknr_gn_silu_forward_noalloc", "qknr_gn_query",
+    "qknr_host_plan_init", "qknr_host_buffer_bytes", "qknr_forward_host", "qknr_sizeof_host_plan",
 )
 GN_MODE = {"auto": 0, "fused": 1, "two_pass": 2}
 GN_FLAG_TEST_NO_RECORDS = 0x2
 GN_NOALLOC_SCRATCH_BYTES = 1 << 20
+HOST_MAX_BUFFERS = 4
 
 
 class QknrArgs(ctypes.Structure):
@@ -114,6 +116,17 @@ class QknrGnArgs(ctypes.Structure):
     ]
 
 
+class QknrHostPlan(ctypes.Structure):
+    """Mirror of ``qknr_host_plan``."""
+
+    _fields_ = [
+        ("abi_version", c_uint32), ("n_buffers", c_int32), ("chunk_rows", c_int64),
+        ("dev_buffers", c_void_p * HOST_MAX_BUFFERS), ("h2d_stream", c_void_p), ("d2h_stream", c_void_p),
+        ("events", c_void_p * (3 * HOST_MAX_BUFFERS + 2)),
+        ("host_gamma_q", c_void_p), ("host_gamma_k", c_void_p), ("host_cos", c_void_p), ("host_sin", c_void_p),
+    ]
+
+
 class QknrError(RuntimeError):
     def __init__(self, status: int, message: str):
         super().__init__(f"{STATUS.get(status, status)}: {message}")
@@ -171,12 +184,21 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
         lib.qknr_gn_silu_forward_noalloc.restype = c_int32
         lib.qknr_gn_query.argtypes = [ctypes.POINTER(QknrGnArgs), ctypes.POINTER(QknrLaunchInfo)]
         lib.qknr_gn_query.restype = c_int32
+        lib.qknr_host_plan_init.argtypes = [ctypes.POINTER(QknrHostPlan)]
+        lib.qknr_host_plan_init.restype = None
+        lib.qknr_host_buffer_bytes.argtypes = [ctypes.POINTER(QknrArgs), ctypes.POINTER(QknrHostPlan),
+                                               ctypes.POINTER(c_size_t)]
+        lib.qknr_host_buffer_bytes.restype = c_int32
+        lib.qknr_forward_host.argtypes = [ctypes.POINTER(QknrArgs), ctypes.POINTER(QknrHostPlan), c_void_p]
+        lib.qknr_forward_host.restype = c_int32
+        lib.qknr_sizeof_host_plan.restype = c_size_t
         if lib.qknr_abi_version() != ABI_VERSION:
             raise RuntimeError("libqknr.so ABI version mismatch")
         if lib.qknr_sizeof_args() != ctypes.sizeof(QknrArgs) or \
                 lib.qknr_sizeof_launch_info() != ctypes.sizeof(QknrLaunchInfo) or \
                 lib.qknr_adaln_sizeof_args() != ctypes.sizeof(QknrAdaLNArgs) or \
-                lib.qknr_gn_sizeof_args() != ctypes.sizeof(QknrGnArgs):
+                lib.qknr_gn_sizeof_args() != ctypes.sizeof(QknrGnArgs) or \
+                lib.qknr_sizeof_host_plan() != ctypes.sizeof(QknrHostPlan):
             raise RuntimeError("libqknr.so struct layout differs from the binding")
         if path is None:
             _lib = lib
@@ -406,13 +428,14 @@ def qk_norm_rope_separate(q, k, n_heads, head_dim, gamma_q, gamma_k, cos, sin, *
 
 
 # ---------------------------------------------------------------------------
-# host-resident activations: chunked, overlapped copies around the kernel
+# host-resident activations: qknr_forward_host (include/qknr.h)
 
 _cudart = None
 
 
 def _cudart_lib() -> ctypes.CDLL:
-    """The CUDA runtime libqknr.so links (already loaded with it)."""
+    """The CUDA runtime libqknr.so links (already loaded with it), for the
+    events the host pipeline hands the library."""
     global _cudart
     if _cudart is None:
         load()
@@ -420,72 +443,116 @@ def _cudart_lib() -> ctypes.CDLL:
         if not cands:
             raise RuntimeError("libcudart.so not found next to the CUDA toolkit")
         lib = ctypes.CDLL(cands[-1])
-        lib.cudaMemcpy2DAsync.argtypes = [c_void_p, c_size_t, c_void_p, c_size_t, c_size_t, c_size_t, c_int32,
-                                          c_void_p]
-        lib.cudaMemcpy2DAsync.restype = c_int32
+        lib.cudaEventCreateWithFlags.argtypes = [ctypes.POINTER(c_void_p), c_uint32]
+        lib.cudaEventCreateWithFlags.restype = c_int32
+        lib.cudaEventDestroy.argtypes = [c_void_p]
+        lib.cudaEventDestroy.restype = c_int32
         _cudart = lib
     return _cudart
 
 
-def copy_rows_async(dst: int, dst_pitch: int, src: int, src_pitch: int, width: int, rows: int,
-                    stream: torch.cuda.Stream) -> None:
-    """``rows`` rows of ``width`` bytes between pitched buffers (host or
-    device, either way; host memory pinned for the copy to be asynchronous),
-    on ``stream``: one cudaMemcpy2DAsync."""
-    if rows == 0 or width == 0:
-        return
-    err = _cudart_lib().cudaMemcpy2DAsync(c_void_p(dst), dst_pitch, c_void_p(src), src_pitch, width, rows,
-                                          4,  # cudaMemcpyDefault: direction from the addresses
-                                          c_void_p(stream.cuda_stream))
-    if err != 0:
-        raise RuntimeError(f"cudaMemcpy2DAsync failed with error {err}")
+def host_args(*, q=None, k=None, v=None, q_out=None, k_out=None, v_out=None, n_heads_q=0, n_heads_k=0,
+              n_heads_v=0, head_dim, tokens, gamma_q=None, gamma_k=None, cos=None, sin=None, cos_rows=0,
+              rope_style="interleaved", cos_layout="shared_row", eps=1e-6, dtype=torch.bfloat16, cos_dtype=FP32,
+              dev_status=None, ctas_per_sm=0, stages=0, consumer_warps=0, group_warps=0, flags=0,
+              wait_limit_ns=0) -> QknrArgs:
+    """``qknr_args`` for qknr_forward_host: q, k, v and the outputs are host
+    tensor views ([T, heads*D] rows with unit inner stride) or None; gamma,
+    cos and sin are device tensors."""
+    a = QknrArgs()
+    load().qknr_args_init(ctypes.byref(a))
+    a.dtype = _ACT[dtype]
+    for name, t in (("q", q), ("k", k), ("v", v), ("q_out", q_out), ("k_out", k_out), ("v_out", v_out)):
+        if t is None:
+            continue
+        if t.is_cuda or t.dim() != 2 or t.stride(1) != 1 or t.dtype != dtype:
+            raise ValueError(f"{name} must be a 2-D host tensor of {dtype} with contiguous rows")
+        setattr(a, name, t.data_ptr())
+        setattr(a, name + "_stride", t.stride(0))
+    a.tokens = tokens
+    a.n_heads_q, a.n_heads_k, a.n_heads_v, a.head_dim = n_heads_q, n_heads_k, n_heads_v, head_dim
+    a.gamma_q, a.gamma_k = _ptr(gamma_q), _ptr(gamma_k)
+    a.eps = eps
+    a.cos, a.sin = _ptr(cos), _ptr(sin)
+    a.cos_dtype = cos_dtype
+    a.cos_layout = COS_LAYOUT[cos_layout]
+    a.cos_rows = cos_rows
+    a.rope_style = ROPE[rope_style]
+    a.dev_status = _ptr(dev_status)
+    a.ctas_per_sm, a.stages, a.consumer_warps, a.group_warps = ctas_per_sm, stages, consumer_warps, group_warps
+    a.flags, a.wait_limit_ns = flags, wait_limit_ns
+    return a
 
 
 class HostPipeline:
-    """Runs the fused QK-RMSNorm + RoPE on a packed QKV activation that lives
-    in (pinned) host memory.  Token rows go through the device in chunks:
-    the host-to-device copy of chunk i+1, the kernel on chunk i and the
-    device-to-host copy of chunk i-1 run on three streams at once, so the
-    call costs about one direction of copy traffic instead of both plus the
-    kernel.
+    """The fused QK-RMSNorm + RoPE on a packed QKV activation that lives in
+    (pinned) host memory, through qknr_forward_host: token rows go through
+    device staging buffers in chunks, with the host-to-device copy of one
+    chunk, the kernel on the previous one and the device-to-host copy of the
+    one before that on three streams.  All of that runs inside the library;
+    this class only owns what the library does not allocate (the staging
+    buffers and the device copies of the gains and tables, made by torch;
+    two copy streams; the events) and marshals the call.
 
     In place on the host (``out_host`` None or the input) only the Q and K
-    columns of each row cross the host link, as pitched 2-D copies: V is
-    neither read nor written by the operation, so it stays where it is.
-    With a separate ``out_host`` whole rows go both ways and V is copied
-    through unchanged.
-
-    The device staging ring (``n_buffers`` chunks) and the device copies of
-    gamma and the cos/sin table are allocated by torch here; the library
-    itself still allocates nothing.  Results are bitwise those of
-    ``qk_norm_rope_packed`` on the whole activation: every row is processed
-    by the same kernel with the same table row.
+    columns of each row cross the host link: V is neither read nor written
+    by the operation, so it stays where it is.  With a separate ``out_host``
+    the Q, K and V columns go both ways and V is copied through unchanged.
+    The gains and tables are copied from the host to the device every call.
+    Results are bitwise those of ``qk_norm_rope_packed`` on the whole
+    activation.
     """
 
     def __init__(self, width: int, dtype: torch.dtype, chunk_rows: int = 4096, n_buffers: int = 3,
                  device=None):
+        lib = load()
         self.device = torch.device("cuda", torch.cuda.current_device() if device is None
                                    else torch.device(device).index)
+        if not 1 <= n_buffers <= 4:
+            raise ValueError("n_buffers must be 1..4")
         self.chunk_rows = int(chunk_rows)
         self.width = int(width)
+        self.dtype = dtype
         self.bufs = [torch.empty(self.chunk_rows * self.width, dtype=dtype, device=self.device)
                      for _ in range(n_buffers)]
         self.h2d = torch.cuda.Stream(self.device)
         self.d2h = torch.cuda.Stream(self.device)
-        self.freed = [None] * n_buffers          # event: the buffer's last D2H finished
         self.status = torch.zeros(1, dtype=torch.int32, device=self.device)
+        self.tables = {}
+        rt = _cudart_lib()
+        self.events = []
+        with torch.cuda.device(self.device):
+            for _ in range(3 * n_buffers + 2):
+                e = c_void_p()
+                err = rt.cudaEventCreateWithFlags(ctypes.byref(e), 2)   # cudaEventDisableTiming
+                if err != 0:
+                    raise RuntimeError(f"cudaEventCreateWithFlags failed with error {err}")
+                self.events.append(e.value)
+        self.plan = QknrHostPlan()
+        lib.qknr_host_plan_init(ctypes.byref(self.plan))
+        self.plan.n_buffers = n_buffers
+        self.plan.chunk_rows = self.chunk_rows
+        for i, b in enumerate(self.bufs):
+            self.plan.dev_buffers[i] = b.data_ptr()
+        self.plan.h2d_stream = self.h2d.cuda_stream
+        self.plan.d2h_stream = self.d2h.cuda_stream
+        for i, e in enumerate(self.events):
+            self.plan.events[i] = e
         self.last_h2d_bytes = self.last_d2h_bytes = 0
 
-    def _stage_tables(self, gamma_q, gamma_k, cos, sin, stream, user):
-        """Device copies of the gains and tables (copied every call, on
-        `stream`; marked as used by `user` so the allocator keeps them until
-        the kernels that read them are done)."""
-        with torch.cuda.stream(stream):
-            dev = [None if t is None else t.to(self.device, non_blocking=True) for t in (gamma_q, gamma_k, cos, sin)]
-        for t in dev:
-            if t is not None:
-                t.record_stream(user)
-        return dev
+    def __del__(self):
+        rt = _cudart
+        if rt is not None:
+            for e in getattr(self, "events", []):
+                rt.cudaEventDestroy(c_void_p(e))
+
+    def _device_table(self, name, t):
+        """The device buffer the host table ``t`` is copied into (kept across calls)."""
+        d = self.tables.get(name)
+        if d is None or d.shape != t.shape or d.dtype != t.dtype:
+            d = torch.empty(t.shape, dtype=t.dtype, device=self.device)
+            self.tables[name] = d
+        return d
 
     def read_status(self) -> int:
         """Synchronise and return (then clear) the kernels' status word."""
@@ -498,62 +565,48 @@ class HostPipeline:
                  out_host=None, rope_style="interleaved", cos_layout="shared_row", eps=1e-6, **tune):
         if qkv_host.is_cuda or qkv_host.dim() != 2 or qkv_host.shape[1] != self.width or qkv_host.stride(1) != 1:
             raise ValueError("qkv_host must be a 2-D host tensor of the pipeline's width with contiguous rows")
+        if qkv_host.dtype != self.dtype:
+            raise ValueError("qkv_host dtype differs from the pipeline's")
         if (n_heads_q + n_heads_k + n_heads_v) * head_dim != self.width:
             raise ValueError("head counts do not match the pipeline's width")
         in_place = out_host is None or out_host.data_ptr() == qkv_host.data_ptr()
-        out_host = qkv_host if out_host is None else out_host
-        if out_host.shape != qkv_host.shape or out_host.dtype != qkv_host.dtype or out_host.stride(1) != 1:
+        if out_host is not None and (out_host.shape != qkv_host.shape or out_host.dtype != qkv_host.dtype or
+                                     out_host.stride(1) != 1):
             raise ValueError("out_host must match qkv_host")
-        T = qkv_host.shape[0]
+        T, D = qkv_host.shape[0], head_dim
+        q0, k0, v0 = 0, n_heads_q * D, (n_heads_q + n_heads_k) * D
+
+        def cols(t, a, b):
+            return None if t is None or a == b else t[:, a:b]
+
+        dev = {n: self._device_table(n, t) for n, t in (("gamma_q", gamma_q), ("gamma_k", gamma_k), ("cos", cos),
+                                                       ("sin", sin))}
+        cos_dtype = _TAB[cos.dtype]
+        a = host_args(q=cols(qkv_host, q0, k0), k=cols(qkv_host, k0, v0), v=cols(qkv_host, v0, self.width),
+                      q_out=None if in_place else cols(out_host, q0, k0),
+                      k_out=None if in_place else cols(out_host, k0, v0),
+                      v_out=None if in_place else cols(out_host, v0, self.width),
+                      n_heads_q=n_heads_q, n_heads_k=n_heads_k, n_heads_v=n_heads_v, head_dim=D, tokens=T,
+                      gamma_q=dev["gamma_q"], gamma_k=dev["gamma_k"], cos=dev["cos"], sin=dev["sin"],
+                      cos_rows=cos.shape[0], rope_style=rope_style, cos_layout=cos_layout, eps=eps,
+                      dtype=qkv_host.dtype, cos_dtype=cos_dtype, dev_status=self.status, **tune)
+        self.plan.host_gamma_q, self.plan.host_gamma_k = gamma_q.data_ptr(), gamma_k.data_ptr()
+        self.plan.host_cos, self.plan.host_sin = cos.data_ptr(), sin.data_ptr()
+        lib = load()
+        stream = torch.cuda.current_stream(self.device)
+        st = lib.qknr_forward_host(ctypes.byref(a), ctypes.byref(self.plan), c_void_p(stream.cuda_stream))
+        if st != OK:
+            raise QknrError(st, lib.qknr_last_error().decode())
+        # the host tables and device buffers are in use until the stream's
+        # work is done
+        for t in list(dev.values()) + self.bufs:
+            t.record_stream(stream)
         es = qkv_host.element_size()
-        # in place: the Q|K columns only; else whole rows
-        cols = (n_heads_q + n_heads_k) * head_dim if in_place else self.width
-        hv = 0 if in_place else n_heads_v
-        compute = torch.cuda.current_stream(self.device)
-        gq, gk, cos_d, sin_d = self._stage_tables(gamma_q, gamma_k, cos, sin, self.h2d, compute)
-        tables_ready = torch.cuda.Event()
-        tables_ready.record(self.h2d)
-        rows = cos_d.shape[0]
-        if rows < T and self.chunk_rows % rows:
-            raise ValueError("with a batch-broadcast table the chunk must be a multiple of its rows")
-        n = len(self.bufs)
-        done = torch.cuda.Event()
-        for i, r0 in enumerate(range(0, T, self.chunk_rows)):
-            r1 = min(T, r0 + self.chunk_rows)
-            b = i % n
-            buf = self.bufs[b][: (r1 - r0) * cols].view(r1 - r0, cols)
-            with torch.cuda.stream(self.h2d):
-                if self.freed[b] is not None:
-                    self.h2d.wait_event(self.freed[b])
-                copy_rows_async(buf.data_ptr(), cols * es, qkv_host[r0].data_ptr(), qkv_host.stride(0) * es,
-                                cols * es, r1 - r0, self.h2d)
-                loaded = torch.cuda.Event()
-                loaded.record(self.h2d)
-            compute.wait_event(loaded)
-            if i == 0:
-                compute.wait_event(tables_ready)
-            # the chunk's table rows: its own slice of a per-token table, or
-            # the whole batch-broadcast table (chunks start on a multiple of it)
-            c, s = (cos_d[r0:r1], sin_d[r0:r1]) if rows >= T else (cos_d, sin_d)
-            launch(packed_args(buf, n_heads_q, n_heads_k, hv, head_dim, gq, gk, c, s,
-                               rope_style=rope_style, cos_layout=cos_layout, eps=eps, dev_status=self.status,
-                               **tune), compute)
-            computed = torch.cuda.Event()
-            computed.record(compute)
-            with torch.cuda.stream(self.d2h):
-                self.d2h.wait_event(computed)
-                copy_rows_async(out_host[r0].data_ptr(), out_host.stride(0) * es, buf.data_ptr(), cols * es,
-                                cols * es, r1 - r0, self.d2h)
-                freed = torch.cuda.Event()
-                freed.record(self.d2h)
-                self.freed[b] = freed
-        # the caller's stream sees the results once every D2H copy is done
-        done.record(self.d2h)
-        compute.wait_event(done)
-        tables = sum(t.numel() * t.element_size() for t in (gamma_q, gamma_k, cos, sin) if t is not None)
-        self.last_h2d_bytes = T * cols * es + tables
-        self.last_d2h_bytes = T * cols * es
-        return out_host
+        moved = (n_heads_q + n_heads_k + (0 if in_place else n_heads_v)) * D * es * T
+        tables = sum(t.numel() * t.element_size() for t in (gamma_q, gamma_k, cos, sin))
+        self.last_h2d_bytes = moved + tables
+        self.last_d2h_bytes = moved
+        return qkv_host if in_place else out_host
 
 
 # ---------------------------------------------------------------------------

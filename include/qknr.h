@@ -188,6 +188,85 @@ const char *qknr_status_string(int32_t status);
 /* Message of the last error returned on this thread (static per thread). */
 const char *qknr_last_error(void);
 
+/*
+ * Host-resident activations: the whole call from host buffers
+ * ---------------------------------------------------------------
+ * For a caller whose activation lives in host memory (a plugin or an
+ * offload path that holds the rows on the host; pinned memory makes the
+ * copies asynchronous).  qknr_forward_host() streams the token rows through
+ * caller-owned device staging buffers in chunks: the host-to-device copy of
+ * one chunk, the kernel on the one before and the device-to-host copy of
+ * the one before that run at once on three streams, so the call costs about
+ * one direction of host-link traffic.  The library still allocates nothing:
+ * buffers, copy streams and events all come from the caller.
+ *
+ * In this call q, k, v, q_out, k_out and v_out of qknr_args are HOST
+ * pointers (strides in elements, as for qknr_forward); gamma_q, gamma_k,
+ * cos and sin are DEVICE pointers.  Only the columns the operation reads or
+ * writes cross the host link: Q and K in and out, and V only when it is
+ * copied (v_out set and different from v); in place, V stays where it is.
+ * Every row is processed by the same kernel with the same table row as in
+ * one qknr_forward() over the whole activation, so the results are the same
+ * bits.  A table with cos_rows < tokens (batch broadcast) needs chunk_rows
+ * to be a multiple of cos_rows.
+ */
+
+/* Same type as cudaEvent_t. */
+struct CUevent_st;
+typedef struct CUevent_st *qknr_event_t;
+
+#define QKNR_HOST_MAX_BUFFERS 4
+/* events a plan of n buffers uses */
+#define QKNR_HOST_EVENTS(n) (3 * (n) + 2)
+
+typedef struct qknr_host_plan {
+  uint32_t abi_version;       /* QKNR_ABI_VERSION */
+  int32_t n_buffers;          /* device staging buffers, 1..QKNR_HOST_MAX_BUFFERS; 3 lets copy-in,
+                                 kernel and copy-out of consecutive chunks overlap */
+  int64_t chunk_rows;         /* token rows per chunk, > 0 */
+  /* device staging buffers, 16-byte aligned, each at least
+     qknr_host_buffer_bytes() bytes; only the first n_buffers are used */
+  void *dev_buffers[QKNR_HOST_MAX_BUFFERS];
+  /* the copy streams; either may be the call's stream (then its copies do
+     not overlap the kernels) */
+  qknr_stream_t h2d_stream, d2h_stream;
+  /* caller-created events on the call's device (cudaEventDisableTiming is
+     enough); the first QKNR_HOST_EVENTS(n_buffers) are used and re-recorded
+     by every call */
+  qknr_event_t events[QKNR_HOST_EVENTS(QKNR_HOST_MAX_BUFFERS)];
+  /* Optional host copies of the gains and tables.  Each one that is not
+     NULL is copied, on h2d_stream before the first chunk, into the device
+     buffer that the qknr_args field of the same name points to (gamma: D
+     floats; cos, sin: cos_rows table rows, cos_rows = tokens when 0). */
+  const void *host_gamma_q, *host_gamma_k, *host_cos, *host_sin;
+} qknr_host_plan;
+
+/* Defaults: 3 buffers, 4096-row chunks, everything else zero. */
+void qknr_host_plan_init(qknr_host_plan *p);
+
+/* Bytes each device staging buffer needs for these arguments and plan:
+   chunk_rows * (n_heads_q + n_heads_k [+ n_heads_v when V is copied]) *
+   head_dim * 2. */
+qknr_status qknr_host_buffer_bytes(const qknr_args *args, const qknr_host_plan *plan, size_t *bytes);
+
+/*
+ * Run the operation on host-resident activations (see above), ordered
+ * after the work already on `stream`; once the call returns, `stream`
+ * waits for every copy back to the host, so work enqueued on it afterwards
+ * (or a synchronisation of it) sees the results.  Nothing is launched when
+ * validation fails (argument errors as qknr_forward, plus QKNR_ERR_NULL for
+ * a missing buffer or event, QKNR_ERR_SHAPE for chunk_rows / n_buffers out
+ * of range or a batch-broadcast table that chunk_rows is not a multiple of,
+ * QKNR_ERR_ALIGN for a staging buffer not on 16 bytes, QKNR_ERR_OVERLAP for
+ * a host output that partially overlaps a host input).  A CUDA error after
+ * the first copy was enqueued returns QKNR_ERR_CUDA; the host outputs are
+ * then unspecified.  Thread-safe for calls with distinct plans.
+ */
+qknr_status qknr_forward_host(const qknr_args *args, const qknr_host_plan *plan, qknr_stream_t stream);
+
+/* sizeof(qknr_host_plan) as compiled into the library. */
+size_t qknr_sizeof_host_plan(void);
+
 /* QKNR_ABI_VERSION of the built library. */
 int32_t qknr_abi_version(void);
 

@@ -302,3 +302,72 @@ def test_gn_validation_rejects(lib, mutate, expect):
     mutate(a)
     st = lib.qknr_gn_silu_forward(ctypes.byref(a), None)
     assert st == expect, (st, lib.qknr_last_error().decode())
+
+
+# ---------------------------------------------------------------------------
+# qknr_forward_host: plan validation returns before any CUDA call
+
+def valid_host_plan(n=3, chunk=16):
+    p = Q.QknrHostPlan()
+    Q.load().qknr_host_plan_init(ctypes.byref(p))
+    assert p.abi_version == Q.ABI_VERSION and p.n_buffers == 3 and p.chunk_rows == 4096
+    p.n_buffers, p.chunk_rows = n, chunk
+    for i in range(n):
+        p.dev_buffers[i] = FAKE + (4 << 30) + i * (1 << 24)
+    for i in range(3 * n + 2):
+        p.events[i] = 0x1000 + 16 * i
+    return p
+
+
+def call_host(lib, a, p):
+    st = lib.qknr_forward_host(ctypes.byref(a) if a is not None else None,
+                               ctypes.byref(p) if p is not None else None, None)
+    return st, lib.qknr_last_error().decode()
+
+
+@pytest.mark.parametrize("mutate,expect", [
+    (lambda a, p: setattr(p, "n_buffers", 0), 2),
+    (lambda a, p: setattr(p, "n_buffers", 5), 2),
+    (lambda a, p: setattr(p, "chunk_rows", 0), 2),
+    (lambda a, p: setattr(p, "abi_version", 1), 8),
+    (lambda a, p: p.dev_buffers.__setitem__(2, None), 1),
+    (lambda a, p: p.dev_buffers.__setitem__(1, FAKE + 8), 3),
+    (lambda a, p: p.events.__setitem__(10, None), 1),
+    (lambda a, p: setattr(a, "head_dim", 96), 4),
+    (lambda a, p: setattr(a, "q", None), 1),
+    (lambda a, p: setattr(a, "q_stride", 100), 2),
+    # a batch-broadcast table of 12 rows with 16-row chunks
+    (lambda a, p: setattr(a, "cos_rows", 12), 2),
+    # a separate output that overlaps the K input rows
+    (lambda a, p: setattr(a, "q_out", FAKE + 4 * 128 * 2 + 64), 7),
+])
+def test_host_call_validation_rejects(lib, mutate, expect):
+    a, p = valid_packed(), valid_host_plan()
+    mutate(a, p)
+    st, msg = call_host(lib, a, p)
+    assert st == expect, (st, msg)
+    assert msg
+
+
+def test_host_call_null_arguments(lib):
+    assert call_host(lib, None, valid_host_plan())[0] == 1
+    assert call_host(lib, valid_packed(), None)[0] == 1
+
+
+def test_host_buffer_bytes(lib):
+    a, p = valid_packed(T=100, H=4, D=128), valid_host_plan(chunk=16)
+    n = ctypes.c_size_t(0)
+    # in place: Q and K columns only
+    assert lib.qknr_host_buffer_bytes(ctypes.byref(a), ctypes.byref(p), ctypes.byref(n)) == 0
+    assert n.value == 16 * 8 * 128 * 2
+    # V copied to a separate output: Q, K and V columns
+    a.v_out = FAKE + (5 << 30)
+    assert lib.qknr_host_buffer_bytes(ctypes.byref(a), ctypes.byref(p), ctypes.byref(n)) == 0
+    assert n.value == 16 * 12 * 128 * 2
+    p.chunk_rows = 0
+    assert lib.qknr_host_buffer_bytes(ctypes.byref(a), ctypes.byref(p), ctypes.byref(n)) == 2
+
+
+def test_host_call_with_no_rows_is_a_no_op(lib):
+    a, p = valid_packed(T=0), valid_host_plan()
+    assert call_host(lib, a, p)[0] == 0

@@ -74,6 +74,22 @@ int main(void) {
   CHECK(qknr_gn_query(&g, NULL) == QKNR_ERR_NULL, 45);
   g.mode = 7;
   CHECK(qknr_gn_workspace_bytes(&g, &ws) == QKNR_ERR_UNSUPPORTED, 46);
+  {
+    qknr_host_plan hp;
+    qknr_args_init(&a);
+    qknr_host_plan_init(&hp);
+    CHECK(qknr_sizeof_host_plan() == sizeof(qknr_host_plan), 50);
+    CHECK(hp.abi_version == QKNR_ABI_VERSION && hp.n_buffers == 3 && hp.chunk_rows == 4096, 51);
+    CHECK(qknr_forward_host(NULL, &hp, NULL) == QKNR_ERR_NULL, 52);
+    CHECK(qknr_forward_host(&a, NULL, NULL) == QKNR_ERR_NULL, 53);
+    a.head_dim = 128;
+    a.n_heads_q = a.n_heads_k = 24;
+    a.tokens = 1000;
+    hp.chunk_rows = 256;
+    CHECK(qknr_host_buffer_bytes(&a, &hp, &ws) == QKNR_OK && ws == (size_t)256 * 48 * 128 * 2, 54);
+    hp.n_buffers = 0;
+    CHECK(qknr_forward_host(&a, &hp, NULL) == QKNR_ERR_SHAPE, 55);
+  }
   printf("ok %d\n", QKNR_GN_NOALLOC_SCRATCH_BYTES);
   return 0;
 }

@@ -254,10 +254,12 @@ def test_host_pipeline_batch_broadcast_table():
          torch.from_numpy(inp["cos"]), torch.from_numpy(inp["sin"]), rope_style=w.rope_style)
     torch.cuda.synchronize()
     assert torch.equal(host.view(torch.int16), ref.cpu().view(torch.int16))
-    with pytest.raises(ValueError):
+    # chunks must start on a multiple of the batch-broadcast table's rows
+    with pytest.raises(Q.QknrError) as e:
         Q.HostPipeline(host.shape[1], torch.bfloat16, chunk_rows=700)(
             host, 24, 24, 24, 128, torch.from_numpy(inp["gamma_q"]), torch.from_numpy(inp["gamma_k"]),
             torch.from_numpy(inp["cos"]), torch.from_numpy(inp["sin"]))
+    assert e.value.status == 2
 
 
 # ---------------------------------------------------------------------------
