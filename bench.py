@@ -691,7 +691,9 @@ def run_ours(args, w):
     value = whole_job_us_per_call(max_elapsed, K, world)
     achieved = run.bytes_per_launch / (max_kernel_ms / 1e3) / 1e9
     peak, peak_kind = hbm_peak()
-    traffic = recorded_traffic(w.name)
+    # the record is of the named workload as it stands (not of an override)
+    named = I.WORKLOADS.get(w.name) or I.ADALN_WORKLOADS.get(w.name) or I.GN_WORKLOADS.get(w.name)
+    traffic = recorded_traffic(w.name) if named == w else None
     info = run.info
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
@@ -895,6 +897,9 @@ def run_config_sweep(dev, status, steps: int, warmup: int, peak: float):
                                                         else "one launch per tensor (Q, then K)")))
         if L > 1:
             entry["us_per_launch"] = t * 1e6 / L
+        if not over and not plain:
+            # ncu DRAM bytes per launch, when the committed record is of these sources
+            entry["traffic_per_launch"] = recorded_traffic(name)
         if not isinstance(w, I.GroupNormWorkload):
             entry["launch_mode"] = ("plain stream order" if plain else
                                     "programmatic dependent launch (the default)")
