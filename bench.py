@@ -122,6 +122,74 @@ def recorded_traffic(workload: str):
     return rec.get("dram_bytes_per_launch")
 
 
+class NvmlClockSampler:
+    """SM clock and clock-event reasons read through NVML (libnvidia-ml, by
+    ctypes; read-only queries) every millisecond on a thread, so that even a
+    timed region of a few milliseconds has samples.  Raises if NVML or the
+    device cannot be opened; ClockSampler then falls back to nvidia-smi."""
+
+    # nvmlClocksEventReasons bits
+    REASONS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20, "hw_thermal_slowdown": 0x40,
+               "hw_power_brake_slowdown": 0x80}
+
+    def __init__(self, uuid: str, period_s: float = 0.001):
+        import ctypes
+
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise RuntimeError("nvmlInit failed")
+        self.lib = lib
+        self.dev = ctypes.c_void_p()
+        if lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.dev)) != 0:
+            raise RuntimeError("nvmlDeviceGetHandleByUUID failed")
+        self.reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint(0)
+        lib.nvmlDeviceGetMaxClockInfo(self.dev, 1, ctypes.byref(mx))       # NVML_CLOCK_SM
+        self.max_mhz = float(mx.value) or None
+        self.samples = []
+        self.period = period_s
+        self.running = True
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        import ctypes
+
+        mhz, reasons = ctypes.c_uint(0), ctypes.c_ulonglong(0)
+        while self.running:
+            ok = self.lib.nvmlDeviceGetClockInfo(self.dev, 1, ctypes.byref(mhz)) == 0
+            ok = ok and self.reasons_fn(self.dev, ctypes.byref(reasons)) == 0
+            if ok:
+                self.samples.append((time.perf_counter(), float(mhz.value), int(reasons.value)))
+            time.sleep(self.period)
+
+    def stop(self):
+        self.running = False
+        self.thread.join(timeout=5)
+        self.lib.nvmlShutdown()
+
+    def summary(self, t0: float, t1: float):
+        inside = [(m, r) for t, m, r in self.samples if t0 <= t <= t1]
+        note = "NVML, sampled every 1 ms during the timed region"
+        if not inside:
+            inside = [(m, r) for _, m, r in self.samples]
+            note = "NVML; no sample fell inside the timed region: samples span warm-up and timed steps"
+        reasons = sorted({n for _, r in inside for n, bit in self.REASONS.items() if r & bit})
+        return {"sm_mhz": statistics.median(m for m, _ in inside) if inside else None, "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(inside), "note": note}
+
+
+def clock_sampler(uuid_or_index: str):
+    """The NVML sampler when NVML is there, else nvidia-smi's."""
+    if uuid_or_index.startswith("GPU-"):
+        try:
+            return NvmlClockSampler(uuid_or_index)
+        except Exception:
+            pass
+    return ClockSampler(uuid_or_index)
+
+
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons, sampled every 100 ms."""
 
@@ -457,14 +525,14 @@ class AdaLNRunner:
     """Device buffers and launch arguments of an AdaLN scale/shift workload
     (one launch per step, in place)."""
 
-    def __init__(self, w, dev, tune, status, tokens=None):
+    def __init__(self, w, dev, tune, status, tokens=None, inp=None):
         import torch
 
         from diffusion_transformer_qk_gb300 import qknr as Q
 
         self.Q, self.w, self.dev, self.tune = Q, w, dev, tune
         self.tokens = w.tokens if tokens is None else tokens
-        self.inp = I.make_adaln_inputs(w, tokens=self.tokens)
+        self.inp = I.make_adaln_inputs(w, tokens=self.tokens) if inp is None else inp
         act = torch.bfloat16 if w.dtype == "bf16" else torch.float16
 
         def bits(a, dt):
@@ -590,7 +658,7 @@ def run_ours(args, w):
 
     props = torch.cuda.get_device_properties(dev)
     gpu_id = ("GPU-" + str(props.uuid)) if getattr(props, "uuid", None) else str(local)
-    sampler = ClockSampler(gpu_id)
+    sampler = clock_sampler(gpu_id)
     time.sleep(0.3)                       # let the sampler start
     for _ in range(args.warmup):
         run.step(stream)

@@ -92,6 +92,12 @@ qknr_status plan(const qknr_adaln_args* a, AdaPlan* pl, bool size_device) {
   kp.flags = a->flags;
   kp.row_bytes = static_cast<unsigned>(C * es);
   kp.stage_bytes = (kp.row_bytes + qknr::kAdaStageAlign - 1) / qknr::kAdaStageAlign * qknr::kAdaStageAlign;
+  // buffer spans for checked builds
+  auto msp = [](Span x) { return qknr::MemSpan{x.lo, x.hi}; };
+  kp.sp_x = msp(span_of(a->x, T, xs * es, (long long)C * es));
+  kp.sp_out = msp(span_of(out, T, os * es, (long long)C * es));
+  kp.sp_scale = msp(span_of(a->scale, B, ms * mes, (long long)C * mes));
+  kp.sp_shift = msp(span_of(a->shift, B, ms * mes, (long long)C * mes));
   pl->stage_bytes = static_cast<int>(kp.stage_bytes);
   pl->launch = true;
   if (!size_device) return QKNR_OK;
@@ -180,6 +186,7 @@ qknr_status plan(const qknr_adaln_args* a, AdaPlan* pl, bool size_device) {
   pl->grid = static_cast<int>(grid);
   pl->block = block;
   pl->smem = static_cast<int>(smem);
+  kp.smem_bytes = static_cast<unsigned>(smem);
   pl->stages = stages;
   pl->ctas_per_sm = per_sm;
   pl->warps = warps;

@@ -66,6 +66,9 @@ struct AdaLNParams {
   unsigned flags;
   unsigned row_bytes;                             // C * 2
   unsigned stage_bytes;
+  unsigned smem_bytes;                            // dynamic shared memory of the launch
+  // address spans of the buffers (checked builds test every access against them)
+  MemSpan sp_x, sp_out, sp_scale, sp_shift;
 };
 
 __device__ __forceinline__ void named_barrier(int id, int threads) {
@@ -141,6 +144,15 @@ __global__ void __launch_bounds__(kAdaMaxThreads, 1) adaln_kernel(const __grid_c
         break;
       }
       if (p.flags & 1u) break;                    // test only: issue nothing
+      // checked builds: the row inside x and the stage inside the launch's
+      // shared memory, else nothing more is issued and the CTA gives up
+      if (!in_span(reinterpret_cast<const void*>(src), p.row_bytes, p.sp_x, p.status) ||
+          (kChecked && stage0 + (s + 1) * p.stage_bytes > base + p.smem_bytes)) {
+        if (p.status) atomicCAS(p.status, 0, kStatusBounds);
+        *abort_flag = 1;
+        ok = false;
+        break;
+      }
       const uint32_t full = full0 + 8 * s;
       mbar_arrive_expect_tx(full, p.row_bytes);
       bulk_load(stage0 + s * p.stage_bytes, reinterpret_cast<const void*>(src), p.row_bytes, full);
@@ -250,6 +262,11 @@ __global__ void __launch_bounds__(kAdaMaxThreads, 1) adaln_kernel(const __grid_c
       all_ok = all_ok && part[2 * kAdaMaxWarps + w] != 0.0f;
     }
     if (!all_ok) break;                           // every warp of the group leaves together
+    // checked builds: the row's modulation rows and its output row inside
+    // their buffers (the same answer in every warp of the group)
+    const bool row_ok = in_span(srow, static_cast<unsigned long long>(p.hidden) * sizeof(MT), p.sp_scale, p.status) &&
+                        in_span(hrow, static_cast<unsigned long long>(p.hidden) * sizeof(MT), p.sp_shift, p.status) &&
+                        in_span(p.out + row * p.out_stride, p.row_bytes, p.sp_out, p.status);
     const Moments row_m = merged(static_cast<float>(p.hidden), ref, sums);
     const float m1 = row_m.u;                     // mean - K
     const float var = __fmul_rn(row_m.m, inv_c);
@@ -265,7 +282,7 @@ __global__ void __launch_bounds__(kAdaMaxThreads, 1) adaln_kernel(const __grid_c
     // second pass over the staged row: normalise, modulate, store
     char* orow = p.out + row * p.out_stride;
 #pragma unroll UNROLL
-    for (int k = lane_g; k < n_chunks; k += gthreads) {
+    for (int k = row_ok ? lane_g : n_chunks; k < n_chunks; k += gthreads) {
       float2 X[4], sc[4], sh[4], o[4];
       Elem<T>::unpack(*reinterpret_cast<const uint4*>(st + k * 16), X);
       load_mod8<MT>(srow, k, sc);

@@ -104,6 +104,7 @@ qknr_status plan(const qknr_gn_args* a, GnPlan* pl) {
   kp.group_channels = a->c / a->groups;
   kp.pieces = pl->pieces;
   kp.eps = a->eps;
+  kp.status = a->dev_status;
 
   // ---- fused path
   const long long fP = (L + qknr::kGnfChunk - 1) / qknr::kGnfChunk;
@@ -221,6 +222,22 @@ qknr_status check_buffers(const qknr_gn_args* a, const GnPlan& pl) {
   return QKNR_OK;
 }
 
+// Address spans of a call's buffers, which checked builds test every access
+// against: x and out (N*C*H*W elements), the part of the workspace the call
+// uses, gamma and beta.
+struct GnSpans {
+  qknr::MemSpan x, out, ws, gamma, beta;
+};
+
+GnSpans spans_of(const qknr_gn_args* a, const GnPlan& pl) {
+  const long long total = pl.spans * pl.L * 2;
+  const void* out = a->out ? a->out : a->x;
+  auto ms = [](Span x) { return qknr::MemSpan{x.lo, x.hi}; };
+  return {ms(span_of(a->x, 1, 0, total)), ms(span_of(out, 1, 0, total)),
+          ms(span_of(a->workspace, 1, 0, static_cast<long long>(pl.workspace))),
+          ms(span_of(a->gamma, 1, 0, (long long)a->c * 4)), ms(span_of(a->beta, 1, 0, (long long)a->c * 4))};
+}
+
 // The tag of calls made while the stream is being captured into a CUDA
 // graph: a replay reuses its launch's parameters, so the captured call
 // clears the records first (a memset node) and uses this fixed tag.
@@ -281,6 +298,12 @@ qknr_status launch_fused(const qknr_gn_args* a, const GnPlan& pl, const FusedLau
   fp.flags = a->flags & (qknr::kGnfFlagStallLoads | qknr::kGnfFlagStallRecords);
   fp.wait_limit_ns = a->wait_limit_ns ? a->wait_limit_ns : kDefaultWaitNs;
   fp.eps = a->eps;
+  const GnSpans sp = spans_of(a, pl);
+  fp.sp_x = sp.x;
+  fp.sp_out = sp.out;
+  fp.sp_ws = sp.ws;
+  fp.sp_gamma = sp.gamma;
+  fp.sp_beta = sp.beta;
   void* kargs[] = {&fp};
   e = cudaLaunchCooperativeKernel(fl.fn, dim3(fl.grid), dim3(qknr::kGnfThreads), kargs,
                                               static_cast<size_t>(qknr::kGnfSmemBytes), s);
@@ -299,9 +322,15 @@ qknr_status launch_two_pass(const qknr_gn_args* a, const GnPlan& pl, cudaStream_
                            : reinterpret_cast<const void*>(&qknr::gn_stats_kernel<__half>);
   const void* apply = bf16 ? reinterpret_cast<const void*>(&qknr::gn_apply_kernel<__nv_bfloat16>)
                            : reinterpret_cast<const void*>(&qknr::gn_apply_kernel<__half>);
+  const GnSpans sp = spans_of(a, pl);
   for (long long s0 = 0; s0 < pl.spans; s0 += pl.batch_spans) {
     qknr::GnParams kp = pl.kp;
     kp.span0 = static_cast<int>(s0);
+    kp.sp_x = sp.x;
+    kp.sp_out = sp.out;
+    kp.sp_ws = sp.ws;
+    kp.sp_gamma = sp.gamma;
+    kp.sp_beta = sp.beta;
     const long long nb = pl.spans - s0 < pl.batch_spans ? pl.spans - s0 : pl.batch_spans;
     const dim3 grid(static_cast<unsigned>(pl.pieces), static_cast<unsigned>(nb));
     void* kargs[] = {&kp};

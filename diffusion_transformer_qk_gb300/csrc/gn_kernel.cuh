@@ -55,6 +55,9 @@ struct GnParams {
   int pieces;                  // P pieces per span
   int span0;                   // first span (n*G + g) of this launch
   float eps;
+  int* status;                 // checked builds: QKNR_ERR_BOUNDS goes here
+  // address spans of the buffers (checked builds test every access against them)
+  MemSpan sp_x, sp_out, sp_ws, sp_gamma, sp_beta;
 };
 
 __device__ __forceinline__ unsigned long long tagged(unsigned tag, float v) {
@@ -140,9 +143,12 @@ __device__ __forceinline__ void give_up(const RecordWait& w) {
 // when a lane gave up (bounded by w->limit_ns, or another CTA gave up).
 template <bool kWait>
 __device__ __forceinline__ bool combine_span(const unsigned long long* rec, int pieces, long long span_len,
-                                             long long piece_len, float eps, const RecordWait* w, float* coef) {
+                                             long long piece_len, float eps, const RecordWait* w, float* coef,
+                                             const MemSpan& ws, int* status) {
   constexpr int kBatch = 8;
   const int lane = threadIdx.x & 31;
+  // checked builds: the span's P + 1 records inside the workspace
+  if (!in_span(rec, static_cast<unsigned long long>(pieces + 1) * 16, ws, status)) return false;
   // the shift K (written with piece 0's sums), loaded with the first batch
   unsigned long long kw = lane == 0 ? ld_record(rec + 2 * pieces).x : 0ull;
   float nl = 0.0f, rl = 0.0f;                        // this lane's count and reference
@@ -280,6 +286,12 @@ __global__ void __launch_bounds__(kGnThreads) gn_stats_kernel(const __grid_const
   const long long lo = static_cast<long long>(piece) * p.piece_len;
   long long hi = lo + p.piece_len;
   if (hi > p.span_len) hi = p.span_len;
+  // checked builds: the span inside x, its records inside the workspace
+  // (the same answer in every thread of the block)
+  if (!in_span(base, static_cast<unsigned long long>(p.span_len) * 2, p.sp_x, p.status) ||
+      !in_span(p.rec + static_cast<long long>(span) * (p.pieces + 1) * 2, static_cast<unsigned long long>(p.pieces + 1) * 16,
+               p.sp_ws, p.status))
+    return;
   float2 first[4];
   Elem<T>::unpack(__ldg(reinterpret_cast<const uint4*>(base)), first);
   const float K = shift_of_first8(first);
@@ -343,9 +355,13 @@ __global__ void __launch_bounds__(kGnThreads) gn_apply_kernel(const __grid_const
   const int piece = blockIdx.x;
   const char* base = p.x + static_cast<long long>(span) * p.span_len * 2;
   char* obase = p.out + static_cast<long long>(span) * p.span_len * 2;
+  // checked builds: the span inside x and out (the same in every thread)
+  if (!in_span(base, static_cast<unsigned long long>(p.span_len) * 2, p.sp_x, p.status) ||
+      !in_span(obase, static_cast<unsigned long long>(p.span_len) * 2, p.sp_out, p.status))
+    return;
   if (threadIdx.x < 32)
     combine_span<false>(p.rec + static_cast<long long>(span) * (p.pieces + 1) * 2, p.pieces, p.span_len,
-                        p.piece_len, p.eps, nullptr, coef);
+                        p.piece_len, p.eps, nullptr, coef, p.sp_ws, p.status);
   __syncthreads();
   const float m1 = coef[0], rstd = coef[1];
   const float2 nk = make_float2(-coef[2], -coef[2]);
@@ -372,7 +388,10 @@ __global__ void __launch_bounds__(kGnThreads) gn_apply_kernel(const __grid_const
       if (e >= ch_end) {
         const unsigned cl = channel_of(e, p.hw);
         ch_end = (static_cast<long long>(cl) + 1) * p.hw;
-        fold_channel(__ldg(p.gamma + ch0 + cl), __ldg(p.beta + ch0 + cl), m1, rstd, A, B);
+        const float* gp = p.gamma + ch0 + cl;
+        const float* bp = p.beta + ch0 + cl;
+        const bool gb = in_span(gp, 4, p.sp_gamma, p.status) && in_span(bp, 4, p.sp_beta, p.status);
+        fold_channel(gb ? __ldg(gp) : 0.0f, gb ? __ldg(bp) : 0.0f, m1, rstd, A, B);
       }
       store16(obase + e * 2, silu_affine<T>(v[b], nk, A, B));
     }
@@ -480,6 +499,8 @@ struct GnFusedParams {
   unsigned flags;
   unsigned long long wait_limit_ns;
   float eps;
+  // address spans of the buffers (checked builds test every access against them)
+  MemSpan sp_x, sp_out, sp_ws, sp_gamma, sp_beta;
 };
 
 // (span, piece) of a CTA's chunks blockIdx.x, blockIdx.x + G, ..., kept as
@@ -598,8 +619,9 @@ __global__ void __launch_bounds__(kGnfThreads, 1) gn_fused_kernel(const __grid_c
   float* sbeta = sgamma + kGnfMaxSmemChannels;
   if (gb_smem) {
     for (int c = threadIdx.x; c < p.channels; c += blockDim.x) {
-      sgamma[c] = __ldg(p.gamma + c);
-      sbeta[c] = __ldg(p.beta + c);
+      const bool gb = in_span(p.gamma + c, 4, p.sp_gamma, p.status) && in_span(p.beta + c, 4, p.sp_beta, p.status);
+      sgamma[c] = gb ? __ldg(p.gamma + c) : 0.0f;
+      sbeta[c] = gb ? __ldg(p.beta + c) : 0.0f;
     }
   }
   __syncthreads();
@@ -638,6 +660,13 @@ __global__ void __launch_bounds__(kGnfThreads, 1) gn_fused_kernel(const __grid_c
       unsigned* meta = reinterpret_cast<unsigned*>(smem + kGnfOffMeta + 8 * s);
       meta[0] = cl;
       meta[1] = (cl + 1u) * static_cast<unsigned>(p.hw);
+      // checked builds: the chunk and the span's first 16 bytes inside x
+      // (the slot map is fixed at compile time), else nothing more is issued
+      if (!in_span(span_x + lo * 2, bytes, p.sp_x, p.status) || !in_span(span_x, 16u, p.sp_x, p.status)) {
+        give_up(RecordWait{p.tag, limit, abort_cta, p.abort_word, p.status});
+        ok = false;
+        break;
+      }
       mbar_arrive_expect_tx(full, bytes + 16u);
       bulk_load(base + kGnfOffSlot0 + s * kGnfChunkBytes, span_x + lo * 2, bytes, full);
       bulk_load(base + kGnfOffK + 16 * s, span_x, 16u, full);
@@ -682,8 +711,10 @@ __global__ void __launch_bounds__(kGnfThreads, 1) gn_fused_kernel(const __grid_c
       if (!gnf_warp_wait(cempty0 + 8 * e, use_parity ^ 1u, limit, abort_cta, p.status)) break;
       if (!gnf_wait_local(stats_done, t_end, rw.tag, rw.limit_ns, rw.abort_cta, rw.abort_grid, rw.status)) break;
       if (!combine_span<true>(p.rec + static_cast<long long>(span) * (P + 1) * 2, static_cast<int>(P), p.span_len,
-                              kGnfChunk, p.eps, &rw, coef + kGnCoefFloats * e))
+                              kGnfChunk, p.eps, &rw, coef + kGnCoefFloats * e, p.sp_ws, p.status)) {
+        if (kChecked) give_up(rw);                   // a record range outside the workspace
         break;
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(cfull0 + 8 * e);    // release: the coefficients are visible
     }
@@ -723,27 +754,37 @@ __global__ void __launch_bounds__(kGnfThreads, 1) gn_fused_kernel(const __grid_c
       const unsigned rest = static_cast<unsigned>(p.span_len) - lo;
       const int nvec = static_cast<int>(rest < kGnfChunk ? rest : kGnfChunk) / 8;
       char* obase = p.out + (static_cast<long long>(span) * p.span_len + lo) * 2;
+      // checked builds: the chunk's output inside out, else it is not written
+      const bool out_ok = in_span(obase, static_cast<unsigned long long>(nvec) * 16, p.sp_out, p.status);
       const unsigned char* slot = smem + kGnfOffSlot0 + s * kGnfChunkBytes;
       const unsigned hw = static_cast<unsigned>(p.hw);
       const uint2 meta = *reinterpret_cast<const uint2*>(smem + kGnfOffMeta + 8 * s);
       unsigned ch_end = meta.y;
+      // gamma and beta of channel ch (checked builds: inside the staged
+      // copies or the buffers)
+      auto fold = [&](int ch, float2& A_, float2& B_) {
+        bool ok;
+        if (gb_smem) {
+          ok = !kChecked || (ch >= 0 && ch < p.channels);
+          if (!ok && p.status) atomicCAS(p.status, 0, kStatusBounds);
+        } else {
+          ok = in_span(p.gamma + ch, 4, p.sp_gamma, p.status) && in_span(p.beta + ch, 4, p.sp_beta, p.status);
+        }
+        const float g = ok ? (gb_smem ? sgamma[ch] : __ldg(p.gamma + ch)) : 0.0f;
+        const float be = ok ? (gb_smem ? sbeta[ch] : __ldg(p.beta + ch)) : 0.0f;
+        fold_channel(g, be, m1, rstd, A_, B_);
+      };
       float2 A, B;
-      {
-        const int ch = ch0 + static_cast<int>(meta.x);
-        fold_channel(gb_smem ? sgamma[ch] : __ldg(p.gamma + ch), gb_smem ? sbeta[ch] : __ldg(p.beta + ch), m1, rstd,
-                     A, B);
-      }
+      fold(ch0 + static_cast<int>(meta.x), A, B);
       auto one = [&](int v) {
         const uint4 raw = *reinterpret_cast<const uint4*>(slot + v * 16);
         const unsigned e = lo + static_cast<unsigned>(v) * 8u;
         if (e >= ch_end) {
           const unsigned cl = e / hw;
           ch_end = (cl + 1u) * hw;
-          const int ch = ch0 + static_cast<int>(cl);
-          fold_channel(gb_smem ? sgamma[ch] : __ldg(p.gamma + ch), gb_smem ? sbeta[ch] : __ldg(p.beta + ch), m1,
-                       rstd, A, B);
+          fold(ch0 + static_cast<int>(cl), A, B);
         }
-        store16(obase + v * 16, silu_affine<T>(raw, nk, A, B));
+        if (out_ok) store16(obase + v * 16, silu_affine<T>(raw, nk, A, B));
       };
       if (nvec == kGnfChunk / 8) {
 #pragma unroll

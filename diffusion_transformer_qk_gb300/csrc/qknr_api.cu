@@ -313,6 +313,20 @@ qknr_status make_plan(const qknr_args* a, Plan* pl) {
   kp.off_cos = q_bytes + k_bytes + v_bytes;
   kp.off_sin = kp.off_cos + static_cast<unsigned>(cos_row_bytes);
   kp.stage_bytes = static_cast<unsigned>(stage_bytes);
+  // buffer spans for checked builds
+  auto ms = [](Span x) { return qknr::MemSpan{x.lo, x.hi}; };
+  kp.sp_q = ms(span_of(q, hq ? T : 0, qs * es, (long long)hq * D * es));
+  kp.sp_k = ms(span_of(k, hk ? T : 0, ks * es, (long long)hk * D * es));
+  kp.sp_v = ms(span_of(v, hv ? T : 0, vs * es, (long long)hv * D * es));
+  kp.sp_q_out = ms(span_of(q_out, hq ? T : 0, qos * es, (long long)hq * D * es));
+  kp.sp_k_out = ms(span_of(k_out, hk ? T : 0, kos * es, (long long)hk * D * es));
+  kp.sp_v_out = ms(span_of(a->v_out, hv ? T : 0, vos * es, (long long)hv * D * es));
+  kp.sp_cos = ms(span_of(a->cos, hq + hk ? cos_rows : 0, cos_row_bytes, cos_row_bytes));
+  kp.sp_sin = ms(span_of(a->sin, hq + hk ? cos_rows : 0, cos_row_bytes, cos_row_bytes));
+  kp.sp_gq = ms(span_of(a->gamma_q, hq ? 1 : 0, 0, (long long)D * 4));
+  kp.sp_gk = ms(span_of(a->gamma_k, hk ? 1 : 0, 0, (long long)D * 4));
+  if ((a->flags & QKNR_FLAG_TEST_SHORT_OUT) && T > 1)
+    kp.sp_q_out = ms(span_of(q_out, hq ? T - 1 : 0, qos * es, (long long)hq * D * es));
   kp.tx_bytes = static_cast<unsigned>(tx);
 
   return QKNR_OK;
@@ -437,6 +451,7 @@ qknr_status size_launch(const qknr_args* a, Plan* pl) {
   pl->grid = static_cast<int>(grid);
   pl->block = block;
   pl->smem = static_cast<int>(smem);
+  pl->kp.smem_bytes = static_cast<unsigned>(smem);
   pl->stages = stages;
   pl->ctas_per_sm = per_sm;
   pl->warps = warps;
@@ -505,6 +520,7 @@ const char* qknr_status_string(int32_t s) {
     case QKNR_ERR_TIMEOUT: return "in-kernel wait timed out";
     case QKNR_ERR_OVERLAP: return "output overlaps an input";
     case QKNR_ERR_ABI: return "ABI version mismatch";
+    case QKNR_ERR_BOUNDS: return "access outside a buffer (checked build)";
     default: return "unknown status";
   }
 }

@@ -89,6 +89,18 @@ struct KernelParams {
   unsigned off_k, off_v, off_cos, off_sin;
   unsigned stage_bytes;                              // stride between stages
   unsigned tx_bytes;                                 // bytes landing per stage
+  unsigned smem_bytes;                               // dynamic shared memory of the launch
+  // address spans of the buffers (checked builds test every access against them)
+  MemSpan sp_q, sp_k, sp_v, sp_q_out, sp_k_out, sp_v_out, sp_cos, sp_sin, sp_gq, sp_gk;
+};
+
+// What a checked build tests one tensor's accesses of one row against: the
+// row's stage in shared memory and the output buffer.
+struct RowChecks {
+  const unsigned char* stage;
+  unsigned stage_bytes;
+  MemSpan out;
+  int* status;
 };
 
 // ---------------------------------------------------------------------------
@@ -207,7 +219,7 @@ template <typename T, typename CT, int D, bool RH, bool EXPANDED>
 __device__ __forceinline__ void process_tensor(const unsigned char* seg, const unsigned char* cos_s,
                                                const unsigned char* sin_s, const float* gamma, char* out_row,
                                                int n_heads, int n_pass, int lw, int G, int lane, float eps,
-                                               float inv_d) {
+                                               float inv_d, const RowChecks& ck) {
   using Geo = Geometry<D, RH>;
   constexpr int LPH = Geo::LPH;
   constexpr int HPW = Geo::HPW;
@@ -215,6 +227,21 @@ __device__ __forceinline__ void process_tensor(const unsigned char* seg, const u
   constexpr int CES = sizeof(CT);
   const int lo = Geo::lo(lane % LPH), hi = Geo::hi(lane % LPH);
   const int hslot = lane / LPH;
+  // checked builds: head 0's staged values and the shared table row (read
+  // by every lane, also for heads past the last) must lie in the stage; a
+  // head whose own staged values, table row or output fall outside is
+  // skipped (warp-uniform for the first test, per lane for the second)
+  if (!in_smem(seg, D * ES, ck.stage, ck.stage_bytes, ck.status) ||
+      !in_smem(cos_s, D * CES, ck.stage, ck.stage_bytes, ck.status) ||
+      !in_smem(sin_s, D * CES, ck.stage, ck.stage_bytes, ck.status))
+    return;
+  auto head_ok = [&](int h) {
+    bool ok = in_smem(seg + h * D * ES, D * ES, ck.stage, ck.stage_bytes, ck.status);
+    if (EXPANDED)
+      ok = ok && in_smem(cos_s + h * D * CES, D * CES, ck.stage, ck.stage_bytes, ck.status) &&
+           in_smem(sin_s + h * D * CES, D * CES, ck.stage, ck.stage_bytes, ck.status);
+    return ok && in_span(out_row + h * D * ES, D * ES, ck.out, ck.status);
+  };
   float2 a[4], b[4];
   if (!EXPANDED) {
     // the row's one cos/sin row, folded once for every head this lane visits
@@ -227,7 +254,7 @@ __device__ __forceinline__ void process_tensor(const unsigned char* seg, const u
   for (; t + G < n_pass; t += 2 * G) {
     const int h0 = t * HPW + hslot;
     const int h1 = (t + G) * HPW + hslot;
-    const bool act0 = h0 < n_heads, act1 = h1 < n_heads;
+    const bool act0 = h0 < n_heads && head_ok(h0), act1 = h1 < n_heads && head_ok(h1);
     const int hc0 = act0 ? h0 : 0, hc1 = act1 ? h1 : 0;
     const uint4 r0 = load_lane8<RH>(seg + hc0 * D * ES, lo, hi);
     const uint4 r1 = load_lane8<RH>(seg + hc1 * D * ES, lo, hi);
@@ -251,7 +278,7 @@ __device__ __forceinline__ void process_tensor(const unsigned char* seg, const u
   }
   if (t < n_pass) {
     const int h0 = t * HPW + hslot;
-    const bool act0 = h0 < n_heads;
+    const bool act0 = h0 < n_heads && head_ok(h0);
     const int hc0 = act0 ? h0 : 0;
     const uint4 r0 = load_lane8<RH>(seg + hc0 * D * ES, lo, hi);
     if (EXPANDED) {
@@ -336,17 +363,38 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qknr_fused_kernel(const __grid
       if (p.flags & kFlagTestStall) break;   // issue nothing: the consumers' waits run out
       const uint32_t full = full0 + 8 * s;
       const uint32_t dst = stage0 + s * p.stage_bytes;
+      // checked builds: every source inside its buffer and the stage inside
+      // the launch's shared memory; a copy that fails is not issued (its
+      // stage then never completes and the waits on it run out)
+      const void* qp = reinterpret_cast<const void*>(qsrc);
+      const void* kp = reinterpret_cast<const void*>(ksrc);
+      const void* vp = reinterpret_cast<const void*>(vsrc);
+      const char* cp = p.cos + crow * p.cos_row_bytes;
+      const char* sp = p.sin + crow * p.cos_row_bytes;
+      const bool ok_copy = (!kChecked || dst + p.tx_bytes <= base + p.smem_bytes) &&
+                           (!q_bytes || in_span(qp, q_bytes, p.sp_q, p.status)) &&
+                           (!k_bytes || in_span(p.qk_merged ? static_cast<const char*>(qp) + q_bytes : kp, k_bytes,
+                                                p.sp_k, p.status)) &&
+                           (!v_bytes || in_span(vp, v_bytes, p.sp_v, p.status)) &&
+                           (!c_bytes || (in_span(cp, c_bytes, p.sp_cos, p.status) &&
+                                         in_span(sp, c_bytes, p.sp_sin, p.status)));
+      if (!ok_copy) {
+        if (p.status) atomicCAS(p.status, 0, kStatusBounds);
+        *abort_flag = 1;
+        ok = false;
+        break;
+      }
       mbar_arrive_expect_tx(full, p.tx_bytes);
       if (p.qk_merged) {
-        bulk_load(dst, reinterpret_cast<const void*>(qsrc), q_bytes + k_bytes, full);
+        bulk_load(dst, qp, q_bytes + k_bytes, full);
       } else {
-        if (q_bytes) bulk_load(dst, reinterpret_cast<const void*>(qsrc), q_bytes, full);
-        if (k_bytes) bulk_load(dst + p.off_k, reinterpret_cast<const void*>(ksrc), k_bytes, full);
+        if (q_bytes) bulk_load(dst, qp, q_bytes, full);
+        if (k_bytes) bulk_load(dst + p.off_k, kp, k_bytes, full);
       }
-      if (v_bytes) bulk_load(dst + p.off_v, reinterpret_cast<const void*>(vsrc), v_bytes, full);
+      if (v_bytes) bulk_load(dst + p.off_v, vp, v_bytes, full);
       if (c_bytes) {
-        bulk_load(dst + p.off_cos, p.cos + crow * p.cos_row_bytes, c_bytes, full);
-        bulk_load(dst + p.off_sin, p.sin + crow * p.cos_row_bytes, c_bytes, full);
+        bulk_load(dst + p.off_cos, cp, c_bytes, full);
+        bulk_load(dst + p.off_sin, sp, c_bytes, full);
       }
       ++issued;
       qsrc += qstep;
@@ -387,8 +435,10 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qknr_fused_kernel(const __grid
   // The gains go to shared memory while the producer's first loads are in
   // flight; the consumer warps alone wait for them (named barrier 1).
   for (int i = threadIdx.x; i < 2 * D; i += NW * 32) {
-    const float* g = i < D ? p.gamma_q : p.gamma_k;
-    gam[i] = g ? g[i < D ? i : i - D] : 1.0f;
+    // a tensor with no heads may come without its gains: not read then
+    const float* g = i < D ? (p.hq ? p.gamma_q : nullptr) : (p.hk ? p.gamma_k : nullptr);
+    const float* gi = g ? g + (i < D ? i : i - D) : nullptr;
+    gam[i] = gi && in_span(gi, 4, i < D ? p.sp_gq : p.sp_gk, p.status) ? *gi : 1.0f;
   }
   named_barrier_sync(1, NW * 32);
 
@@ -418,15 +468,18 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qknr_fused_kernel(const __grid
     if (do_q && nq)
       process_tensor<T, CT, D, RH, EXPANDED>(st, st + p.off_cos, st + p.off_sin, gam,
                                              p.q_out + row * p.q_out_stride, p.hq, nq, gw, p.warps_q, lane, eps,
-                                             inv_d);
+                                             inv_d, RowChecks{st, p.stage_bytes, p.sp_q_out, p.status});
     if (do_k && nk)
       process_tensor<T, CT, D, RH, EXPANDED>(st + p.off_k, st + p.off_cos, st + p.off_sin, gam + D,
                                              p.k_out + row * p.k_out_stride, p.hk, nk, gw - (GW - p.warps_k),
-                                             p.warps_k, lane, eps, inv_d);
+                                             p.warps_k, lane, eps, inv_d,
+                                             RowChecks{st, p.stage_bytes, p.sp_k_out, p.status});
     // V pass-through copy, 16 bytes per lane
     for (int off = (gw * 32 + lane) * 16; off < v_row; off += GW * 512) {
-      const uint4 raw = *reinterpret_cast<const uint4*>(st + p.off_v + off);
-      store16(p.v_out + row * p.v_out_stride + off, raw);
+      const unsigned char* src = st + p.off_v + off;
+      char* dstv = p.v_out + row * p.v_out_stride + off;
+      if (in_smem(src, 16, st, p.stage_bytes, p.status) && in_span(dstv, 16, p.sp_v_out, p.status))
+        store16(dstv, *reinterpret_cast<const uint4*>(src));
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(empty0 + 8 * (ring0 + s));

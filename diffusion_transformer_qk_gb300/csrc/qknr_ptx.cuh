@@ -11,6 +11,43 @@
 namespace qknr {
 
 constexpr int kStatusTimeout = 6;     // QKNR_ERR_TIMEOUT
+constexpr int kStatusBounds = 9;      // QKNR_ERR_BOUNDS
+
+// ---------------------------------------------------------------------------
+// Debug builds (QKNR_CHECKED): every global access is checked against the
+// address span of the buffer it belongs to, and every shared-memory stage
+// read against its stage.  An access outside them is skipped and
+// QKNR_ERR_BOUNDS goes to the caller's status word (no assert, no trap).
+// In the regular build the checks are constant true and compile away.
+
+#ifdef QKNR_CHECKED
+constexpr bool kChecked = true;
+#else
+constexpr bool kChecked = false;
+#endif
+
+// [lo, hi) byte addresses of a buffer (empty: lo == hi)
+struct MemSpan {
+  unsigned long long lo, hi;
+};
+
+__device__ __forceinline__ bool in_span(const void* p, unsigned long long bytes, const MemSpan& s, int* status) {
+  if (!kChecked) return true;
+  const unsigned long long a = reinterpret_cast<unsigned long long>(p);
+  if (a >= s.lo && a + bytes >= a && a + bytes <= s.hi) return true;
+  if (status) atomicCAS(status, 0, kStatusBounds);
+  return false;
+}
+
+// a generic pointer into this CTA's shared memory, within [lo, lo + size)
+__device__ __forceinline__ bool in_smem(const void* p, unsigned bytes, const void* lo, unsigned size, int* status) {
+  if (!kChecked) return true;
+  const char* a = static_cast<const char*>(p);
+  const char* b = static_cast<const char*>(lo);
+  if (a >= b && a + bytes <= b + size) return true;
+  if (status) atomicCAS(status, 0, kStatusBounds);
+  return false;
+}
 
 // ---------------------------------------------------------------------------
 // PTX helpers

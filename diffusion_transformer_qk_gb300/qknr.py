@@ -28,11 +28,13 @@ COS_LAYOUT = {"shared_row": 0, "per_head_expanded": 1}
 STATUS = {
     0: "QKNR_OK", 1: "QKNR_ERR_NULL", 2: "QKNR_ERR_SHAPE", 3: "QKNR_ERR_ALIGN",
     4: "QKNR_ERR_UNSUPPORTED", 5: "QKNR_ERR_CUDA", 6: "QKNR_ERR_TIMEOUT",
-    7: "QKNR_ERR_OVERLAP", 8: "QKNR_ERR_ABI",
+    7: "QKNR_ERR_OVERLAP", 8: "QKNR_ERR_ABI", 9: "QKNR_ERR_BOUNDS",
 }
+STATUS_BY_NAME = {v: k for k, v in STATUS.items()}
 OK, ERR_TIMEOUT = 0, 6
 FLAG_TEST_STALL = 0x1
 FLAG_NO_OVERLAP = 0x2
+FLAG_TEST_SHORT_OUT = 0x4
 ABI_VERSION = 2
 
 EXPORTS = (
@@ -137,8 +139,8 @@ _lib = None
 _lock = threading.Lock()
 
 
-def library_path() -> str:
-    return _build.library_path()
+def library_path(checked: bool = False) -> str:
+    return _build.library_path(checked)
 
 
 def load(path: Optional[str] = None) -> ctypes.CDLL:

@@ -75,7 +75,10 @@ typedef enum {
   QKNR_ERR_CUDA = 5,        /* a CUDA runtime call failed; see qknr_last_error() */
   QKNR_ERR_TIMEOUT = 6,     /* written to *dev_status by a kernel whose wait ran out */
   QKNR_ERR_OVERLAP = 7,     /* an output partially overlaps an input */
-  QKNR_ERR_ABI = 8          /* args->abi_version != QKNR_ABI_VERSION */
+  QKNR_ERR_ABI = 8,         /* args->abi_version != QKNR_ABI_VERSION */
+  QKNR_ERR_BOUNDS = 9       /* written to *dev_status by a kernel of the checked build
+                               (libqknr_checked.so) that found an access outside its
+                               buffers; the access was skipped */
 } qknr_status;
 
 /* Launch-time flags (qknr_args.flags). */
@@ -83,6 +86,10 @@ typedef enum {
                                      and the kernel reports QKNR_ERR_TIMEOUT */
 #define QKNR_FLAG_NO_OVERLAP 0x2u /* launch without programmatic dependent launch (see
                                      qknr_forward) */
+#define QKNR_FLAG_TEST_SHORT_OUT 0x4u /* test only, checked build: the Q output span its
+                                         kernel checks against ends one row early, so the
+                                         last row's Q stores are refused and reported as
+                                         QKNR_ERR_BOUNDS (ignored by the regular build) */
 
 /*
  * Arguments of one call.  Fill with qknr_args_init() and then set fields.
