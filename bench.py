@@ -1039,7 +1039,7 @@ def main(argv=None):
     p.add_argument("--consumer-warps", type=int, default=0)
     p.add_argument("--group-warps", type=int, default=0)
     p.add_argument("--e2e-steps", type=int, default=20)
-    p.add_argument("--e2e-chunk-rows", type=int, default=4096)
+    p.add_argument("--e2e-chunk-rows", type=int, default=2048)
     p.add_argument("--l2-flush", choices=["auto", "on", "off"], default="auto")
     p.add_argument("--dtype", choices=["bf16", "fp16"], default=None,
                    help="activation dtype of the workload (default: the workload's own, bf16)")

@@ -203,7 +203,7 @@ void qknr_host_plan_init(qknr_host_plan* p) {
   memset(p, 0, sizeof(*p));
   p->abi_version = QKNR_ABI_VERSION;
   p->n_buffers = 3;
-  p->chunk_rows = 4096;
+  p->chunk_rows = 2048;
 }
 
 size_t qknr_sizeof_host_plan(void) { return sizeof(qknr_host_plan); }
@@ -251,23 +251,49 @@ qknr_status qknr_forward_host(const qknr_args* args, const qknr_host_plan* plan,
   if ((st = record(start, s)) != QKNR_OK || (st = wait(h2d, start)) != QKNR_OK || (st = wait(d2h, start)) != QKNR_OK)
     return st;
   const long long D = P.D;
+  // the gains, and a batch-broadcast table, go in first; a per-token table
+  // goes in with each chunk, its rows ahead of the chunk's activation
   const void* host_tab[4] = {plan->host_gamma_q, plan->host_gamma_k, plan->host_cos, plan->host_sin};
   const void* dev_tab[4] = {args->gamma_q, args->gamma_k, args->cos, args->sin};
   const long long tab_bytes[4] = {D * 4, D * 4, P.cos_rows * P.cos_row_bytes, P.cos_rows * P.cos_row_bytes};
-  for (int i = 0; i < 4; ++i) {
-    if (!host_tab[i]) continue;
-    if (!dev_tab[i]) return fail(QKNR_ERR_NULL, "a host table is given but its device pointer is NULL");
-    const cudaError_t e = cudaMemcpyAsync(const_cast<void*>(dev_tab[i]), host_tab[i], static_cast<size_t>(tab_bytes[i]),
+  for (int i = 0; i < 4; ++i)
+    if (host_tab[i] && !dev_tab[i]) return fail(QKNR_ERR_NULL, "a host table is given but its device pointer is NULL");
+  auto copy_table = [&](int i, long long off, long long bytes) -> qknr_status {
+    const cudaError_t e = cudaMemcpyAsync(const_cast<char*>(static_cast<const char*>(dev_tab[i])) + off,
+                                          static_cast<const char*>(host_tab[i]) + off, static_cast<size_t>(bytes),
                                           cudaMemcpyHostToDevice, h2d);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync(table)");
-  }
+    return e == cudaSuccess ? QKNR_OK : cuda_fail(e, "cudaMemcpyAsync(table)");
+  };
+  for (int i = 0; i < 4; ++i)
+    if (host_tab[i] && (i < 2 || !P.per_token_table) && (st = copy_table(i, 0, tab_bytes[i])) != QKNR_OK) return st;
+  // Chunk sizes: with a per-token table the first chunks ramp up (1/8, 1/4,
+  // 1/2 of chunk_rows) and the last ones ramp down the same way, so that
+  // the copy in of the first chunk and the copy out of the last, which
+  // nothing overlaps, are short; in between, chunk_rows each.  (A
+  // batch-broadcast table needs every chunk to start on a multiple of its
+  // rows: chunk_rows each.)
+  const long long C = P.chunk, c8 = C / 8;
+  const bool ramp = P.per_token_table && c8 >= 8 && P.T >= 4 * C;
+  const long long head_end = 7 * c8, tail_start = P.T - 8 * c8;
+  auto chunk_rows_at = [&](long long r0) -> long long {
+    if (ramp && r0 < head_end) return r0 == 0 ? c8 : (r0 == c8 ? 2 * c8 : 4 * c8);
+    if (ramp && r0 >= tail_start) {
+      const long long k = r0 - tail_start;
+      return k == 0 ? 4 * c8 : (k == 4 * c8 ? 2 * c8 : c8);
+    }
+    const long long end = ramp ? tail_start : P.T;
+    return end - r0 < C ? end - r0 : C;
+  };
   long long i = 0;
-  for (long long r0 = 0; r0 < P.T; r0 += P.chunk, ++i) {
-    const long long rows = P.T - r0 < P.chunk ? P.T - r0 : P.chunk;
+  for (long long r0 = 0; r0 < P.T; ++i) {
+    const long long rows = chunk_rows_at(r0);
     const int b = static_cast<int>(i % nb);
     char* buf = static_cast<char*>(plan->dev_buffers[b]);
     // in: after this buffer's previous chunk has been copied out
     if (i >= nb && (st = wait(h2d, freed[b])) != QKNR_OK) return st;
+    if (P.per_token_table)
+      for (int t = 2; t < 4; ++t)
+        if (host_tab[t] && (st = copy_table(t, r0 * P.cos_row_bytes, rows * P.cos_row_bytes)) != QKNR_OK) return st;
     if ((st = copy_chunk(P, P.in, P.in_joined, buf, r0, rows, true, h2d)) != QKNR_OK) return st;
     if ((st = record(loaded[b], h2d)) != QKNR_OK || (st = wait(s, loaded[b])) != QKNR_OK) return st;
     // the kernel, in place in the staging buffer
@@ -277,6 +303,7 @@ qknr_status qknr_forward_host(const qknr_args* args, const qknr_host_plan* plan,
     // out
     if ((st = copy_chunk(P, P.out, P.out_joined, buf, r0, rows, false, d2h)) != QKNR_OK) return st;
     if ((st = record(freed[b], d2h)) != QKNR_OK) return st;
+    r0 += rows;
   }
   // the call's stream sees the results once every copy out is done
   if ((st = record(done, d2h)) != QKNR_OK) return st;

@@ -505,7 +505,7 @@ class HostPipeline:
     activation.
     """
 
-    def __init__(self, width: int, dtype: torch.dtype, chunk_rows: int = 4096, n_buffers: int = 3,
+    def __init__(self, width: int, dtype: torch.dtype, chunk_rows: int = 2048, n_buffers: int = 3,
                  device=None):
         lib = load()
         self.device = torch.device("cuda", torch.cuda.current_device() if device is None

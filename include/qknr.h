@@ -215,7 +215,11 @@ const char *qknr_last_error(void);
  * Every row is processed by the same kernel with the same table row as in
  * one qknr_forward() over the whole activation, so the results are the same
  * bits.  A table with cos_rows < tokens (batch broadcast) needs chunk_rows
- * to be a multiple of cos_rows.
+ * to be a multiple of cos_rows.  With a per-token table and at least four
+ * chunks' worth of rows, the first chunks ramp up (chunk_rows/8, /4, /2)
+ * and the last ones ramp down, so the copy in of the first chunk and the
+ * copy out of the last, which nothing overlaps, stay short; each chunk's
+ * table rows are copied in with it.
  */
 
 /* Same type as cudaEvent_t. */
@@ -248,7 +252,7 @@ typedef struct qknr_host_plan {
   const void *host_gamma_q, *host_gamma_k, *host_cos, *host_sin;
 } qknr_host_plan;
 
-/* Defaults: 3 buffers, 4096-row chunks, everything else zero. */
+/* Defaults: 3 buffers, 2048-row chunks, everything else zero. */
 void qknr_host_plan_init(qknr_host_plan *p);
 
 /* Bytes each device staging buffer needs for these arguments and plan:

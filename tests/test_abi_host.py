@@ -310,7 +310,7 @@ def test_gn_validation_rejects(lib, mutate, expect):
 def valid_host_plan(n=3, chunk=16):
     p = Q.QknrHostPlan()
     Q.load().qknr_host_plan_init(ctypes.byref(p))
-    assert p.abi_version == Q.ABI_VERSION and p.n_buffers == 3 and p.chunk_rows == 4096
+    assert p.abi_version == Q.ABI_VERSION and p.n_buffers == 3 and p.chunk_rows == 2048
     p.n_buffers, p.chunk_rows = n, chunk
     for i in range(n):
         p.dev_buffers[i] = FAKE + (4 << 30) + i * (1 << 24)

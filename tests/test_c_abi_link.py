@@ -79,7 +79,7 @@ int main(void) {
     qknr_args_init(&a);
     qknr_host_plan_init(&hp);
     CHECK(qknr_sizeof_host_plan() == sizeof(qknr_host_plan), 50);
-    CHECK(hp.abi_version == QKNR_ABI_VERSION && hp.n_buffers == 3 && hp.chunk_rows == 4096, 51);
+    CHECK(hp.abi_version == QKNR_ABI_VERSION && hp.n_buffers == 3 && hp.chunk_rows == 2048, 51);
     CHECK(qknr_forward_host(NULL, &hp, NULL) == QKNR_ERR_NULL, 52);
     CHECK(qknr_forward_host(&a, NULL, NULL) == QKNR_ERR_NULL, 53);
     a.head_dim = 128;

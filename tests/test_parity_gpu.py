@@ -195,7 +195,7 @@ def test_shared_fp32_matches_expanded_matrix(style, H, D):
 # ---------------------------------------------------------------------------
 # host-resident activations through the chunked pipeline
 
-@pytest.mark.parametrize("T,chunk", [(10000, 4096), (4096, 4096), (777, 256)])
+@pytest.mark.parametrize("T,chunk", [(10000, 4096), (4096, 4096), (777, 256), (20000, 2048)])
 def test_host_pipeline_matches_device_path(T, chunk):
     w = I.WORKLOADS["wan_32760x40x128"].with_(n_heads_q=8, n_heads_k=8, n_heads_v=8)
     inp = I.make_inputs(w, tokens=T)
