@@ -133,3 +133,31 @@ def test_adaln_chain_matches_plain_launches():
         np.testing.assert_array_equal(a, b)
     ref = A.adaln_modulate(inp["x"], w.dtype, inp["scale"], inp["shift"], w.mod_dtype, w.eps, w.seq)
     compare(outs[0][0], ref, w.dtype, "AdaLN")
+
+
+def test_calls_right_after_a_cooperative_group_norm_launch():
+    # the fused group norm is a cooperative launch; the QK and AdaLN calls
+    # launched right after it (programmatic dependent launch) read what it
+    # wrote and must give the bits of plain launches
+    wg = I.GroupNormWorkload("g", 1, 64, 96, 96, groups=32, seed=41)
+    ig = I.make_gn_inputs(wg)
+    gam, bet = torch.from_numpy(ig["gamma"]).cuda(), torch.from_numpy(ig["beta"]).cuda()
+    w, inp, dev = _dense(tokens=2304)
+    res = []
+    for flags in (0, Q.FLAG_NO_OVERLAP):
+        x = to_dev(ig["x"], wg.dtype)
+        qkv = to_dev(inp["qkv"], w.dtype)
+        torch.cuda.synchronize()
+        # the group norm writes x; the QK call then takes x's bits as its Q|K
+        # columns' source: copy x into them with a kernel, then normalise
+        Q.group_norm_silu(x, wg.groups, gam, bet, eps=wg.eps, mode="fused")
+        rows = x.numel() // (48 * 128)                      # 96 rows of Q|K columns
+        qk = qkv.view(torch.int16)[:rows, : 48 * 128]
+        torch.bitwise_or(x.view(torch.int16).reshape(rows, 48 * 128), 0, out=qk)
+        _call(w, qkv, dev, flags)
+        Q.group_norm_silu(x, wg.groups, gam, bet, eps=wg.eps, mode="fused")
+        _call(w, qkv, dev, flags)
+        torch.cuda.synchronize()
+        res.append((to_bits(x), to_bits(qkv)))
+    np.testing.assert_array_equal(res[0][0], res[1][0])
+    np.testing.assert_array_equal(res[0][1], res[1][1])
