@@ -9,9 +9,11 @@ in place, V untouched.
 
 Prints one JSON line: microseconds per call (whole job), achieved HBM
 bandwidth against the measured copy peak, the CPU oracle's time on a
-bounded sample, an end-to-end number through the public Python API with
-host buffers, the SM clocks seen during the timed region and the launch
-count.  ``--impl reference`` times the fp64 CPU oracle instead.
+bounded sample, an end-to-end number from pinned host buffers (one
+qknr_forward_host call per step), the SM clocks seen during the timed
+region, the launch count, and (with the default workload) every other
+workload and variant timed the same way (``configs``).  ``--impl
+reference`` times the fp64 CPU oracle instead.
 
 Multi-GPU: one process per GPU (torchrun); every rank runs its own full
 workload (replicas, weak scaling), timing is the max over ranks.
@@ -482,9 +484,10 @@ class Runner:
 
     def e2e_buffers(self, chunk_rows):
         """Pinned host copies of every input and output.  Packed workloads go
-        through the binding's chunked host pipeline (copies in, kernel and
-        copies out overlapped on three streams); separate tensors are copied
-        in, processed and copied out on one stream."""
+        through qknr_forward_host (the binding's HostPipeline: copies in,
+        kernel and copies out overlapped on three streams inside the
+        library); separate tensors are copied in, processed and copied out
+        on one stream."""
         self.pinned = {k: v.pin_memory() for k, v in self.host.items() if k not in self.outputs or k in
                        ("qkv", "q", "k")}
         self.pinned_out = {k: torch_empty_pinned_like(self.host[k]) for k in self.outputs}

@@ -29,8 +29,9 @@
  * give bitwise-equal outputs.
  *
  * Ownership: the caller owns every buffer.  The library allocates no
- * memory, never synchronises the stream, and keeps no state between calls
- * beyond a per-kernel "max dynamic shared memory" attribute it sets once.
+ * memory and never synchronises the stream.  Between calls it keeps only
+ * what it looks up once and caches: device attributes, a per-kernel
+ * "max dynamic shared memory" attribute it sets, and occupancy queries.
  */
 #ifndef QKNR_H_
 #define QKNR_H_
