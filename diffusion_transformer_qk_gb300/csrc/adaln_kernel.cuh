@@ -9,7 +9,11 @@
 // Same streaming structure as the QK kernel: a persistent CTA per SM, one
 // producer lane bulk-copying token rows into per-group shared-memory rings,
 // consumer warps in groups that each take whole rows, so several rows are
-// in flight.  Lane l of warp w of a group of GW warps handles the 16-byte
+// in flight.  The producer gives each of the CTA's rows (blockIdx.x,
+// blockIdx.x + gridDim.x, ...) to whichever group has a free stage first,
+// writing the row's index beside the stage; a group that works faster
+// takes more rows, and when the rows run out each group's next stage
+// carries an end mark.  Lane l of warp w of a group of GW warps handles the 16-byte
 // chunks k = (w*32 + l) + i*32*GW of the staged row.
 //
 // Statistics in one pass over the staged row (moments.cuh): each thread
@@ -30,6 +34,7 @@
 
 #include "moments.cuh"
 #include "qknr_ptx.cuh"
+#include "rings.cuh"
 
 namespace qknr {
 
@@ -40,6 +45,9 @@ constexpr int kAdaMaxGroups = 8;                  // named barriers 1..8
 // dynamic shared memory map (bytes)
 constexpr int kAdaOffBarriers = 0;                // full[32], empty[32]
 constexpr int kAdaOffAbort = 512;
+constexpr int kAdaOffStageRow = 576;              // [32] int64: the row a stage holds (-1: no more rows)
+constexpr int kAdaOffGroupPos = 832;              // producer's ring bookkeeping (rings.cuh), 192 B
+static_assert(kAdaOffGroupPos + kRingPosBytes <= 1024 && kAdaMaxGroups <= kRingMaxGroups, "shared memory map");
 // per group: two row-parity buffers of [3][kAdaMaxWarps] floats (two sums, ok flags)
 constexpr int kAdaOffPartial = 1024;
 constexpr int kAdaPartialFloats = 2 * 3 * kAdaMaxWarps;
@@ -116,6 +124,7 @@ __global__ void __launch_bounds__(kAdaMaxThreads, 1) adaln_kernel(const __grid_c
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, GW);
     }
+    GroupRings(smem + kAdaOffGroupPos, n_groups, S, empty0).init();
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -129,21 +138,20 @@ __global__ void __launch_bounds__(kAdaMaxThreads, 1) adaln_kernel(const __grid_c
     // ---------------- producer: one lane, one bulk copy per row
     if (lane != 0) return;
     const uint32_t stage0 = base + kAdaOffStage0;
-    long long issued = 0;
-    int g = 0, js = 0;
-    uint32_t ph = 0;
+    long long* stage_row = reinterpret_cast<long long*>(smem + kAdaOffStageRow);
+    GroupRings rings(smem + kAdaOffGroupPos, n_groups, S, empty0);
     const long long step = gridDim.x;
     unsigned long long src = reinterpret_cast<unsigned long long>(p.x) + blockIdx.x * p.x_stride;
     const unsigned long long src_step = step * p.x_stride;
     bool ok = true;
     for (long long row = blockIdx.x; row < p.tokens; row += step) {
-      const int s = g * S + js;
-      const uint32_t empty = empty0 + 8 * s;
-      if (!mbar_try_wait(empty, ph ^ 1u) && !bounded_wait(empty, ph ^ 1u, limit, abort_flag, p.status)) {
+      const int gg = rings.free_group(limit, abort_flag, p.status);
+      if (gg < 0) {
         ok = false;
         break;
       }
       if (p.flags & 1u) break;                    // test only: issue nothing
+      const int s = gg * S + rings.slot(gg);
       // checked builds: the row inside x and the stage inside the launch's
       // shared memory, else nothing more is issued and the CTA gives up
       if (!in_span(reinterpret_cast<const void*>(src), p.row_bytes, p.sp_x, p.status) ||
@@ -153,33 +161,29 @@ __global__ void __launch_bounds__(kAdaMaxThreads, 1) adaln_kernel(const __grid_c
         ok = false;
         break;
       }
+      stage_row[s] = row;                         // published by the arrive below
       const uint32_t full = full0 + 8 * s;
       mbar_arrive_expect_tx(full, p.row_bytes);
       bulk_load(stage0 + s * p.stage_bytes, reinterpret_cast<const void*>(src), p.row_bytes, full);
-      ++issued;
+      rings.advance(gg);
       src += src_step;
-      if (++g == n_groups) {
-        g = 0;
-        if (++js == S) {
-          js = 0;
-          ph ^= 1u;
-        }
-      }
     }
     grid_dependents_launch();
-    if (!ok || *abort_flag) {
-      // wait (bounded) for the copies of the latest use of every stage
-      const long long total = static_cast<long long>(n_groups) * S;
-      const long long first = issued > total ? issued - total : 0;
-      for (long long it = first; it < issued; ++it) {
-        const long long j = it / n_groups;
-        const uint32_t bar = full0 + 8 * (static_cast<int>(it % n_groups) * S + static_cast<int>(j % S));
-        const uint32_t phase = static_cast<uint32_t>((j / S) & 1);
-        const unsigned long long t0 = global_timer_ns();
-        while (!mbar_try_wait(bar, phase) && global_timer_ns() - t0 < limit) {
+    if (ok && !(p.flags & 1u)) {
+      // no more rows: each group's next stage carries the end mark
+      for (int done = 0; done < n_groups; ++done) {
+        const int gg = rings.free_group(limit, abort_flag, p.status);
+        if (gg < 0) {
+          ok = false;
+          break;
         }
+        const int s = gg * S + rings.slot(gg);
+        stage_row[s] = -1;
+        mbar_arrive(full0 + 8 * s);
+        rings.mark(gg);
       }
     }
+    if (!ok || *abort_flag) rings.drain(full0, limit);
     return;
   }
 
@@ -195,18 +199,18 @@ __global__ void __launch_bounds__(kAdaMaxThreads, 1) adaln_kernel(const __grid_c
   const float my_n = lane_g < n_chunks ? 8.0f * static_cast<float>((n_chunks - 1 - lane_g) / gthreads + 1) : 0.0f;
   const int ring0 = grp * S;
 
+  const long long* stage_row = reinterpret_cast<const long long*>(smem + kAdaOffStageRow);
   int s = 0;
   uint32_t ph = 0;
   int parity = 0;                                 // partial-sum buffer of this row
-  const long long step = static_cast<long long>(n_groups) * gridDim.x;
-  long long row = blockIdx.x + static_cast<long long>(grp) * gridDim.x;
-  // sample of the current row, kept as a running quotient and remainder
-  long long batch = row / p.rows_per_batch;
-  long long in_batch = row - batch * p.rows_per_batch;
-  const long long step_b = step / p.rows_per_batch, step_r = step - step_b * p.rows_per_batch;
-  for (; row < p.tokens; row += step) {
+  for (;;) {
     const uint32_t full = full0 + 8 * (ring0 + s);
-    const bool ok = mbar_try_wait(full, ph) || bounded_wait(full, ph, limit, abort_flag, p.status);
+    const bool got = mbar_try_wait(full, ph) || bounded_wait(full, ph, limit, abort_flag, p.status);
+    // the row this stage holds; the end mark (or a failed wait) makes the
+    // group leave together at the barrier below
+    const long long row = got ? stage_row[ring0 + s] : -1;
+    const bool ok = got && row >= 0;
+    const long long batch = ok ? row / p.rows_per_batch : 0;
     const unsigned char* st = smem + kAdaOffStage0 + (ring0 + s) * p.stage_bytes;
 
     float2 a1 = make_float2(0.0f, 0.0f), a2 = make_float2(0.0f, 0.0f);
@@ -300,12 +304,6 @@ __global__ void __launch_bounds__(kAdaMaxThreads, 1) adaln_kernel(const __grid_c
     if (++s == S) {
       s = 0;
       ph ^= 1u;
-    }
-    batch += step_b;
-    in_batch += step_r;
-    if (in_batch >= p.rows_per_batch) {
-      in_batch -= p.rows_per_batch;
-      ++batch;
     }
   }
 }
