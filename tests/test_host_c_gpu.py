@@ -4,6 +4,7 @@ packed QKV activation and the tables from files, makes its staging buffers,
 streams and events, runs the call in place and out of place, and writes the
 results back; they must be bitwise those of qknr_forward on a device copy of
 the whole activation, with V unchanged (in place) or copied (out of place)."""
+import ctypes
 import os
 import shutil
 import subprocess
@@ -201,3 +202,71 @@ def test_c_program_host_call_matches_the_device_path(program, tmp_path, T, seq, 
     np.testing.assert_array_equal(ip, once)                           # V never left the host
     np.testing.assert_array_equal(ip2, twice)
     np.testing.assert_array_equal(ip[:, 2 * H * D:], inp["qkv"][:, 2 * H * D:])
+
+
+# ---------------------------------------------------------------------------
+# qknr_forward_host through the binding: per-head expanded tables, separate
+# host tensors, fp16
+
+def _pinned_bits(bits, dtype):
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(
+        torch.bfloat16 if dtype == "bf16" else torch.float16)
+    return t.pin_memory()
+
+
+@pytest.mark.parametrize("dtype,cos_dtype", [("bf16", "fp32"), ("fp16", "bf16")])
+def test_host_pipeline_with_expanded_tables_that_differ_per_head(built_lib, cuda_device, dtype, cos_dtype):
+    H, D, T, chunk = 8, 128, 9000, 1024           # T >= 4 chunks: the chunk sizes ramp up and down
+    w = I.WORKLOADS["wan_32760x40x128"].with_(n_heads_q=H, n_heads_k=H, n_heads_v=H, dtype=dtype, seq=T,
+                                              positions="1d", grid=(), axes_dim=(D,), rope_style="rotate_half",
+                                              cos_dtype=cos_dtype, cos_layout="per_head_expanded")
+    inp = I.make_inputs(w)
+    ce, se = I.per_head_tables(T, H, D, "rotate_half", cos_dtype, seed=71)
+    dev_tab = (lambda t: table_to_dev(t, cos_dtype))
+    ref = to_dev(inp["qkv"], dtype)
+    Q.qk_norm_rope_packed(ref, H, H, H, D, torch.from_numpy(inp["gamma_q"]).cuda(),
+                          torch.from_numpy(inp["gamma_k"]).cuda(), dev_tab(ce), dev_tab(se), rope_style="rotate_half",
+                          cos_layout="per_head_expanded", eps=w.eps)
+    host = _pinned_bits(inp["qkv"], dtype)
+    host_tab = (lambda t: torch.from_numpy(t).pin_memory() if cos_dtype == "fp32" else _pinned_bits(t, "bf16"))
+    pipe = Q.HostPipeline(host.shape[1], host.dtype, chunk_rows=chunk)
+    pipe(host, H, H, H, D, torch.from_numpy(inp["gamma_q"]).pin_memory(), torch.from_numpy(inp["gamma_k"]).pin_memory(),
+         host_tab(ce), host_tab(se), rope_style="rotate_half", cos_layout="per_head_expanded", eps=w.eps)
+    torch.cuda.synchronize()
+    assert pipe.read_status() == 0
+    np.testing.assert_array_equal(host.view(torch.int16).numpy().view(np.uint16), to_bits(ref))
+
+
+def test_host_call_on_separate_host_tensors_with_a_v_copy(built_lib, cuda_device):
+    # FLUX.2-style separate Q, K, V in host memory, written to separate host
+    # outputs with V copied through, in one qknr_forward_host call
+    H, D, S, B = 16, 128, 1000, 3                 # a batch-broadcast table: chunks are whole samples
+    T = B * S
+    w = I.WORKLOADS["flux2_2x4608x48x128"].with_(n_heads_q=H, n_heads_k=H, n_heads_v=H, seq=S, batch=B,
+                                                 positions="1d", grid=(), axes_dim=(D,))
+    inp = I.make_inputs(w)
+    cos, sin = table_to_dev(inp["cos"], "fp32"), table_to_dev(inp["sin"], "fp32")
+    gq, gk = torch.from_numpy(inp["gamma_q"]).cuda(), torch.from_numpy(inp["gamma_k"]).cuda()
+    dq, dk = to_dev(inp["q"], "bf16"), to_dev(inp["k"], "bf16")
+    Q.qk_norm_rope_separate(dq, dk, H, D, gq, gk, cos, sin, rope_style=w.rope_style)
+    hq, hk, hv = (_pinned_bits(inp[n], "bf16") for n in ("q", "k", "v"))
+    oq, ok, ov = (torch.empty_like(t).pin_memory() for t in (hq, hk, hv))
+    pipe = Q.HostPipeline(3 * H * D, torch.bfloat16, chunk_rows=2000)      # staging rows hold Q | K | V
+    a = Q.host_args(q=hq, k=hk, v=hv, q_out=oq, k_out=ok, v_out=ov, n_heads_q=H, n_heads_k=H, n_heads_v=H,
+                    head_dim=D, tokens=T, gamma_q=gq, gamma_k=gk, cos=cos, sin=sin, cos_rows=S,
+                    rope_style=w.rope_style, eps=w.eps, dev_status=pipe.status)
+    need = ctypes.c_size_t(0)
+    lib = Q.load()
+    assert lib.qknr_host_buffer_bytes(ctypes.byref(a), ctypes.byref(pipe.plan), ctypes.byref(need)) == 0
+    assert need.value == 2000 * 3 * H * D * 2                          # chunks of 2000 and 1000 rows
+    pipe.plan.host_gamma_q = pipe.plan.host_gamma_k = pipe.plan.host_cos = pipe.plan.host_sin = None
+    st = lib.qknr_forward_host(ctypes.byref(a), ctypes.byref(pipe.plan), ctypes.c_void_p(
+        torch.cuda.current_stream().cuda_stream))
+    assert st == 0, lib.qknr_last_error()
+    torch.cuda.synchronize()
+    assert pipe.read_status() == 0
+    np.testing.assert_array_equal(oq.view(torch.int16).numpy().view(np.uint16), to_bits(dq))
+    np.testing.assert_array_equal(ok.view(torch.int16).numpy().view(np.uint16), to_bits(dk))
+    np.testing.assert_array_equal(ov.view(torch.int16).numpy().view(np.uint16), inp["v"])
+    for t, n in ((hq, "q"), (hk, "k"), (hv, "v")):                         # inputs untouched
+        np.testing.assert_array_equal(t.view(torch.int16).numpy().view(np.uint16), inp[n])
