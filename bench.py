@@ -786,7 +786,7 @@ def run_ours(args, w):
         "gpu_launches": K * L * getattr(run, "launches_per_call", 1),
         "clocks": clocks,
         "launch": {k: info[k] for k in ("grid", "block", "dyn_smem", "stages", "ctas_per_sm", "consumer_warps",
-                                        "stage_bytes", "registers", "num_sms")},
+                                        "stage_bytes", "registers", "num_sms", "prefetch_rows") if k in info},
     }
     if e2e:
         line["e2e"] = e2e
@@ -959,7 +959,7 @@ def run_config_sweep(dev, status, steps: int, warmup: int, peak: float):
                    "launches move more than 2x L2: calls back to back between one pair of CUDA events"),
             "dtype": w.dtype, "kernel": info["kernel"],
             "launch": {k: info[k] for k in ("grid", "block", "dyn_smem", "stages", "consumer_warps", "group_warps",
-                                            "registers") if k in info},
+                                            "prefetch_rows", "registers") if k in info},
         }
         if isinstance(w, I.Workload):
             entry.update(cos_dtype=w.cos_dtype, cos_layout=w.cos_layout, rope=w.rope_style,

@@ -436,6 +436,18 @@ qknr_status size_launch(const qknr_args* a, Plan* pl) {
   pl->kp.stages = stages;
   pl->kp.consumer_warps = warps;
   pl->kp.group_warps = gw;
+  // Before its dependency wait a CTA asks L2 for its second ring fill (rows
+  // ring .. 2 ring - 1 of its own), when it has at least four fills of rows.
+  // Under programmatic dependent launch that read overlaps the previous
+  // kernel's last rows: back to back, Wan 208.3 -> 207.5 us, the FLUX.2
+  // per-tensor pair 75.7 -> 71.2 us, Q and K in one launch 71.8 -> 69.2 us.
+  // Prefetching the first fill instead (which the producer's own copies
+  // request right after the wait) gained less on the pair (73.2 us), and
+  // shorter launches, whose inputs the previous kernel often leaves in L2,
+  // only lose (4096 x 24 x 128 back to back 14.1 -> 15.2 us).
+  const long long ring_rows = static_cast<long long>(stages) * n_groups;
+  const long long cta_rows = (a->tokens + grid - 1) / grid;
+  pl->kp.prefetch_rows = cta_rows >= 4 * ring_rows ? static_cast<int>(ring_rows) : 0;
   // split a group's warps between Q and K in proportion to their passes
   if (nq == 0 || nk == 0) {
     pl->kp.warps_q = nq ? gw : 0;
@@ -494,6 +506,7 @@ qknr_status qknr_query(const qknr_args* args, qknr_launch_info* info) {
   info->group_warps = pl.group_warps;
   info->registers = pl.regs;
   info->num_sms = pl.num_sms;
+  info->prefetch_rows = pl.kp.prefetch_rows;
   return QKNR_OK;
 }
 

@@ -56,7 +56,7 @@ constexpr int kOffStage0 = 2048;      // stage rings
 constexpr int kStageAlign = 128;
 
 constexpr unsigned kFlagTestStall = 1u;
-constexpr unsigned kFlagNoOverlap = 2u;     // host side only: plain launch
+constexpr unsigned kFlagNoOverlap = 2u;     // plain launch, no L2 prefetch before the wait
 
 struct KernelParams {
   const char* q;
@@ -90,6 +90,7 @@ struct KernelParams {
   unsigned stage_bytes;                              // stride between stages
   unsigned tx_bytes;                                 // bytes landing per stage
   unsigned smem_bytes;                               // dynamic shared memory of the launch
+  int prefetch_rows;                                 // rows of the second ring fill prefetched before the wait (0: none)
   // address spans of the buffers (checked builds test every access against them)
   MemSpan sp_q, sp_k, sp_v, sp_q_out, sp_k_out, sp_v_out, sp_cos, sp_sin, sp_gq, sp_gk;
 };
@@ -294,6 +295,36 @@ __device__ __forceinline__ void process_tensor(const unsigned char* seg, const u
 }
 
 // ---------------------------------------------------------------------------
+// L2 prefetch of the CTA's second ring fill: with n = p.prefetch_rows (the
+// rows of all its groups' rings), rows blockIdx.x + (n + i) * gridDim.x for
+// i < n, every segment the producer will copy for them.  The first fill is
+// left to the producer's own copies, which go out at once after the wait;
+// the prefetched rows are then in L2 when the stages free up.
+
+template <int D>
+__device__ __forceinline__ void prefetch_second_fill(const KernelParams& p) {
+  constexpr int ES = 2;
+  const uint32_t q_bytes = p.hq * D * ES, k_bytes = p.hk * D * ES, v_bytes = p.hv * D * ES;
+  const uint32_t c_bytes = static_cast<uint32_t>(p.cos_row_bytes);
+  const int n = p.prefetch_rows;
+  long long row = blockIdx.x + static_cast<long long>(n) * gridDim.x;
+  for (int i = 0; i < n && row < p.tokens; ++i, row += gridDim.x) {
+    if (p.qk_merged) {
+      bulk_prefetch_l2(p.q + row * p.q_stride, q_bytes + k_bytes);
+    } else {
+      if (q_bytes) bulk_prefetch_l2(p.q + row * p.q_stride, q_bytes);
+      if (k_bytes) bulk_prefetch_l2(p.k + row * p.k_stride, k_bytes);
+    }
+    if (v_bytes) bulk_prefetch_l2(p.v + row * p.v_stride, v_bytes);
+    if (c_bytes) {
+      const long long crow = row % p.cos_rows;
+      bulk_prefetch_l2(p.cos + crow * p.cos_row_bytes, c_bytes);
+      bulk_prefetch_l2(p.sin + crow * p.cos_row_bytes, c_bytes);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
 // the kernel
 
 template <typename T, typename CT, int D, bool RH, bool EXPANDED>
@@ -325,7 +356,13 @@ __global__ void __launch_bounds__(kMaxThreads, 1) qknr_fused_kernel(const __grid
   // Nothing above touches global memory, so under programmatic dependent
   // launch it overlaps the end of the kernel before this one in the stream.
   // Every global read and write comes after this wait: the inputs may be
-  // that kernel's outputs, and an in-place output may be its input.
+  // that kernel's outputs, and an in-place output may be its input.  Only
+  // L2 prefetches go before it (when the launch asks for them): they read
+  // nothing into the CTA, and a load after the wait that hits a prefetched
+  // line sees what the previous kernel wrote (its writes reach the same L2
+  // lines), so those rows' DRAM reads overlap that kernel's last rows.
+  if (!kChecked && p.prefetch_rows && warp == NW && lane == 0 && !(p.flags & kFlagNoOverlap))
+    prefetch_second_fill<D>(p);
   grid_dependency_wait();
 
   const unsigned long long limit = p.wait_limit_ns;

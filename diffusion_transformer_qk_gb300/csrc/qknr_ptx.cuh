@@ -137,6 +137,13 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       : "memory");
 }
 
+// Bring `bytes` at `src` into L2.  A hint: no data reaches the program, so
+// it cannot observe a stale value (L2 is where every SM's writes land).
+// 16-byte aligned address, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // Wait for phase `parity` of `bar` to complete, giving up at the deadline
 // or when another warp of the CTA has aborted.  Returns false on give-up.
 // The waiting thread sleeps in the barrier (20 us at a time) instead of

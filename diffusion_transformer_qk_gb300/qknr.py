@@ -35,7 +35,7 @@ OK, ERR_TIMEOUT = 0, 6
 FLAG_TEST_STALL = 0x1
 FLAG_NO_OVERLAP = 0x2
 FLAG_TEST_SHORT_OUT = 0x4
-ABI_VERSION = 2
+ABI_VERSION = 3
 
 EXPORTS = (
     "qknr_args_init", "qknr_forward", "qknr_query", "qknr_status_string",
@@ -80,7 +80,7 @@ class QknrLaunchInfo(ctypes.Structure):
         ("grid", c_int32), ("block", c_int32), ("dyn_smem", c_int32), ("stages", c_int32),
         ("ctas_per_sm", c_int32), ("consumer_warps", c_int32), ("group_warps", c_int32),
         ("stage_bytes", c_int32),
-        ("registers", c_int32), ("num_sms", c_int32), ("kernel", c_char * 96),
+        ("registers", c_int32), ("num_sms", c_int32), ("prefetch_rows", c_int32), ("kernel", c_char * 96),
     ]
 
     def as_dict(self):

@@ -47,7 +47,7 @@ extern "C" {
 struct CUstream_st;
 typedef struct CUstream_st *qknr_stream_t;
 
-#define QKNR_ABI_VERSION 2
+#define QKNR_ABI_VERSION 3
 
 typedef enum {
   QKNR_BF16 = 0, /* activations or cos/sin */
@@ -85,8 +85,8 @@ typedef enum {
 /* Launch-time flags (qknr_args.flags). */
 #define QKNR_FLAG_TEST_STALL 0x1u /* test only: issue no loads, so every wait runs out
                                      and the kernel reports QKNR_ERR_TIMEOUT */
-#define QKNR_FLAG_NO_OVERLAP 0x2u /* launch without programmatic dependent launch (see
-                                     qknr_forward) */
+#define QKNR_FLAG_NO_OVERLAP 0x2u /* launch without programmatic dependent launch and
+                                     without the early L2 prefetch (see qknr_forward) */
 #define QKNR_FLAG_TEST_SHORT_OUT 0x4u /* test only, checked build: the Q output span its
                                          kernel checks against ends one row early, so the
                                          last row's Q stores are refused and reported as
@@ -159,6 +159,8 @@ typedef struct qknr_launch_info {
   int32_t stage_bytes;        /* bytes staged per token row */
   int32_t registers;          /* registers per thread of the chosen kernel */
   int32_t num_sms;
+  int32_t prefetch_rows;      /* rows each CTA asks L2 for before its dependency wait (its second
+                                 ring fill; 0: none) */
   char kernel[96];            /* kernel variant name */
 } qknr_launch_info;
 
@@ -177,7 +179,10 @@ void qknr_args_init(qknr_args *a);
  * stream is a kernel, this one may launch while that kernel finishes, sets
  * up its shared memory, and then waits for it to complete before it reads
  * or writes any global memory, so stream order holds as with a plain
- * launch.  Each CTA signals dependents once all of its loads are issued, so
+ * launch.  Before that wait a CTA with many rows only asks L2 to prefetch
+ * some of the input rows it will load (Q, K, V segments and table rows
+ * inside the buffers given): a prefetch delivers no data to the kernel, and
+ * its loads after the wait see the previous kernel's writes.  Each CTA signals dependents once all of its loads are issued, so
  * a kernel launched after this one the same way (another qknr_forward, for
  * example the K launch after the Q launch) overlaps this one's last rows in
  * the same manner.  A kernel the caller launches after this one with that

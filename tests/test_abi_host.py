@@ -198,7 +198,7 @@ def test_adaln_args_init_defaults(lib):
 
 
 @pytest.mark.parametrize("mutate,expect", [
-    (lambda a: setattr(a, "abi_version", 3), 8),
+    (lambda a: setattr(a, "abi_version", Q.ABI_VERSION + 1), 8),
     (lambda a: setattr(a, "dtype", 2), 4),
     (lambda a: setattr(a, "mod_dtype", 1), 4),            # fp16 modulation for bf16 activations
     (lambda a: setattr(a, "hidden", 100), 4),             # not a multiple of 8

@@ -39,9 +39,22 @@ def _call(w, qkv, dev, flags):
                           dev["cos"], dev["sin"], rope_style=w.rope_style, eps=w.eps, flags=flags)
 
 
-def test_chain_of_dependent_calls_matches_plain_launches():
+def _prefetch_rows(w, qkv, dev):
+    a = Q.packed_args(qkv, w.n_heads_q, w.n_heads_k, w.n_heads_v, w.head_dim, dev["gq"], dev["gk"], dev["cos"],
+                      dev["sin"], rope_style=w.rope_style, eps=w.eps)
+    return Q.query(a)["prefetch_rows"]
+
+
+# 4096 rows: 27 per CTA, no L2 prefetch before the dependency wait; 9728
+# rows: 64 per CTA, each CTA prefetches its second ring fill before it
+PREFETCH_CASES = [(4096, False), (9728, True)]
+
+
+@pytest.mark.parametrize("tokens,prefetch", PREFETCH_CASES)
+def test_chain_of_dependent_calls_matches_plain_launches(tokens, prefetch):
     # every call reads the previous call's output in place
-    w, inp, dev = _dense()
+    w, inp, dev = _dense(tokens)
+    assert (_prefetch_rows(w, to_dev(inp["qkv"], w.dtype), dev) > 0) == prefetch
     outs = []
     for flags in (0, Q.FLAG_NO_OVERLAP):
         qkv = to_dev(inp["qkv"], w.dtype)
@@ -80,10 +93,14 @@ def test_in_place_call_waits_for_a_kernel_still_reading_its_input():
         np.testing.assert_array_equal(to_bits(seen), inp["qkv"])
 
 
-def test_call_sees_the_writes_of_the_kernel_before_it():
+@pytest.mark.parametrize("tokens,prefetch", PREFETCH_CASES)
+def test_call_sees_the_writes_of_the_kernel_before_it(tokens, prefetch):
     # a torch kernel writes the activation; the call right after it reads it
-    w, inp, dev = _dense()
+    # (with the prefetch, L2 may be asked for rows before that kernel wrote
+    # them: the loads after the wait must still see the new bits)
+    w, inp, dev = _dense(tokens)
     src = to_dev(inp["qkv"], w.dtype)
+    assert (_prefetch_rows(w, src, dev) > 0) == prefetch
     plain = to_dev(inp["qkv"], w.dtype)
     _call(w, plain, dev, Q.FLAG_NO_OVERLAP)
     for _ in range(3):
