@@ -444,10 +444,13 @@ qknr_status size_launch(const qknr_args* a, Plan* pl) {
   // Prefetching the first fill instead (which the producer's own copies
   // request right after the wait) gained less on the pair (73.2 us), and
   // shorter launches, whose inputs the previous kernel often leaves in L2,
-  // only lose (4096 x 24 x 128 back to back 14.1 -> 15.2 us).
+  // only lose (4096 x 24 x 128 back to back 14.1 -> 15.2 us).  A call that
+  // starts cold (after an L2 flush, nothing to overlap) loses about 1 us:
+  // Wan 8192 x 40 x 128 60.8 -> 62.0 us, the FLUX.2 Q launch 43.3 -> 43.8.
   const long long ring_rows = static_cast<long long>(stages) * n_groups;
   const long long cta_rows = (a->tokens + grid - 1) / grid;
-  pl->kp.prefetch_rows = cta_rows >= 4 * ring_rows ? static_cast<int>(ring_rows) : 0;
+  pl->kp.prefetch_rows =
+      !(a->flags & QKNR_FLAG_NO_PREFETCH) && cta_rows >= 4 * ring_rows ? static_cast<int>(ring_rows) : 0;
   // split a group's warps between Q and K in proportion to their passes
   if (nq == 0 || nk == 0) {
     pl->kp.warps_q = nq ? gw : 0;

@@ -35,6 +35,7 @@ OK, ERR_TIMEOUT = 0, 6
 FLAG_TEST_STALL = 0x1
 FLAG_NO_OVERLAP = 0x2
 FLAG_TEST_SHORT_OUT = 0x4
+FLAG_NO_PREFETCH = 0x8
 ABI_VERSION = 3
 
 EXPORTS = (

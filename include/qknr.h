@@ -87,6 +87,9 @@ typedef enum {
                                      and the kernel reports QKNR_ERR_TIMEOUT */
 #define QKNR_FLAG_NO_OVERLAP 0x2u /* launch without programmatic dependent launch and
                                      without the early L2 prefetch (see qknr_forward) */
+#define QKNR_FLAG_NO_PREFETCH 0x8u /* keep programmatic dependent launch but skip the L2
+                                      prefetch before the dependency wait (see
+                                      qknr_forward) */
 #define QKNR_FLAG_TEST_SHORT_OUT 0x4u /* test only, checked build: the Q output span its
                                          kernel checks against ends one row early, so the
                                          last row's Q stores are refused and reported as
@@ -182,7 +185,12 @@ void qknr_args_init(qknr_args *a);
  * launch.  Before that wait a CTA with many rows only asks L2 to prefetch
  * some of the input rows it will load (Q, K, V segments and table rows
  * inside the buffers given): a prefetch delivers no data to the kernel, and
- * its loads after the wait see the previous kernel's writes.  Each CTA signals dependents once all of its loads are issued, so
+ * its loads after the wait see the previous kernel's writes.  The prefetch
+ * pays when the call overlaps the end of the kernel before it (back-to-back
+ * calls, the K call after the Q call); a call that starts cold, after work
+ * that does not let it start early, loses about 1 us to it
+ * (QKNR_FLAG_NO_PREFETCH skips it; qknr_launch_info.prefetch_rows says
+ * whether a launch does it).  Each CTA signals dependents once all of its loads are issued, so
  * a kernel launched after this one the same way (another qknr_forward, for
  * example the K launch after the Q launch) overlaps this one's last rows in
  * the same manner.  A kernel the caller launches after this one with that

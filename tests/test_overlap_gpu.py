@@ -93,6 +93,20 @@ def test_in_place_call_waits_for_a_kernel_still_reading_its_input():
         np.testing.assert_array_equal(to_bits(seen), inp["qkv"])
 
 
+def test_no_prefetch_flag_gives_the_same_bits():
+    w, inp, dev = _dense(9728)
+    ref = to_dev(inp["qkv"], w.dtype)
+    a = Q.packed_args(ref, w.n_heads_q, w.n_heads_k, w.n_heads_v, w.head_dim, dev["gq"], dev["gk"], dev["cos"],
+                      dev["sin"], rope_style=w.rope_style, eps=w.eps, flags=Q.FLAG_NO_PREFETCH)
+    assert Q.query(a)["prefetch_rows"] == 0
+    got = to_dev(inp["qkv"], w.dtype)
+    for _ in range(3):
+        _call(w, ref, dev, 0)
+        _call(w, got, dev, Q.FLAG_NO_PREFETCH)
+    torch.cuda.synchronize()
+    assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
+
+
 @pytest.mark.parametrize("tokens,prefetch", PREFETCH_CASES)
 def test_call_sees_the_writes_of_the_kernel_before_it(tokens, prefetch):
     # a torch kernel writes the activation; the call right after it reads it
