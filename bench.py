@@ -968,6 +968,13 @@ def run_config_sweep(dev, status, steps: int, warmup: int, peak: float):
                                                         else "one launch per tensor (Q, then K)")))
         if L > 1:
             entry["us_per_launch"] = t * 1e6 / L
+        if flush is not None:
+            # the same calls back to back without the flush: inputs partly
+            # served from L2 across calls (the hot number; frac of the HBM
+            # peak then overstates DRAM work and is not reported)
+            t_hot = time_steps(lambda: run.step(stream), stream, steps, None, dev)
+            entry["hot"] = {"us_per_call": t_hot * 1e6, "achieved_gbs": step_bytes / t_hot / 1e9,
+                            "l2": "calls back to back, no flush"}
         if not over and not plain:
             # ncu DRAM bytes per launch, when the committed record is of these sources
             entry["traffic_per_launch"] = recorded_traffic(name)
