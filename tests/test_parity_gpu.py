@@ -365,3 +365,40 @@ def test_wan_expanded_distinct_heads_sampled(wan, style, cos_dtype):
     compare(bits[rows][:, : H * D], ref["q"], "bf16", "Q")
     compare(bits[rows][:, H * D:2 * H * D], ref["k"], "bf16", "K")
     np.testing.assert_array_equal(bits[:, 2 * H * D:], inp["qkv"][:, 2 * H * D:])
+
+
+@pytest.mark.parametrize("cos_dtype", ["fp32", "bf16"])
+def test_expanded_distinct_heads_separate_tensors_with_the_prefetch(cos_dtype):
+    # as above at 68 rows per CTA, where both launch forms prefetch their
+    # second ring fill into L2 before the dependency wait (Q/K/V segments
+    # and the per-head table rows of a batch-broadcast table)
+    H, D, S, B, dtype = 16, 128, 5120, 2, "bf16"
+    T = B * S
+    g = np.random.Generator(np.random.PCG64(23))
+    xs = {n: I.to_storage_bits(g.standard_normal((T, H * D)).astype(np.float32), dtype) for n in "qkv"}
+    gq = (1 + 0.1 * g.standard_normal(D)).astype(np.float32)
+    gk = (1 + 0.1 * g.standard_normal(D)).astype(np.float32)
+    ce, se = I.per_head_tables(S, H, D, "interleaved", cos_dtype, seed=24)
+    cos, sin = _dev_table(ce, cos_dtype), _dev_table(se, cos_dtype)
+    dgq, dgk = torch.from_numpy(gq).cuda(), torch.from_numpy(gk).cuda()
+    kw = dict(rope_style="interleaved", cos_layout="per_head_expanded")
+    refs = {n: O.forward_separate(xs[n], dtype, H, D, gam, 1e-6, ce, se, cos_dtype, "interleaved",
+                                  "per_head_expanded") for n, gam in (("q", gq), ("k", gk))}
+    q, k = to_dev(xs["q"], dtype), to_dev(xs["k"], dtype)
+    assert Q.query(Q.make_args(q=q, n_heads_q=H, head_dim=D, gamma_q=dgq, cos=cos, sin=sin, cos_rows=S,
+                               **kw))["prefetch_rows"] > 0
+    Q.qk_norm_rope_tensor(q, H, D, dgq, cos, sin, **kw)
+    Q.qk_norm_rope_tensor(k, H, D, dgk, cos, sin, **kw)
+    torch.cuda.synchronize()
+    compare(to_bits(q), refs["q"], dtype, "Q per tensor")
+    compare(to_bits(k), refs["k"], dtype, "K per tensor")
+    q2, k2, v2 = (to_dev(xs[n], dtype) for n in "qkv")
+    qo, ko, vo = torch.empty_like(q2), torch.empty_like(k2), torch.empty_like(v2)
+    a = Q.make_args(q=q2, k=k2, v=v2, q_out=qo, k_out=ko, v_out=vo, n_heads_q=H, n_heads_k=H, n_heads_v=H,
+                    head_dim=D, gamma_q=dgq, gamma_k=dgk, cos=cos, sin=sin, cos_rows=S, **kw)
+    assert Q.query(a)["prefetch_rows"] > 0
+    Q.qk_norm_rope_separate(q2, k2, H, D, dgq, dgk, cos, sin, v=v2, q_out=qo, k_out=ko, v_out=vo, **kw)
+    torch.cuda.synchronize()
+    compare(to_bits(qo), refs["q"], dtype, "Q single launch")
+    compare(to_bits(ko), refs["k"], dtype, "K single launch")
+    np.testing.assert_array_equal(to_bits(vo), xs["v"])
