@@ -1057,7 +1057,7 @@ def main(argv=None):
                    help="launch without programmatic dependent launch (plain stream order)")
     p.add_argument("--rope-style", choices=["interleaved", "rotate_half"], default=None,
                    help="QK workloads: pairing (default: the workload's own)")
-    p.add_argument("--gn-mode", choices=["auto", "fused", "two_pass"], default="auto",
+    p.add_argument("--gn-mode", choices=["auto", "fused", "two_pass", "cluster"], default="auto",
                    help="group-norm workloads: which path to time")
     p.add_argument("--copy-calibration", action="store_true",
                    help="print the device copy rate at the workloads' sizes (one JSON line each) and exit")

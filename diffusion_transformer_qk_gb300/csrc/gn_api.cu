@@ -6,9 +6,12 @@
 #include <atomic>
 #include <cstdio>
 #include <cstring>
+#include <map>
 #include <mutex>
+#include <tuple>
 
 #include "../../include/qknr_gn.h"
+#include "gn_cluster.cuh"
 #include "gn_kernel.cuh"
 #include "qknr_host.h"
 
@@ -42,8 +45,44 @@ struct GnPlan {
   size_t f_records = 0;         // bytes of the [spans][P + 1] 16-byte records
   size_t ws_fused = 0;
   bool want_fused = false;      // AUTO without two-pass tuning, or FUSED
+  // cluster path (sizes that do not depend on the device)
+  bool cluster_shape = false;   // a group fits the shared memory of a cluster (200 KB parts)
+  bool cluster_auto = false;    // ... with parts of at most 32 KB
+  bool want_cluster = false;    // AUTO without two-pass tuning on such a shape, or CLUSTER
   size_t workspace = 0;         // what qknr_gn_workspace_bytes reports
 };
+
+// The cluster path's split of a group of L elements over c CTAs (a power
+// of two up to kGncMaxCluster): parts of at most 32 KB where a cluster can
+// hold the group so (the automatic choice takes the cluster path only
+// then), else, when asked for, of at most 200 KB; then, while the grid
+// would have fewer than two CTAs per SM and parts stay at 4 KB or more,
+// twice as many CTAs per group.  Sweeps on GB300 (flushed calls): groups of
+// 32 KB to 512 KB ran 15-25 % faster than on the fused path with parts of
+// 8-32 KB; groups of 1 MB tied it and of 2 MB took 60 % longer (few
+// clusters of 16 fit at once).
+constexpr long long kGncSmallPartBytes = 32 * 1024;
+constexpr long long kGncMaxPartBytes = 200 * 1024;
+constexpr long long kGncMinPartBytes = 4 * 1024;
+
+long long cluster_part(long long L, int c) { return ((L + c - 1) / c + 7) / 8 * 8; }
+
+// smallest c whose parts fit `cap` bytes, or 0
+int cluster_fit(long long L, long long cap) {
+  for (int c = 1; c <= qknr::kGncMaxCluster; c *= 2)
+    if (cluster_part(L, c) * 2 <= cap) return c;
+  return 0;
+}
+
+void cluster_split(long long L, long long spans, int num_sms, bool allow_large, int* cluster, long long* part_len) {
+  int c = cluster_fit(L, kGncSmallPartBytes);
+  if (c == 0 && allow_large) c = cluster_fit(L, kGncMaxPartBytes);
+  while (c > 0 && c < qknr::kGncMaxCluster && spans * c < 2ll * num_sms &&
+         cluster_part(L, 2 * c) * 2 >= kGncMinPartBytes)
+    c *= 2;
+  *cluster = c;
+  *part_len = c > 0 ? cluster_part(L, c) : 0;
+}
 
 qknr_status plan(const qknr_gn_args* a, GnPlan* pl) {
   if (!a) return fail(QKNR_ERR_NULL, "args is NULL");
@@ -51,7 +90,8 @@ qknr_status plan(const qknr_gn_args* a, GnPlan* pl) {
     return fail(QKNR_ERR_ABI, "abi_version %u, library expects %d", a->abi_version, QKNR_ABI_VERSION);
   if (a->dtype != QKNR_BF16 && a->dtype != QKNR_FP16)
     return fail(QKNR_ERR_UNSUPPORTED, "activation dtype must be BF16 or FP16");
-  if (a->mode != QKNR_GN_AUTO && a->mode != QKNR_GN_FUSED && a->mode != QKNR_GN_TWO_PASS)
+  if (a->mode != QKNR_GN_AUTO && a->mode != QKNR_GN_FUSED && a->mode != QKNR_GN_TWO_PASS &&
+      a->mode != QKNR_GN_CLUSTER)
     return fail(QKNR_ERR_UNSUPPORTED, "unknown mode %d", a->mode);
   if (a->n <= 0 || a->c <= 0 || a->h <= 0 || a->w <= 0 || a->groups <= 0)
     return fail(QKNR_ERR_SHAPE, "n, c, h, w and groups must be positive");
@@ -113,8 +153,22 @@ qknr_status plan(const qknr_gn_args* a, GnPlan* pl) {
   pl->f_records = static_cast<size_t>(pl->spans * (fP + 1) * 2 * sizeof(double));
   pl->ws_fused = pl->f_records + 16;   // + the abort word
 
+  // ---- cluster path (the split itself depends on the device's SM count)
+  const bool grid_ok = pl->spans <= 0x7fffffffll / qknr::kGncMaxCluster;
+  pl->cluster_shape = grid_ok && cluster_fit(L, kGncMaxPartBytes) > 0;
+  pl->cluster_auto = grid_ok && cluster_fit(L, kGncSmallPartBytes) > 0;
+
   const bool tuned = a->piece_elems != 0 || a->l2_batch_bytes != 0;
+  pl->want_cluster = a->mode == QKNR_GN_CLUSTER || (a->mode == QKNR_GN_AUTO && !tuned && pl->cluster_auto);
   pl->want_fused = a->mode == QKNR_GN_FUSED || (a->mode == QKNR_GN_AUTO && !tuned);
+  if (a->mode == QKNR_GN_CLUSTER) {
+    if (!pl->cluster_shape)
+      return fail(QKNR_ERR_UNSUPPORTED, "a group of %lld elements does not fit a cluster of %d CTAs", L,
+                  qknr::kGncMaxCluster);
+    pl->want_fused = false;
+    pl->workspace = 0;                   // the cluster path keeps its statistics on chip
+    return QKNR_OK;
+  }
   if (a->mode == QKNR_GN_FUSED) {
     if (!pl->fused_shape) return fail(QKNR_ERR_UNSUPPORTED, "2^31 or more pieces in all for the fused path");
     pl->workspace = pl->ws_fused;
@@ -184,6 +238,103 @@ qknr_status fused_launch(const qknr_gn_args* a, const GnPlan& pl, FusedLaunch* f
   return QKNR_OK;
 }
 
+// The cluster launch on the current device, or why there is none.
+struct ClusterLaunch {
+  bool ok = false;
+  const void* fn = nullptr;
+  int cluster = 0;            // CTAs per cluster (per group of a sample)
+  long long part_len = 0;     // elements per CTA
+  int grid = 0;
+  int smem = 0;
+  int regs = 0;
+  int num_sms = 0;
+  int max_clusters = 0;       // clusters of this launch resident at once
+  char why[160] = "";
+};
+
+qknr_status cluster_launch(const qknr_gn_args* a, const GnPlan& pl, ClusterLaunch* cl) {
+  cl->fn = a->dtype == QKNR_BF16 ? reinterpret_cast<const void*>(&qknr::gn_cluster_kernel<__nv_bfloat16>)
+                                 : reinterpret_cast<const void*>(&qknr::gn_cluster_kernel<__half>);
+  if (!pl.cluster_shape) {
+    snprintf(cl->why, sizeof(cl->why), "a group does not fit a cluster");
+    return QKNR_OK;
+  }
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return qknr_host::cuda_fail(e, "cudaGetDevice");
+  qknr_host::DeviceInfo di;
+  qknr_status st = qknr_host::device_info(dev, &di);
+  if (st != QKNR_OK) return st;
+  cl->num_sms = di.num_sms;
+  int cluster_launch = 0;
+  e = cudaDeviceGetAttribute(&cluster_launch, cudaDevAttrClusterLaunch, dev);
+  if (e != cudaSuccess) return qknr_host::cuda_fail(e, "cudaDeviceGetAttribute(ClusterLaunch)");
+  if (!cluster_launch) {
+    snprintf(cl->why, sizeof(cl->why), "the device has no cluster launch");
+    return QKNR_OK;
+  }
+  cluster_split(pl.L, pl.spans, di.num_sms, a->mode == QKNR_GN_CLUSTER, &cl->cluster, &cl->part_len);
+  cl->smem = static_cast<int>(qknr::kGncOffData + cl->part_len * 2);
+  if (di.smem_optin < cl->smem) {
+    snprintf(cl->why, sizeof(cl->why), "%d bytes of shared memory per block, %d needed", di.smem_optin, cl->smem);
+    return QKNR_OK;
+  }
+  st = qknr_host::configure_kernel(cl->fn, dev, di, &cl->regs);
+  if (st != QKNR_OK) return st;
+  // clusters of this size and shared memory that fit at once, asked once
+  // per kernel, device, size and shared memory
+  static std::mutex mu;
+  static std::map<std::tuple<const void*, int, int, int>, int> resident;
+  const auto key = std::make_tuple(cl->fn, dev, cl->cluster, cl->smem);
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    auto it = resident.find(key);
+    if (it != resident.end()) {
+      cl->max_clusters = it->second;
+      if (it->second < 1) {
+        snprintf(cl->why, sizeof(cl->why), "no cluster of %d CTAs with %d bytes each fits", cl->cluster, cl->smem);
+        return QKNR_OK;
+      }
+      cl->grid = static_cast<int>(pl.spans * cl->cluster);
+      cl->ok = true;
+      return QKNR_OK;
+    }
+  }
+  if (cl->cluster > 8) {
+    e = cudaFuncSetAttribute(cl->fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return qknr_host::cuda_fail(e, "cudaFuncSetAttribute(NonPortableClusterSizeAllowed)");
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(cl->cluster);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(pl.spans * cl->cluster));
+  cfg.blockDim = dim3(qknr::kGncThreads);
+  cfg.dynamicSmemBytes = static_cast<size_t>(cl->smem);
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  e = cudaOccupancyMaxActiveClusters(&n, cl->fn, &cfg);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();                  // a configuration the device cannot place: not sticky
+    n = 0;
+  }
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    resident[key] = n;
+  }
+  if (n < 1) {
+    snprintf(cl->why, sizeof(cl->why), "no cluster of %d CTAs with %d bytes each fits", cl->cluster, cl->smem);
+    return QKNR_OK;
+  }
+  cl->max_clusters = n;
+  cl->grid = static_cast<int>(pl.spans * cl->cluster);
+  cl->ok = true;
+  return QKNR_OK;
+}
+
 // Resolve the path: *use_fused, with fl filled when it is true.
 qknr_status choose(const qknr_gn_args* a, const GnPlan& pl, FusedLaunch* fl, bool* use_fused) {
   *use_fused = false;
@@ -201,7 +352,8 @@ qknr_status choose(const qknr_gn_args* a, const GnPlan& pl, FusedLaunch* fl, boo
 
 qknr_status check_buffers(const qknr_gn_args* a, const GnPlan& pl) {
   if (!a->x || !a->gamma || !a->beta) return fail(QKNR_ERR_NULL, "x, gamma and beta are required");
-  if (!a->workspace) return fail(QKNR_ERR_NULL, "workspace is required (qknr_gn_workspace_bytes)");
+  if (!a->workspace && pl.workspace > 0)
+    return fail(QKNR_ERR_NULL, "workspace is required (qknr_gn_workspace_bytes)");
   if (a->workspace_bytes < pl.workspace)
     return fail(QKNR_ERR_SHAPE, "workspace of %zu bytes, %zu needed", a->workspace_bytes, pl.workspace);
   const void* out = a->out ? a->out : a->x;
@@ -217,7 +369,8 @@ qknr_status check_buffers(const qknr_gn_args* a, const GnPlan& pl) {
   if (out != a->x && (qknr_host::overlaps(so, sx) || qknr_host::overlaps(so, sg) || qknr_host::overlaps(so, sb) ||
                       qknr_host::overlaps(so, sw)))
     return fail(QKNR_ERR_OVERLAP, "out overlaps an input without being in place");
-  if (qknr_host::overlaps(sw, sx) || qknr_host::overlaps(sw, sg) || qknr_host::overlaps(sw, sb))
+  if (pl.workspace > 0 &&
+      (qknr_host::overlaps(sw, sx) || qknr_host::overlaps(sw, sg) || qknr_host::overlaps(sw, sb)))
     return fail(QKNR_ERR_OVERLAP, "workspace overlaps an input");
   return QKNR_OK;
 }
@@ -316,6 +469,46 @@ qknr_status launch_fused(const qknr_gn_args* a, const GnPlan& pl, const FusedLau
   return QKNR_OK;
 }
 
+qknr_status launch_cluster(const qknr_gn_args* a, const GnPlan& pl, const ClusterLaunch& cl, cudaStream_t s) {
+  qknr::GnClusterParams cp;
+  memset(&cp, 0, sizeof(cp));
+  cp.x = static_cast<const char*>(a->x);
+  cp.out = static_cast<char*>(a->out ? a->out : const_cast<void*>(a->x));
+  cp.gamma = a->gamma;
+  cp.beta = a->beta;
+  cp.status = a->dev_status;
+  cp.span_len = pl.L;
+  cp.hw = (long long)a->h * a->w;
+  cp.part_len = cl.part_len;
+  cp.groups = a->groups;
+  cp.group_channels = a->c / a->groups;
+  cp.flags = a->flags & qknr::kGnfFlagStallLoads;
+  cp.smem_bytes = static_cast<unsigned>(cl.smem);
+  cp.wait_limit_ns = a->wait_limit_ns ? a->wait_limit_ns : kDefaultWaitNs;
+  cp.eps = a->eps;
+  const GnSpans sp = spans_of(a, pl);
+  cp.sp_x = sp.x;
+  cp.sp_out = sp.out;
+  cp.sp_gamma = sp.gamma;
+  cp.sp_beta = sp.beta;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(cl.cluster);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(static_cast<unsigned>(cl.grid));
+  cfg.blockDim = dim3(qknr::kGncThreads);
+  cfg.dynamicSmemBytes = static_cast<size_t>(cl.smem);
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  void* kargs[] = {&cp};
+  const cudaError_t e = cudaLaunchKernelExC(&cfg, cl.fn, kargs);
+  if (e != cudaSuccess) return qknr_host::cuda_fail(e, "cudaLaunchKernelExC(cluster group norm)");
+  return QKNR_OK;
+}
+
 qknr_status launch_two_pass(const qknr_gn_args* a, const GnPlan& pl, cudaStream_t s) {
   const bool bf16 = a->dtype == QKNR_BF16;
   const void* stats = bf16 ? reinterpret_cast<const void*>(&qknr::gn_stats_kernel<__nv_bfloat16>)
@@ -370,11 +563,18 @@ qknr_status qknr_gn_silu_forward(const qknr_gn_args* args, qknr_stream_t stream)
   if (st != QKNR_OK) return st;
   st = check_buffers(args, pl);
   if (st != QKNR_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (pl.want_cluster) {
+    ClusterLaunch cl;
+    st = cluster_launch(args, pl, &cl);
+    if (st != QKNR_OK) return st;
+    if (cl.ok) return launch_cluster(args, pl, cl, s);
+    if (args->mode == QKNR_GN_CLUSTER) return fail(QKNR_ERR_UNSUPPORTED, "cluster group norm: %s", cl.why);
+  }
   FusedLaunch fl;
   bool fused = false;
   st = choose(args, pl, &fl, &fused);
   if (st != QKNR_OK) return st;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (fused) {
     bool too_large = false;
     st = launch_fused(args, pl, fl, s, &too_large);
@@ -389,11 +589,31 @@ qknr_status qknr_gn_query(const qknr_gn_args* args, qknr_launch_info* info) {
   GnPlan pl;
   qknr_status st = plan(args, &pl);
   if (st != QKNR_OK) return st;
+  const char* dt = args->dtype == QKNR_BF16 ? "bf16" : "fp16";
+  if (pl.want_cluster) {
+    ClusterLaunch cl;
+    st = cluster_launch(args, pl, &cl);
+    if (st != QKNR_OK) return st;
+    if (cl.ok) {
+      info->grid = cl.grid;
+      info->block = qknr::kGncThreads;
+      info->dyn_smem = cl.smem;
+      info->stages = 1;
+      info->ctas_per_sm = 0;
+      info->consumer_warps = qknr::kGncThreads / 32;
+      info->stage_bytes = static_cast<int32_t>(cl.part_len * 2);
+      info->registers = cl.regs;
+      info->num_sms = cl.num_sms;
+      snprintf(info->kernel, sizeof(info->kernel), "gn_cluster<%s>, clusters of %d CTAs, %lld elements each, %d resident",
+               dt, cl.cluster, cl.part_len, cl.max_clusters);
+      return QKNR_OK;
+    }
+    if (args->mode == QKNR_GN_CLUSTER) return fail(QKNR_ERR_UNSUPPORTED, "cluster group norm: %s", cl.why);
+  }
   FusedLaunch fl;
   bool fused = false;
   st = choose(args, pl, &fl, &fused);
   if (st != QKNR_OK) return st;
-  const char* dt = args->dtype == QKNR_BF16 ? "bf16" : "fp16";
   if (fused) {
     info->grid = fl.grid;
     info->block = qknr::kGnfThreads;

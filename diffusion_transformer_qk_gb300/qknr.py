@@ -46,7 +46,7 @@ EXPORTS = (
     "qknr_gn_silu_forward_noalloc", "qknr_gn_query",
     "qknr_host_plan_init", "qknr_host_buffer_bytes", "qknr_forward_host", "qknr_sizeof_host_plan",
 )
-GN_MODE = {"auto": 0, "fused": 1, "two_pass": 2}
+GN_MODE = {"auto": 0, "fused": 1, "two_pass": 2, "cluster": 3}
 GN_FLAG_TEST_NO_RECORDS = 0x2
 GN_NOALLOC_SCRATCH_BYTES = 1 << 20
 HOST_MAX_BUFFERS = 4

@@ -61,7 +61,8 @@ extern "C" {
 typedef enum {
   QKNR_GN_AUTO = 0,
   QKNR_GN_FUSED = 1,          /* QKNR_ERR_UNSUPPORTED where the fused path cannot run */
-  QKNR_GN_TWO_PASS = 2
+  QKNR_GN_TWO_PASS = 2,
+  QKNR_GN_CLUSTER = 3         /* QKNR_ERR_UNSUPPORTED where the cluster path cannot run */
 } qknr_gn_mode;
 
 /* test only: the fused path publishes no piece statistics, so every wait

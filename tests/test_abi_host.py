@@ -270,6 +270,19 @@ def test_gn_workspace_bytes(lib):
     assert gn_ws(lib, a) == 32 * (3 + 1) * 16 + 16
 
 
+def test_gn_cluster_mode_needs_no_workspace_and_takes_groups_up_to_a_cluster(lib):
+    a = valid_gn()
+    a.mode = Q.GN_MODE["cluster"]
+    assert gn_ws(lib, a) == 0
+    # 16 CTAs of at most 200 KB each: a group of 1,638,400 elements fits,
+    # one of 1,703,936 does not (checked before any CUDA call)
+    a.c, a.groups, a.h, a.w = 25, 1, 256, 256
+    assert gn_ws(lib, a) == 0
+    a.c = 26
+    n = ctypes.c_size_t(0)
+    assert lib.qknr_gn_workspace_bytes(ctypes.byref(a), ctypes.byref(n)) == 4
+
+
 def test_gn_workspace_does_not_depend_on_the_device(lib):
     # no CUDA call is made: the size comes from the arguments alone
     a = valid_gn()
@@ -294,7 +307,7 @@ def test_gn_workspace_does_not_depend_on_the_device(lib):
     (lambda a: setattr(a, "gamma", FAKE + (1 << 30) + 2), 3),
     (lambda a: setattr(a, "out", FAKE + 1024), 7),          # out inside x
     (lambda a: setattr(a, "workspace", FAKE + 4096), 7),    # workspace inside x
-    (lambda a: setattr(a, "mode", 3), 4),
+    (lambda a: setattr(a, "mode", 4), 4),
     (lambda a: setattr(a, "dev_status", FAKE + 3 * (1 << 30) + 2), 3),
 ])
 def test_gn_validation_rejects(lib, mutate, expect):

@@ -98,3 +98,32 @@ def test_fused_group_norm_replays_in_a_cuda_graph():
         torch.cuda.synchronize()
         assert int(status.item()) == 0
         assert torch.equal(x.view(torch.int16), ref.view(torch.int16))
+
+
+def test_cluster_group_norm_replays_in_a_cuda_graph():
+    # clusters of 4 CTAs per group; a graph keeps the launch's cluster shape
+    w = I.GroupNormWorkload("gc", 3, 256, 128, 64, groups=32, scale=1.5, offset=0.2, seed=25)
+    base = I.make_gn_inputs(w)
+    gamma, beta = torch.from_numpy(base["gamma"]).cuda(), torch.from_numpy(base["beta"]).cuda()
+    refs = []
+    for sd in (26, 27):
+        bits = I.make_gn_inputs(w.with_(seed=sd))["x"]
+        r = to_dev(bits, "bf16")
+        Q.group_norm_silu(r, w.groups, gamma, beta, eps=w.eps, mode="cluster")
+        refs.append((bits, r))
+    x = to_dev(base["x"], "bf16")
+    a = Q.gn_args(x, w.groups, gamma, beta, eps=w.eps, mode="cluster")
+    assert Q.gn_query(a)["kernel"].startswith("gn_cluster<bf16>, clusters of 4 CTAs")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            Q.group_norm_silu(x, w.groups, gamma, beta, eps=w.eps, mode="cluster", dev_status=status)
+    for bits, ref in refs:
+        x.copy_(to_dev(bits, "bf16"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        assert torch.equal(x.view(torch.int16), ref.view(torch.int16))

@@ -113,11 +113,19 @@ def query(w, **kw):
     return Q.gn_query(Q.gn_args(x, w.groups, g, g, **kw))
 
 
+# groups of up to 512 KB (16 parts of at most 32 KB) take the cluster path,
+# larger ones the fused one
+VAE_PATHS = {"gn_vae_1x128x1024x1024": "gn_fused", "gn_vae_1x256x512x512": "gn_fused",
+             "gn_vae_1x512x256x256": "gn_fused", "gn_vae_1x512x128x128": "gn_cluster"}
+
+
 @pytest.mark.parametrize("name", list(I.GN_WORKLOADS))
-def test_vae_shapes_take_the_fused_path(name):
+def test_vae_shapes_take_the_expected_path(name):
     info = query(I.GN_WORKLOADS[name])
-    assert info["kernel"].startswith("gn_fused<bf16>"), info
-    assert info["grid"] == info["num_sms"] and info["block"] == 800 and info["stages"] == 9
+    assert info["kernel"].startswith(VAE_PATHS[name] + "<bf16>"), info
+    fused = query(I.GN_WORKLOADS[name], mode="fused")
+    assert fused["kernel"].startswith("gn_fused<bf16>"), fused
+    assert fused["grid"] == fused["num_sms"] and fused["block"] == 800 and fused["stages"] == 9
     two = query(I.GN_WORKLOADS[name], mode="two_pass")
     assert two["kernel"].startswith("gn_stats+gn_apply"), two
 
@@ -141,7 +149,7 @@ def test_fused_equals_two_pass_with_the_same_pieces(shape, groups, dtype):
 
 @pytest.mark.parametrize("dtype,spread,mean", [("fp16", 0.05, -30.0), ("fp16", 0.01, -8.0), ("bf16", 0.05, -30.0),
                                                ("bf16", 0.02, 60.0)])
-@pytest.mark.parametrize("mode", ["fused", "two_pass"])
+@pytest.mark.parametrize("mode", ["fused", "two_pass", "cluster"])
 def test_large_mean_small_spread(dtype, spread, mean, mode):
     # groups whose mean is hundreds of times their spread: the small
     # differences must not be lost to the rounding of the mean (every output
@@ -156,7 +164,7 @@ def test_large_mean_small_spread(dtype, spread, mean, mode):
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp16"])
 @pytest.mark.parametrize("spike", [300.0, 3000.0])
-@pytest.mark.parametrize("mode", ["fused", "two_pass"])
+@pytest.mark.parametrize("mode", ["fused", "two_pass", "cluster"])
 def test_outlier_at_the_first_element(dtype, spike, mode):
     # the group's first element is an outlier that carries most of the
     # variance: neither the statistics nor the shift may let it cancel the
@@ -171,7 +179,7 @@ def test_outlier_at_the_first_element(dtype, spike, mode):
     compare_ulps(to_bits(res), ref, dtype, 1, f"spike {spike}")
 
 
-@pytest.mark.parametrize("mode,piece", [("fused", 0), ("two_pass", 0), ("two_pass", 12288)])
+@pytest.mark.parametrize("mode,piece", [("fused", 0), ("two_pass", 0), ("two_pass", 12288), ("cluster", 0)])
 def test_spikes_scattered_through_large_groups(mode, piece):
     # fp16 groups of 110k values with 30-sigma spikes scattered through them
     # and a 300-sigma one first, gamma near -2 and beta near -3 (outputs
@@ -265,3 +273,98 @@ def test_vae_shapes_fused_equals_two_pass(name):
     b = gn_call(to_dev(inp["x"], w.dtype), w, inp, mode="two_pass", piece_elems=12288)
     torch.cuda.synchronize()
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+# ---------------------------------------------------------------------------
+# the cluster path: one cluster of CTAs per group (of one sample), each CTA
+# holding an equal part in shared memory, the parts' statistics merged over
+# distributed shared memory
+
+# (shape, groups, CTAs per cluster on 152 SMs): the fewest CTAs whose parts
+# take at most 32 KB (200 KB when no cluster of 16 holds the group so), then
+# twice as many while the grid has fewer than 2 CTAs per SM and parts stay at
+# 4 KB or more; ragged last parts at 40040 and 1040040 elements per group
+CLUSTER_CASES = [((2, 64, 16, 16), 32, 1), ((3, 12, 4, 6), 3, 1), ((6, 256, 64, 64), 32, 2),
+                 ((3, 256, 128, 64), 32, 4), ((4, 128, 64, 64), 32, 4), ((2, 256, 128, 128), 32, 8),
+                 ((20, 10, 88, 91), 2, 8), ((1, 512, 128, 128), 32, 16), ((1, 10, 88, 91), 2, 16),
+                 ((1, 10, 24, 8667), 2, 16), ((1, 512, 256, 256), 32, 16)]
+
+
+@pytest.mark.parametrize("shape,groups,cluster", CLUSTER_CASES)
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_cluster_path_matches_the_oracle(shape, groups, cluster, dtype):
+    w = I.GroupNormWorkload("c", *shape, groups=groups, dtype=dtype, scale=1.5, offset=0.3, seed=sum(shape) + 5)
+    info = query(w, mode="cluster")
+    assert info["kernel"].startswith(f"gn_cluster<{dtype}>, clusters of {cluster} CTAs"), info
+    inp = I.make_gn_inputs(w)
+    res, src = run(w, inp, out=True, mode="cluster")
+    np.testing.assert_array_equal(to_bits(src), inp["x"])              # out of place: x unchanged
+    got = to_bits(res)
+    if inp["x"].size <= 1 << 22:
+        ref = G.group_norm_silu(inp["x"], dtype, groups, inp["gamma"], inp["beta"], w.eps)
+        compare(got, ref, dtype, f"cluster {shape}")
+    else:
+        g = np.random.Generator(np.random.PCG64(17))
+        idx = tuple(g.integers(0, s_, 6000) for s_ in shape)
+        ref = G.group_norm_silu_at(inp["x"], dtype, groups, inp["gamma"], inp["beta"], w.eps, idx)
+        compare(got[idx], ref, dtype, f"cluster {shape}")
+    # in place gives the same bits
+    ip, _ = run(w, inp, mode="cluster")
+    assert torch.equal(ip.view(torch.int16), res.view(torch.int16))
+
+
+def test_cluster_path_with_one_cta_equals_the_one_piece_paths():
+    # a group held by one CTA is one part: the same sums in the same order as
+    # one piece of the fused and two-pass paths
+    w = I.GroupNormWorkload("one", 2, 64, 32, 32, groups=32, scale=2.0, offset=-1.0, seed=46)
+    inp = I.make_gn_inputs(w)
+    assert query(w, mode="cluster")["kernel"].startswith("gn_cluster<bf16>, clusters of 1 CTAs")
+    a = gn_call(to_dev(inp["x"], "bf16"), w, inp, mode="cluster")
+    b = gn_call(to_dev(inp["x"], "bf16"), w, inp, mode="fused")
+    c = gn_call(to_dev(inp["x"], "bf16"), w, inp, mode="two_pass")
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    assert torch.equal(a.view(torch.int16), c.view(torch.int16))
+
+
+def test_cluster_path_needs_no_workspace():
+    w = I.GroupNormWorkload("nw", 1, 64, 64, 64, groups=32, seed=47)
+    inp = I.make_gn_inputs(w)
+    x = to_dev(inp["x"], "bf16")
+    g, b = torch.from_numpy(inp["gamma"]).cuda(), torch.from_numpy(inp["beta"]).cuda()
+    a = Q.gn_args(x, w.groups, g, b, eps=w.eps, mode="cluster", dev_status=Q.status_buffer())
+    assert Q.gn_workspace_bytes(a) == 0
+    Q.gn_launch(a)                                      # a.workspace is NULL
+    torch.cuda.synchronize()
+    ref = G.group_norm_silu(inp["x"], "bf16", w.groups, inp["gamma"], inp["beta"], w.eps)
+    compare(to_bits(x), ref, "bf16", "no workspace")
+
+
+def test_cluster_path_rejects_groups_too_large():
+    w = I.GN_WORKLOADS["gn_vae_1x256x512x512"]             # 4 MB groups: 256 KB parts at 16 CTAs
+    with pytest.raises(Q.QknrError) as e:
+        query(w, mode="cluster")
+    assert e.value.status == 4
+
+
+@pytest.mark.parametrize("cluster_shape", [(1, 64, 64, 64), (1, 512, 128, 128), (1, 10, 24, 8667)])
+def test_cluster_bounded_wait_reports_timeout(cluster_shape):
+    # no copy is issued: every CTA's wait runs out, every CTA of every
+    # cluster still passes both cluster barriers, nothing is written
+    groups = 2 if cluster_shape[1] == 10 else 32
+    w = I.GroupNormWorkload("t", *cluster_shape, groups=groups, seed=48)
+    inp = I.make_gn_inputs(w)
+    x = to_dev(inp["x"], "bf16")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gn_call(x, w, inp, mode="cluster", dev_status=status, flags=Q.FLAG_TEST_STALL, wait_limit_ns=2_000_000)
+    torch.cuda.synchronize()
+    assert int(status.item()) == Q.ERR_TIMEOUT
+    np.testing.assert_array_equal(to_bits(x), inp["x"])
+    status.zero_()
+    res = gn_call(x, w, inp, mode="cluster", dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    g = np.random.Generator(np.random.PCG64(18))
+    idx = tuple(g.integers(0, s_, 3000) for s_ in cluster_shape)
+    ref = G.group_norm_silu_at(inp["x"], "bf16", groups, inp["gamma"], inp["beta"], w.eps, idx)
+    compare(to_bits(res)[idx], ref, "bf16", "after timeout")

@@ -2,7 +2,8 @@
 oracle: batch, groups, channels per group (past the 1280 channels that the
 fused kernel stages in shared memory), ragged H*W, dtypes, value scale and
 offset, in place / out of place; the fused path is also checked bit for bit
-against the two-pass path with pieces of the same size."""
+against the two-pass path with pieces of the same size, and groups that fit a
+cluster also go through the cluster path (the automatic choice for them)."""
 import numpy as np
 import pytest
 import torch
@@ -15,6 +16,21 @@ from tests.gpu_util import compare, to_bits, to_dev
 pytestmark = pytest.mark.gpu
 
 FUSED_PIECE = 12288          # elements per piece of the fused path
+
+
+def cluster_part_bytes(L, c=16):
+    return ((L + c - 1) // c + 7) // 8 * 8 * 2
+
+
+def cluster_auto(L):
+    """Whether the automatic choice takes the cluster path for groups of L
+    elements: parts of at most 32 KB over at most 16 CTAs."""
+    return cluster_part_bytes(L) <= 32 * 1024
+
+
+def cluster_any(L):
+    """Whether the cluster path can run: parts of at most 200 KB."""
+    return cluster_part_bytes(L) <= 200 * 1024
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -54,8 +70,9 @@ def test_random_group_norm(seed):
     inp = I.make_gn_inputs(w)
     x = to_dev(inp["x"], w.dtype)
     out = torch.empty_like(x) if out_of_place else None
+    L = (w.c // w.groups) * w.h * w.w
     info = Q.gn_query(Q.gn_args(x, w.groups, torch.ones(w.c, device="cuda"), torch.ones(w.c, device="cuda")))
-    assert info["kernel"].startswith("gn_fused"), info
+    assert info["kernel"].startswith("gn_cluster" if cluster_auto(L) else "gn_fused"), info
     res = call(x, w, inp, out=out, mode="fused")
     two = call(to_dev(inp["x"], w.dtype), w, inp, mode="two_pass", piece_elems=FUSED_PIECE)
     torch.cuda.synchronize()
@@ -64,3 +81,13 @@ def test_random_group_norm(seed):
         np.testing.assert_array_equal(to_bits(x), inp["x"])
     ref = G.group_norm_silu(inp["x"], w.dtype, w.groups, inp["gamma"], inp["beta"], w.eps)
     compare(to_bits(res), ref, w.dtype, w.name)
+    if cluster_any(L):
+        xc = to_dev(inp["x"], w.dtype)
+        cl = call(xc, w, inp, out=torch.empty_like(xc) if out_of_place else None, mode="cluster")
+        auto = call(to_dev(inp["x"], w.dtype), w, inp)
+        torch.cuda.synchronize()
+        if cluster_auto(L):
+            assert torch.equal(cl.view(torch.int16), auto.view(torch.int16)), w
+        if out_of_place:
+            np.testing.assert_array_equal(to_bits(xc), inp["x"])
+        compare(to_bits(cl), ref, w.dtype, w.name + " cluster")
