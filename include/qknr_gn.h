@@ -37,12 +37,24 @@
  *   two-pass (QKNR_GN_TWO_PASS): a statistics kernel and a normalise + SiLU
  *     kernel, once for all groups or once per batch of groups; x is read
  *     twice.  No CTA waits for another.
+ *   cluster (QKNR_GN_CLUSTER): one thread-block cluster (up to 16 CTAs) per
+ *     group of a sample; each CTA holds an equal part of the group in
+ *     shared memory, the parts' statistics are merged over distributed
+ *     shared memory in one fixed order, and each CTA writes its own part:
+ *     x read once, no workspace (qknr_gn_workspace_bytes reports 0), no CTA
+ *     waits outside its cluster.  Needs cluster launch support and groups
+ *     whose parts fit 200 KB of shared memory at 16 CTAs (about 1.6 M
+ *     elements); a CTA's copy wait is bounded like the fused path's.
  *
- * QKNR_GN_AUTO takes the fused path when this device and shape allow it
- * and piece_elems and l2_batch_bytes are 0 (they tune the two-pass path),
- * else the two-pass path; it also falls back to the two-pass path when the
- * cooperative launch does not fit the SMs the context may use.  Both give the same bits when the two-pass
- * pieces are 12288 elements.
+ * QKNR_GN_AUTO, when piece_elems and l2_batch_bytes are 0 (they tune the
+ * two-pass path), takes the cluster path for groups of at most 512 KB
+ * (parts of at most 32 KB) where the device can place the clusters, else
+ * the fused path when this device and shape allow it, else the two-pass
+ * path; it also falls back to the two-pass path when the cooperative
+ * launch does not fit the SMs the context may use.  The fused and two-pass
+ * paths give the same bits when the two-pass pieces are 12288 elements;
+ * the cluster path sums in other parts, so its bits differ from theirs
+ * within the same tolerance (and equal them when one CTA holds a group).
  *
  * Ownership and errors follow qknr.h: the caller owns every buffer
  * (activations, gamma, beta and the workspace); the library allocates
@@ -78,13 +90,13 @@ typedef struct qknr_gn_args {
   int32_t groups;             /* G, divides C */
   const float *gamma, *beta;  /* device fp32 [C] */
   float eps;                  /* default 1e-6 */
-  void *workspace;            /* device, 16-byte aligned, qknr_gn_workspace_bytes() */
+  void *workspace;            /* device, 16-byte aligned, qknr_gn_workspace_bytes() (NULL when 0) */
   size_t workspace_bytes;
   int32_t piece_elems;        /* elements per piece (multiple of 8); 0 = about 1024 pieces in all, >= 65536 each */
   int64_t l2_batch_bytes;     /* activation bytes per batch of groups; 0 or -1 = one batch */
   int32_t *dev_status;        /* optional device int32: the fused path writes QKNR_ERR_TIMEOUT
                                  here when one of its waits runs out (see qknr.h) */
-  int32_t mode;               /* QKNR_GN_AUTO, QKNR_GN_FUSED or QKNR_GN_TWO_PASS */
+  int32_t mode;               /* QKNR_GN_AUTO, QKNR_GN_FUSED, QKNR_GN_TWO_PASS or QKNR_GN_CLUSTER */
   uint32_t flags;             /* QKNR_FLAG_TEST_STALL, QKNR_GN_FLAG_TEST_NO_RECORDS (tests only) */
   uint64_t wait_limit_ns;     /* bound of each wait of the fused path; 0 = 2 s */
 } qknr_gn_args;
@@ -94,8 +106,9 @@ void qknr_gn_args_init(qknr_gn_args *a);
 
 /* Device workspace the call needs for these arguments: 16 bytes per piece
    and one more per group of each sample, plus 16 bytes for the fused path
-   (in QKNR_GN_AUTO the larger of the two paths' needs).  Depends on the
-   arguments only, not on the device. */
+   (in QKNR_GN_AUTO the larger of the two paths' needs, since it may fall
+   back to either); 0 in QKNR_GN_CLUSTER, where workspace may be NULL.
+   Depends on the arguments only, not on the device. */
 qknr_status qknr_gn_workspace_bytes(const qknr_gn_args *args, size_t *bytes);
 
 /* Validate and launch on `stream` (asynchronous). */
@@ -104,7 +117,9 @@ qknr_status qknr_gn_silu_forward(const qknr_gn_args *args, qknr_stream_t stream)
 /* Validate and describe the launch without launching: for the fused path
    the grid, block, shared memory, ring slots (stages) and piece bytes
    (stage_bytes); for the two-pass path the apply kernel's grid (pieces x
-   groups of a batch) and block.  Queries the current device. */
+   groups of a batch) and block; for the cluster path the grid, block,
+   shared memory and part bytes, with the CTAs per cluster in `kernel`.
+   Queries the current device. */
 qknr_status qknr_gn_query(const qknr_gn_args *args, qknr_launch_info *info);
 
 /* sizeof(qknr_gn_args) as compiled into the library. */
@@ -133,8 +148,9 @@ size_t qknr_gn_sizeof_args(void);
  * on.  Every call on a device shares the one array, and
  * nothing in it needs clearing: the two-pass path reads only what the same
  * call wrote, and the fused path accepts only statistics tagged with its
- * own call's tag.  Calls whose kernels overlap on the GPU (different
- * streams, no ordering between them) race on the array.
+ * own call's tag; the cluster path does not touch it.  Calls whose kernels
+ * overlap on the GPU (different streams, no ordering between them) race on
+ * the array, except on the cluster path.
  */
 #define QKNR_GN_NOALLOC_SCRATCH_BYTES (1 << 20)
 qknr_status qknr_gn_silu_forward_noalloc(const qknr_gn_args *args, qknr_stream_t stream);
