@@ -48,7 +48,8 @@
  *
  * QKNR_GN_AUTO, when piece_elems and l2_batch_bytes are 0 (they tune the
  * two-pass path), takes the cluster path for groups of at most 512 KB
- * (parts of at most 32 KB) where the device can place the clusters, else
+ * (parts of at most 32 KB) when the device can place all the call's
+ * clusters at once, else
  * the fused path when this device and shape allow it, else the two-pass
  * path; it also falls back to the two-pass path when the cooperative
  * launch does not fit the SMs the context may use.  The fused and two-pass

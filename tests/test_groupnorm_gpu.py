@@ -340,6 +340,22 @@ def test_cluster_path_needs_no_workspace():
     compare(to_bits(x), ref, "bf16", "no workspace")
 
 
+def test_many_groups_take_the_fused_path():
+    # 256 groups of 512 KB: their clusters of 16 do not all fit at once, so
+    # the automatic choice is the fused path; the cluster path still runs
+    # when asked for
+    w = I.GroupNormWorkload("many", 8, 512, 128, 128, groups=32, seed=49)
+    assert query(w)["kernel"].startswith("gn_fused<bf16>")
+    cl = query(w, mode="cluster")
+    assert cl["kernel"].startswith("gn_cluster<bf16>, clusters of 16 CTAs"), cl
+    inp = I.make_gn_inputs(w)
+    res, _ = run(w, inp, mode="cluster")
+    g = np.random.Generator(np.random.PCG64(19))
+    idx = tuple(g.integers(0, s_, 4000) for s_ in (w.n, w.c, w.h, w.w))
+    ref = G.group_norm_silu_at(inp["x"], w.dtype, w.groups, inp["gamma"], inp["beta"], w.eps, idx)
+    compare(to_bits(res)[idx], ref, w.dtype, "many groups, cluster path")
+
+
 def test_cluster_path_rejects_groups_too_large():
     w = I.GN_WORKLOADS["gn_vae_1x256x512x512"]             # 4 MB groups: 256 KB parts at 16 CTAs
     with pytest.raises(Q.QknrError) as e:

@@ -4,6 +4,8 @@ fused kernel stages in shared memory), ragged H*W, dtypes, value scale and
 offset, in place / out of place; the fused path is also checked bit for bit
 against the two-pass path with pieces of the same size, and groups that fit a
 cluster also go through the cluster path (the automatic choice for them)."""
+import re
+
 import numpy as np
 import pytest
 import torch
@@ -71,8 +73,16 @@ def test_random_group_norm(seed):
     x = to_dev(inp["x"], w.dtype)
     out = torch.empty_like(x) if out_of_place else None
     L = (w.c // w.groups) * w.h * w.w
-    info = Q.gn_query(Q.gn_args(x, w.groups, torch.ones(w.c, device="cuda"), torch.ones(w.c, device="cuda")))
-    assert info["kernel"].startswith("gn_cluster" if cluster_auto(L) else "gn_fused"), info
+    ones = torch.ones(w.c, device="cuda")
+    info = Q.gn_query(Q.gn_args(x, w.groups, ones, ones))
+    # the automatic choice: the cluster path for small groups whose clusters
+    # all fit on the GPU at once (the query reports how many fit)
+    auto_cluster = False
+    if cluster_auto(L):
+        resident = int(re.search(r"(\d+) resident", Q.gn_query(Q.gn_args(x, w.groups, ones, ones,
+                                                                          mode="cluster"))["kernel"]).group(1))
+        auto_cluster = w.n * w.groups <= resident
+    assert info["kernel"].startswith("gn_cluster" if auto_cluster else "gn_fused"), info
     res = call(x, w, inp, out=out, mode="fused")
     two = call(to_dev(inp["x"], w.dtype), w, inp, mode="two_pass", piece_elems=FUSED_PIECE)
     torch.cuda.synchronize()
@@ -86,7 +96,7 @@ def test_random_group_norm(seed):
         cl = call(xc, w, inp, out=torch.empty_like(xc) if out_of_place else None, mode="cluster")
         auto = call(to_dev(inp["x"], w.dtype), w, inp)
         torch.cuda.synchronize()
-        if cluster_auto(L):
+        if auto_cluster:
             assert torch.equal(cl.view(torch.int16), auto.view(torch.int16)), w
         if out_of_place:
             np.testing.assert_array_equal(to_bits(xc), inp["x"])
