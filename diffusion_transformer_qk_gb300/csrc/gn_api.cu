@@ -244,6 +244,7 @@ struct ClusterLaunch {
   const void* fn = nullptr;
   int cluster = 0;            // CTAs per cluster (per group of a sample)
   long long part_len = 0;     // elements per CTA
+  int threads = 0;            // per CTA
   int grid = 0;
   int smem = 0;
   int regs = 0;
@@ -267,8 +268,9 @@ qknr_status one_wave(const qknr_gn_args* a, const GnPlan& pl, ClusterLaunch* cl)
 }
 
 qknr_status cluster_launch(const qknr_gn_args* a, const GnPlan& pl, ClusterLaunch* cl) {
-  cl->fn = a->dtype == QKNR_BF16 ? reinterpret_cast<const void*>(&qknr::gn_cluster_kernel<__nv_bfloat16>)
-                                 : reinterpret_cast<const void*>(&qknr::gn_cluster_kernel<__half>);
+  cl->fn = a->dtype == QKNR_BF16 ? reinterpret_cast<const void*>(&qknr::gn_cluster_kernel<__nv_bfloat16, 256>)
+                                 : reinterpret_cast<const void*>(&qknr::gn_cluster_kernel<__half, 256>);
+  cl->threads = 256;
   if (!pl.cluster_shape) {
     snprintf(cl->why, sizeof(cl->why), "a group does not fit a cluster");
     return QKNR_OK;
@@ -299,7 +301,7 @@ qknr_status cluster_launch(const qknr_gn_args* a, const GnPlan& pl, ClusterLaunc
   // per kernel, device, size and shared memory
   static std::mutex mu;
   static std::map<std::tuple<const void*, int, int, int>, int> resident;
-  const auto key = std::make_tuple(cl->fn, dev, cl->cluster, cl->smem);
+  const auto key = std::make_tuple(cl->fn, dev, cl->cluster, cl->smem);   // fn fixes the threads
   {
     std::lock_guard<std::mutex> lk(mu);
     auto it = resident.find(key);
@@ -325,7 +327,7 @@ qknr_status cluster_launch(const qknr_gn_args* a, const GnPlan& pl, ClusterLaunc
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.gridDim = dim3(static_cast<unsigned>(pl.spans * cl->cluster));
-  cfg.blockDim = dim3(qknr::kGncThreads);
+  cfg.blockDim = dim3(static_cast<unsigned>(cl->threads));
   cfg.dynamicSmemBytes = static_cast<size_t>(cl->smem);
   cfg.attrs = attr;
   cfg.numAttrs = 1;
@@ -512,7 +514,7 @@ qknr_status launch_cluster(const qknr_gn_args* a, const GnPlan& pl, const Cluste
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.gridDim = dim3(static_cast<unsigned>(cl.grid));
-  cfg.blockDim = dim3(qknr::kGncThreads);
+  cfg.blockDim = dim3(static_cast<unsigned>(cl.threads));
   cfg.dynamicSmemBytes = static_cast<size_t>(cl.smem);
   cfg.stream = s;
   cfg.attrs = attr;
@@ -610,11 +612,11 @@ qknr_status qknr_gn_query(const qknr_gn_args* args, qknr_launch_info* info) {
     if (st != QKNR_OK) return st;
     if (cl.ok) {
       info->grid = cl.grid;
-      info->block = qknr::kGncThreads;
+      info->block = cl.threads;
       info->dyn_smem = cl.smem;
       info->stages = 1;
       info->ctas_per_sm = 0;
-      info->consumer_warps = qknr::kGncThreads / 32;
+      info->consumer_warps = cl.threads / 32;
       info->stage_bytes = static_cast<int32_t>(cl.part_len * 2);
       info->registers = cl.regs;
       info->num_sms = cl.num_sms;

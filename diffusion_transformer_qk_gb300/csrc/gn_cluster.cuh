@@ -26,19 +26,19 @@
 
 namespace qknr {
 
-constexpr int kGncThreads = kGnThreads;          // 256: the block piece_moments merges over
+constexpr int kGncMaxThreads = 1024;
 constexpr int kGncOffFull = 0;                   // mbarrier of the part's copies
 constexpr int kGncOffBad = 8;                    // int: this CTA's part is not usable
 constexpr int kGncOffIssued = 12;                // int: the part's copies were issued
 constexpr int kGncOffK = 16;                     // the group's first 16 bytes
-constexpr int kGncOffRed = 64;                   // [2 * kGnWarps] floats
-constexpr int kGncOffPart = 128;                 // this CTA's part: mean - K, sum of squared deviations
-constexpr int kGncOffCoef = 144;                 // m1, rstd, K, and 1.0 when the cluster skips its writes
-constexpr int kGncOffData = 256;                 // the part's elements
+constexpr int kGncOffPart = 32;                  // this CTA's part: mean - K, sum of squared deviations
+constexpr int kGncOffCoef = 48;                  // m1, rstd, K, and 1.0 when the cluster skips its writes
+constexpr int kGncOffRed = 64;                   // [2 * warps] floats
+constexpr int kGncOffData = 384;                 // the part's elements
 constexpr unsigned kGncCopyBytes = 32768;        // bytes per bulk copy
 constexpr int kGncMaxCluster = 16;
-static_assert(kGncOffRed + 8 * kGnWarps <= kGncOffPart, "shared memory map");
-static_assert(kGncOffCoef + 16 <= kGncOffData, "shared memory map");
+static_assert(kGncOffRed + 8 * (kGncMaxThreads / 32) <= kGncOffData, "shared memory map");
+static_assert(kGncOffData % 128 == 0, "shared memory map");
 
 struct GnClusterParams {
   const char* x;
@@ -98,6 +98,29 @@ __device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t local, unsigned rank
   return v;
 }
 
+// The part of a CTA of NT threads from the threads' parts, as piece_moments
+// (the same order for NT = 256): an xor tree in each warp, then thread 0
+// merges the warps' parts in order.  Valid in thread 0.
+template <int NT>
+__device__ __forceinline__ Moments part_moments(const Moments& mine, int nvec, float* red) {
+  constexpr int kWarps = NT / 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const Moments wp = warp_moments(mine, warp_count(warp, nvec, NT, 8));
+  if (lane == 0) {
+    red[warp] = wp.u;
+    red[kWarps + warp] = wp.m;
+  }
+  __syncthreads();
+  Moments t{0.0f, 0.0f, 0.0f};
+  if (threadIdx.x == 0) {
+    const float r = red[0];                      // warp 0 holds values whenever the part does
+    RefSums sums;
+    for (int w = 0; w < kWarps; ++w) sums.add(Moments{warp_count(w, nvec, NT, 8), red[w], red[kWarps + w]}, r);
+    t = merged(8.0f * static_cast<float>(nvec), r, sums);
+  }
+  return t;
+}
+
 // Elements of part `rank` of a group of L elements in parts of `part`.
 __device__ __forceinline__ long long part_elems(unsigned rank, long long part, long long L) {
   const long long lo = static_cast<long long>(rank) * part;
@@ -105,8 +128,8 @@ __device__ __forceinline__ long long part_elems(unsigned rank, long long part, l
   return hi > lo ? hi - lo : 0;
 }
 
-template <typename T>
-__global__ void __launch_bounds__(kGncThreads, 1) gn_cluster_kernel(const __grid_constant__ GnClusterParams p) {
+template <typename T, int NT>
+__global__ void __launch_bounds__(NT, 1) gn_cluster_kernel(const __grid_constant__ GnClusterParams p) {
   extern __shared__ __align__(128) unsigned char smem[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -161,7 +184,7 @@ __global__ void __launch_bounds__(kGncThreads, 1) gn_cluster_kernel(const __grid
   }
   const bool ok = __syncthreads_and(got) != 0;
 
-  // this part's statistics around K: thread t sums vectors t, t + 256, ...
+  // this part's statistics around K: thread t sums vectors t, t + NT, ...
   // in batches of kGnBatch around each batch's first value, as the two-pass
   // statistics kernel does over a piece
   float K = 0.0f;
@@ -174,11 +197,11 @@ __global__ void __launch_bounds__(kGncThreads, 1) gn_cluster_kernel(const __grid
   float tn = 0.0f, tr = 0.0f;
   RefSums ts;
   if (ok) {
-    for (int v0 = threadIdx.x; v0 < nvec; v0 += kGncThreads * kGnBatch) {
+    for (int v0 = threadIdx.x; v0 < nvec; v0 += NT * kGnBatch) {
       uint4 v[kGnBatch];
 #pragma unroll
       for (int b = 0; b < kGnBatch; ++b) {
-        const int k = v0 + b * kGncThreads;
+        const int k = v0 + b * NT;
         v[b] = k < nvec ? *reinterpret_cast<const uint4*>(data + k * 16) : make_uint4(0, 0, 0, 0);
       }
       float2 f[4];
@@ -189,7 +212,7 @@ __global__ void __launch_bounds__(kGncThreads, 1) gn_cluster_kernel(const __grid
       float nb = 0.0f;
 #pragma unroll
       for (int b = 0; b < kGnBatch; ++b) {
-        if (v0 + b * kGncThreads < nvec) {
+        if (v0 + b * NT < nvec) {
           float2 X[4];
           Elem<T>::unpack(v[b], X);
 #pragma unroll
@@ -208,7 +231,7 @@ __global__ void __launch_bounds__(kGncThreads, 1) gn_cluster_kernel(const __grid
     }
   }
   const Moments mine = tn == 0.0f ? Moments{0.0f, 0.0f, 0.0f} : merged(tn, tr, ts);
-  const Moments pm = piece_moments(mine, ok ? nvec : 0, red, CtaSync());
+  const Moments pm = part_moments<NT>(mine, ok ? nvec : 0, red);
   if (threadIdx.x == 0) {
     part[0] = pm.u;
     part[1] = pm.m;
@@ -255,7 +278,7 @@ __global__ void __launch_bounds__(kGncThreads, 1) gn_cluster_kernel(const __grid
     const unsigned hw = static_cast<unsigned>(p.hw);
     unsigned ch_end = 0;
     float2 A = make_float2(0.0f, 0.0f), B = make_float2(0.0f, 0.0f);
-    for (int v = threadIdx.x; v < nvec && out_ok; v += kGncThreads) {
+    for (int v = threadIdx.x; v < nvec && out_ok; v += NT) {
       const unsigned e = static_cast<unsigned>(lo) + static_cast<unsigned>(v) * 8u;   // < L < 2^31
       if (e >= ch_end) {
         const unsigned cl = e / hw;
