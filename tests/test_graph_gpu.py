@@ -46,6 +46,40 @@ def test_qk_norm_rope_replays_in_a_cuda_graph():
     assert torch.equal(qkv.view(torch.int16), ref.view(torch.int16))
 
 
+def test_chain_of_calls_with_the_prefetch_replays_in_a_cuda_graph():
+    # three in-place calls in a row, each reading the previous output, after a
+    # copy kernel that writes the input: captured, the calls keep their
+    # programmatic dependent launch (graph edges) and the L2 prefetch before
+    # each wait (64 rows per CTA), and a replay gives the eager bits
+    w = I.WORKLOADS["wan_32760x40x128"]
+    T = 9728
+    a = I.make_inputs(w, tokens=T)
+    gq, gk = torch.from_numpy(a["gamma_q"]).cuda(), torch.from_numpy(a["gamma_k"]).cuda()
+    cos, sin = torch.from_numpy(a["cos"]).cuda(), torch.from_numpy(a["sin"]).cuda()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    src = to_dev(a["qkv"], "bf16")
+    assert Q.query(Q.packed_args(src, 40, 40, 40, 128, gq, gk, cos, sin))["prefetch_rows"] > 0
+    ref = src.clone()
+    for _ in range(3):
+        Q.qk_norm_rope_packed(ref, 40, 40, 40, 128, gq, gk, cos, sin, flags=Q.FLAG_NO_OVERLAP)
+    qkv = torch.zeros_like(src)
+    Q.qk_norm_rope_packed(qkv.clone(), 40, 40, 40, 128, gq, gk, cos, sin, dev_status=status)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            torch.bitwise_or(src.view(torch.int16), 0, out=qkv.view(torch.int16))
+            for _ in range(3):
+                Q.qk_norm_rope_packed(qkv, 40, 40, 40, 128, gq, gk, cos, sin, dev_status=status)
+    for _ in range(2):
+        qkv.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        assert torch.equal(qkv.view(torch.int16), ref.view(torch.int16))
+
+
 def test_adaln_replays_in_a_cuda_graph():
     w = I.ADALN_WORKLOADS["adaln_flux2_2x4608x6144"]
     a = I.make_adaln_inputs(w, tokens=3000)
