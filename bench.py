@@ -574,10 +574,9 @@ class AdaLNRunner:
 
 class GroupNormRunner:
     """Device buffers and arguments of a VAE group-norm + SiLU workload.  One
-    step is one call: on the fused path a memset of the workspace counters
-    and one launch; on the two-pass path two launches (statistics, apply)
-    per batch of groups.  The caller-owned workspace is allocated once
-    here."""
+    step is one call: one launch on the fused or the cluster path, two
+    launches (statistics, apply) per batch of groups on the two-pass path.
+    The caller-owned workspace is allocated once here."""
 
     def __init__(self, w, dev, tune, status, tokens=None):
         import re
@@ -603,8 +602,8 @@ class GroupNormRunner:
         self.outputs = ["x"]
         self.pipe = None
         self.info = Q.gn_query(a)
-        if self.info["kernel"].startswith("gn_fused"):
-            self.launches_per_call = 1             # the memset is not a kernel of ours
+        if self.info["kernel"].startswith(("gn_fused", "gn_cluster")):
+            self.launches_per_call = 1
         else:
             m = re.search(r" x(\d+),", self.info["kernel"])
             self.launches_per_call = 2 * (int(m.group(1)) if m else 1)

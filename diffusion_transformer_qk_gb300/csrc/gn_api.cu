@@ -1,6 +1,7 @@
 // C-ABI launcher of the group-norm + SiLU kernels: validation, the choice
-// between the fused and the two-pass path, piece and batch planning, and
-// the launches.  No allocation, no synchronisation.
+// between the cluster, fused and two-pass paths, the cluster split, piece
+// and batch planning, and the launches.  No allocation, no
+// synchronisation.
 #include <cuda_runtime.h>
 
 #include <atomic>

@@ -107,8 +107,9 @@ void qknr_gn_args_init(qknr_gn_args *a);
 
 /* Device workspace the call needs for these arguments: 16 bytes per piece
    and one more per group of each sample, plus 16 bytes for the fused path
-   (in QKNR_GN_AUTO the larger of the two paths' needs, since it may fall
-   back to either); 0 in QKNR_GN_CLUSTER, where workspace may be NULL.
+   (in QKNR_GN_AUTO the larger of the fused and two-pass paths' needs,
+   since it may fall back to either); 0 in QKNR_GN_CLUSTER, where workspace
+   may be NULL.
    Depends on the arguments only, not on the device. */
 qknr_status qknr_gn_workspace_bytes(const qknr_gn_args *args, size_t *bytes);
 
