@@ -70,7 +70,7 @@ def test_adaln_nonfinite_stays_in_its_row():
     np.testing.assert_array_equal(dirty[others], clean[others])
 
 
-@pytest.mark.parametrize("mode", ["fused", "two_pass"])
+@pytest.mark.parametrize("mode", ["fused", "two_pass", "cluster"])
 def test_group_norm_nonfinite_stays_in_its_group(mode):
     w = I.GroupNormWorkload("n", 2, 64, 96, 96, groups=32, seed=62)
     inp = I.make_gn_inputs(w)

@@ -59,12 +59,13 @@ def test_gn_stress(seed):
     gamma = (float(g.choice([1.0, -2.0, 0.3])) * (1 + 0.1 * g.standard_normal(c))).astype(np.float32)
     beta = (float(g.choice([0.0, 0.5, -3.0])) + 0.1 * g.standard_normal(c)).astype(np.float32)
     eps = float(g.choice([1e-6, 1e-3]))
-    mode = str(g.choice(["fused", "two_pass"]))
-    res = Q.group_norm_silu(to_dev(xb, dtype), groups, torch.from_numpy(gamma).cuda(), torch.from_numpy(beta).cuda(),
-                            eps=eps, mode=mode)
-    torch.cuda.synchronize()
+    g.choice(["fused", "two_pass"])                  # (kept so the seeds draw what they always drew)
     ref = G.group_norm_silu(xb, dtype, groups, gamma, beta, eps)
-    compare_ulps(to_bits(res), ref, dtype, BOUND[dtype], f"gn {dtype} {kind} {mode} {(n, c, h, w_)} G{groups}")
+    for mode in ("fused", "two_pass", "cluster"):
+        res = Q.group_norm_silu(to_dev(xb, dtype), groups, torch.from_numpy(gamma).cuda(),
+                                torch.from_numpy(beta).cuda(), eps=eps, mode=mode)
+        torch.cuda.synchronize()
+        compare_ulps(to_bits(res), ref, dtype, BOUND[dtype], f"gn {dtype} {kind} {mode} {(n, c, h, w_)} G{groups}")
 
 
 @pytest.mark.parametrize("seed", range(100))
