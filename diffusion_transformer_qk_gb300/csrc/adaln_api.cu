@@ -178,6 +178,13 @@ qknr_status plan(const qknr_adaln_args* a, AdaPlan* pl, bool size_device) {
   kp.consumer_warps = warps;
   kp.group_warps = gw;
   kp.stages = stages;
+  // Before its dependency wait each CTA asks L2 for its first four rows of
+  // x (sweeps on GB300 against none: Wan 107.0 -> 106.6 us back to back,
+  // FLUX.2 45.2 -> 44.9 us flushed and 39.9 -> 38.7 us back to back; two,
+  // six or eight rows about the same, the whole first ring fill of 16 rows
+  // or the second fill slower on Wan and flushed)
+  const bool no_prefetch = (a->flags & (QKNR_FLAG_NO_OVERLAP | QKNR_FLAG_NO_PREFETCH)) != 0;
+  kp.prefetch_rows = no_prefetch ? 0 : 4;
   pl->grid = static_cast<int>(grid);
   pl->block = block;
   pl->smem = static_cast<int>(smem);
@@ -224,6 +231,7 @@ qknr_status qknr_adaln_query(const qknr_adaln_args* args, qknr_launch_info* info
   info->group_warps = pl.group_warps;
   info->registers = pl.regs;
   info->num_sms = pl.num_sms;
+  info->prefetch_rows = pl.kp.prefetch_rows;
   return QKNR_OK;
 }
 

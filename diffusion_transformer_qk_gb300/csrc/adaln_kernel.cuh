@@ -75,6 +75,7 @@ struct AdaLNParams {
   unsigned row_bytes;                             // C * 2
   unsigned stage_bytes;
   unsigned smem_bytes;                            // dynamic shared memory of the launch
+  int prefetch_rows;                              // first rows of the CTA prefetched into L2 before the wait
   // address spans of the buffers (checked builds test every access against them)
   MemSpan sp_x, sp_out, sp_scale, sp_shift;
 };
@@ -129,8 +130,16 @@ __global__ void __launch_bounds__(kAdaMaxThreads, 1) adaln_kernel(const __grid_c
     fence_barrier_init();
   }
   __syncthreads();
-  // all global memory accesses come after the previous kernel in the stream
-  // has completed (programmatic dependent launch; see the QK kernel)
+  // All global memory accesses come after the previous kernel in the stream
+  // has completed (programmatic dependent launch; see the QK kernel).  Only
+  // L2 prefetches of the CTA's first p.prefetch_rows rows of x go before the
+  // wait: they deliver no data, and the copies after the wait that hit them
+  // see the previous kernel's writes.
+  if (!kChecked && warp == NW && lane == 0) {
+    long long row = blockIdx.x;
+    for (int i = 0; i < p.prefetch_rows && row < p.tokens; ++i, row += gridDim.x)
+      bulk_prefetch_l2(p.x + row * p.x_stride, p.row_bytes);
+  }
   grid_dependency_wait();
   const unsigned long long limit = p.wait_limit_ns;
 

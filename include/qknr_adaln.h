@@ -61,7 +61,11 @@ void qknr_adaln_args_init(qknr_adaln_args *a);
 
 /* Validate and launch on `stream` (asynchronous).  Base addresses, row and
    sample strides must be 16-byte aligned; `out` must not partially overlap
-   x, scale or shift. */
+   x, scale or shift.  Launched like qknr_forward (programmatic dependent
+   launch unless flags has QKNR_FLAG_NO_OVERLAP); before its wait for the
+   previous kernel each CTA only asks L2 to prefetch its first four rows of
+   x (QKNR_FLAG_NO_PREFETCH skips that; qknr_launch_info.prefetch_rows
+   reports it). */
 qknr_status qknr_adaln_forward(const qknr_adaln_args *args, qknr_stream_t stream);
 
 /* Validate and describe the launch without launching. */

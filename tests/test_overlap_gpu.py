@@ -166,6 +166,30 @@ def test_adaln_chain_matches_plain_launches():
     compare(outs[0][0], ref, w.dtype, "AdaLN")
 
 
+def test_adaln_call_sees_the_writes_of_the_kernel_before_it():
+    # a torch kernel writes x; the in-place AdaLN call right after it, which
+    # asks L2 for its first rows before its dependency wait, must read the
+    # new bits; and QKNR_FLAG_NO_PREFETCH gives the same bits
+    w = I.ADALN_WORKLOADS["adaln_flux2_2x4608x6144"]
+    inp = I.make_adaln_inputs(w, tokens=3000)
+    sc, sh = to_dev(inp["scale"], w.mod_dtype), to_dev(inp["shift"], w.mod_dtype)
+    src = to_dev(inp["x"], w.dtype)
+    info = Q.adaln_query(Q.adaln_args(src, sc, sh, rows_per_batch=w.seq, eps=w.eps))
+    assert info["prefetch_rows"] > 0
+    assert Q.adaln_query(Q.adaln_args(src, sc, sh, rows_per_batch=w.seq, eps=w.eps,
+                                      flags=Q.FLAG_NO_PREFETCH))["prefetch_rows"] == 0
+    plain = src.clone()
+    Q.adaln_modulate(plain, sc, sh, rows_per_batch=w.seq, eps=w.eps, flags=Q.FLAG_NO_OVERLAP)
+    for flags in (0, Q.FLAG_NO_PREFETCH):
+        for _ in range(3):
+            x = torch.full_like(src, 3.0)
+            torch.cuda.synchronize()
+            torch.bitwise_or(src.view(torch.int16), 0, out=x.view(torch.int16))
+            Q.adaln_modulate(x, sc, sh, rows_per_batch=w.seq, eps=w.eps, flags=flags)
+            torch.cuda.synchronize()
+            assert torch.equal(x.view(torch.int16), plain.view(torch.int16))
+
+
 def test_calls_right_after_a_cooperative_group_norm_launch():
     # the fused group norm is a cooperative launch; the QK and AdaLN calls
     # launched right after it (programmatic dependent launch) read what it
