@@ -1,4 +1,6 @@
-// Group norm + SiLU with one thread-block cluster per group.
+// Group norm + SiLU with one thread-block cluster per group ("fused qknorm
+// rope Flux 2.0", section "Not in this PR — follow-ups", names the VAE's
+// group_norm_silu; the operation is restated in include/qknr_gn.h).
 //
 // When a group's (C/G)*H*W elements fit in the shared memory of a cluster
 // of CTAs (up to 16 on GB300), the group is split into equal parts, one
